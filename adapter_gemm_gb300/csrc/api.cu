@@ -1,0 +1,418 @@
+// Host side of the C ABI declared in include/lora_gb300.h: argument checks,
+// workspace carving, tensor-map encoding, launch configuration and dispatch.
+// The library allocates no device memory; every buffer comes from the caller.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include "lora_gb300.h"
+#include "kernels.h"
+
+namespace lora {
+
+// Dynamic shared memory limits already raised, per device and kernel slot.
+cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes) {
+    static std::mutex mu;
+    static size_t done[64][4] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || slot < 0 || slot >= 4)
+        return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev][slot] >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done[dev][slot] = bytes;
+    return e;
+}
+
+}  // namespace lora
+
+using namespace lora;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int num_sms() {
+    static int cache[kMaxDevices] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// 2-D bf16 tensor [outer, inner] (row-major, row pitch inner*2 bytes) tiled in
+// boxes of box_outer rows x box_inner columns, 128-byte swizzle, zero fill
+// outside the tensor.
+bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool valid_sizes(int S, int R_max, int d_in) {
+    return S >= 1 && S <= kMaxSlots && R_max >= 8 && R_max <= kMaxRank && (R_max % 8) == 0 &&
+           d_in >= 8 && (d_in % 8) == 0;
+}
+
+int max_tiles_for(int T, int S) { return (T + kTileRows - 1) / kTileRows + S; }
+
+bool plan_needs_xsorted(int T) { return T > kSkinnyMaxT; }
+
+// Sub-buffer sizes of the plan workspace, in carve order.
+void plan_layout(int T, int S, int R_max, int d_in_cap, size_t sizes[11]) {
+    const int mt = max_tiles_for(T, S);
+    sizes[0] = (size_t)T * 4;                 // slot_of_token
+    sizes[1] = (size_t)T * 4;                 // token_order
+    sizes[2] = (size_t)S * 4;                 // counts
+    sizes[3] = (size_t)(S + 1) * 4;           // indptr
+    sizes[4] = (size_t)S * 4;                 // active
+    sizes[5] = 4;                             // n_active
+    sizes[6] = (size_t)mt * 16;               // tiles
+    sizes[7] = 4;                             // n_tiles
+    sizes[8] = 4;                             // n_invalid
+    sizes[9] = (size_t)T * R_max * 4;         // U
+    sizes[10] = plan_needs_xsorted(T) ? (size_t)T * d_in_cap * 2 : 0;   // x_sorted
+}
+
+struct SkinnyConfig { int TN, stages, ks, occ; };
+
+SkinnyConfig skinny_config(int T, int K, int N) {
+    SkinnyConfig c;
+    const int Tt = T < kSkinnyMaxT ? T : kSkinnyMaxT;
+    c.TN = ((Tt + 15) / 16) * 16;
+    if (c.TN < 16) c.TN = 16;
+    const size_t stage = (size_t)128 * 64 * 2 + (size_t)c.TN * 64 * 2;
+    if (skinny_smem_bytes(c.TN, 4) <= 113 * 1024) {
+        c.stages = 4;
+        c.occ = 2;
+    } else {
+        c.stages = (int)((200 * 1024) / stage);
+        if (c.stages > 6) c.stages = 6;
+        if (c.stages < 2) c.stages = 2;
+        c.occ = 1;
+    }
+    const int units = ((N + 127) / 128) * ((T + c.TN - 1) / c.TN);
+    const int kb = (K + 63) / 64;
+    const int cap = num_sms() * c.occ;
+    c.ks = 1;
+    while (c.ks < 8 && units * c.ks * 2 <= cap && kb >= c.ks * 2) c.ks *= 2;
+    // every split must own at least one K block
+    while (c.ks > 1) {
+        const int per = (kb + c.ks - 1) / c.ks;
+        if ((c.ks - 1) * per < kb) break;
+        c.ks /= 2;
+    }
+    return c;
+}
+
+cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+int shrink_splits(int max_tiles, int K) {
+    const int cap = 2 * num_sms();
+    int ks = 1;
+    while (ks < 8 && max_tiles * ks * 2 <= cap && K / (ks * 2) >= 256) ks *= 2;
+    return ks;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lora_version(void) { return 1; }
+
+const char* lora_strerror(lora_status s) {
+    switch (s) {
+        case LORA_OK: return "ok";
+        case LORA_EINVAL: return "invalid argument (null or misaligned pointer, bad size)";
+        case LORA_ESLOT: return "slot out of range (slot 0 is the zero adapter and cannot be installed)";
+        case LORA_ERANK: return "rank out of range";
+        case LORA_ESHAPE: return "shapes of x, W, pool and plan do not agree";
+        case LORA_ENONFINITE: return "adapter factor holds NaN or Inf";
+        case LORA_ECUDA: return "CUDA runtime call or launch failed";
+        case LORA_EIDRANGE: return "token slot ids outside [0, S) were seen";
+        case LORA_ESPACE: return "workspace too small";
+        case LORA_ETIMEOUT: return "a kernel gave up a bounded wait";
+    }
+    return "unknown status";
+}
+
+size_t lora_plan_workspace_bytes(int T, int S, int R_max, int d_in_cap) {
+    if (T < 0 || !valid_sizes(S, R_max, d_in_cap)) return 0;
+    size_t sizes[11];
+    plan_layout(T, S, R_max, d_in_cap, sizes);
+    size_t total = 0;
+    for (int i = 0; i < 11; ++i) total += align_up(sizes[i], 256);
+    return total;
+}
+
+lora_status lora_plan_init(lora_plan_t* plan, void* workspace, size_t bytes, int T, int S, int R_max,
+                           int d_in_cap) {
+    if (!plan || !workspace || T < 0) return LORA_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LORA_EINVAL;
+    if (S < 1 || S > kMaxSlots) return LORA_ESLOT;
+    if (R_max < 8 || R_max > kMaxRank || (R_max % 8) != 0) return LORA_ERANK;
+    if (d_in_cap < 8 || (d_in_cap % 8) != 0) return LORA_ESHAPE;
+    const size_t need = lora_plan_workspace_bytes(T, S, R_max, d_in_cap);
+    if (bytes < need) return LORA_ESPACE;
+    size_t sizes[11];
+    plan_layout(T, S, R_max, d_in_cap, sizes);
+    uint8_t* p = static_cast<uint8_t*>(workspace);
+    void* ptrs[11];
+    for (int i = 0; i < 11; ++i) {
+        ptrs[i] = sizes[i] ? p : nullptr;
+        p += align_up(sizes[i], 256);
+    }
+    plan->slot_of_token = static_cast<int32_t*>(ptrs[0]);
+    plan->token_order = static_cast<int32_t*>(ptrs[1]);
+    plan->counts = static_cast<int32_t*>(ptrs[2]);
+    plan->indptr = static_cast<int32_t*>(ptrs[3]);
+    plan->active = static_cast<int32_t*>(ptrs[4]);
+    plan->n_active = static_cast<int32_t*>(ptrs[5]);
+    plan->tiles = static_cast<int32_t*>(ptrs[6]);
+    plan->n_tiles = static_cast<int32_t*>(ptrs[7]);
+    plan->n_invalid = static_cast<int32_t*>(ptrs[8]);
+    plan->U = static_cast<float*>(ptrs[9]);
+    plan->x_sorted = ptrs[10];
+    plan->T = T;
+    plan->S = S;
+    plan->R_max = R_max;
+    plan->d_in_cap = d_in_cap;
+    plan->max_tiles = max_tiles_for(T, S);
+    return LORA_OK;
+}
+
+lora_status lora_pool_init(lora_pool* pool, void* A, void* B, float* scale, int32_t* rank, int32_t* work,
+                           int S, int R_max, int d_in, int d_out, void* stream) {
+    if (!pool || !A || !B || !scale || !rank || !work) return LORA_EINVAL;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(scale) || !aligned16(rank)) return LORA_EINVAL;
+    if (S < 1 || S > kMaxSlots) return LORA_ESLOT;
+    if (R_max < 8 || R_max > kMaxRank || (R_max % 8) != 0) return LORA_ERANK;
+    if (d_in < 8 || d_out < 8 || (d_in % 8) != 0 || (d_out % 8) != 0) return LORA_ESHAPE;
+    pool->A = A;
+    pool->B = B;
+    pool->scale = scale;
+    pool->rank = rank;
+    pool->work = work;
+    pool->S = S;
+    pool->R_max = R_max;
+    pool->d_in = d_in;
+    pool->d_out = d_out;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(A, 0, (size_t)S * R_max * d_in * 2, st) != cudaSuccess ||
+        cudaMemsetAsync(B, 0, (size_t)S * d_out * R_max * 2, st) != cudaSuccess ||
+        cudaMemsetAsync(scale, 0, (size_t)S * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(rank, 0, (size_t)S * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(work, 0, 16, st) != cudaSuccess)
+        return LORA_ECUDA;
+    return LORA_OK;
+}
+
+lora_status lora_pool_install(lora_pool* pool, int slot, const void* A, const void* B, float alpha, int rank,
+                              void* stream) {
+    if (!pool || !A || !B || !pool->A || !pool->B || !pool->scale || !pool->rank || !pool->work)
+        return LORA_EINVAL;
+    if (slot <= 0 || slot >= pool->S) return LORA_ESLOT;
+    if (rank < 1 || rank > pool->R_max) return LORA_ERANK;
+    if (!aligned16(A) || !aligned16(B)) return LORA_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int K = pool->d_in, N = pool->d_out, R = pool->R_max;
+    // Validate before writing: count non-finite values of both factors.
+    if (cudaMemsetAsync(pool->work, 0, 4, st) != cudaSuccess) return LORA_ECUDA;
+    if (launch_count_nonfinite(static_cast<const __nv_bfloat16*>(A), (size_t)rank * K, pool->work, st) != cudaSuccess ||
+        launch_count_nonfinite(static_cast<const __nv_bfloat16*>(B), (size_t)N * rank, pool->work, st) != cudaSuccess)
+        return LORA_ECUDA;
+    int32_t bad = 0;
+    if (cudaMemcpyAsync(&bad, pool->work, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return LORA_ECUDA;
+    if (bad != 0) return LORA_ENONFINITE;
+    // Zero the slot's padded block, then copy the factors into its leading rows/columns.
+    uint8_t* Aslot = static_cast<uint8_t*>(pool->A) + (size_t)slot * R * K * 2;
+    uint8_t* Bslot = static_cast<uint8_t*>(pool->B) + (size_t)slot * N * R * 2;
+    const float scale = alpha / (float)rank;
+    const int32_t rk = rank;
+    if (cudaMemsetAsync(Aslot, 0, (size_t)R * K * 2, st) != cudaSuccess ||
+        cudaMemsetAsync(Bslot, 0, (size_t)N * R * 2, st) != cudaSuccess ||
+        cudaMemcpyAsync(Aslot, A, (size_t)rank * K * 2, cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+        cudaMemcpy2DAsync(Bslot, (size_t)R * 2, B, (size_t)rank * 2, (size_t)rank * 2, (size_t)N,
+                          cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(pool->rank + slot, &rk, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(pool->scale + slot, &scale, 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return LORA_ECUDA;
+    return LORA_OK;
+}
+
+lora_status lora_plan(const int32_t* ids, int T, lora_plan_t* plan, void* stream) {
+    if (!plan || T < 0) return LORA_EINVAL;
+    if (T != plan->T) return LORA_ESHAPE;
+    if (T > 0 && !ids) return LORA_EINVAL;
+    if (!plan->token_order || !plan->indptr || !plan->tiles) return LORA_EINVAL;
+    PlanArgs p;
+    p.slot_of_token = plan->slot_of_token;
+    p.token_order = plan->token_order;
+    p.counts = plan->counts;
+    p.indptr = plan->indptr;
+    p.active = plan->active;
+    p.n_active = plan->n_active;
+    p.tiles = plan->tiles;
+    p.n_tiles = plan->n_tiles;
+    p.n_invalid = plan->n_invalid;
+    p.S = plan->S;
+    return launch_plan(ids, T, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK : LORA_ECUDA;
+}
+
+lora_status lora_plan_check(const lora_plan_t* plan, void* stream, int32_t* n_invalid_out) {
+    if (!plan || !plan->n_invalid) return LORA_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, plan->n_invalid, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return LORA_ECUDA;
+    if (n_invalid_out) *n_invalid_out = v;
+    return v ? LORA_EIDRANGE : LORA_OK;
+}
+
+int lora_linear_path(int T, int d_in, int d_out) {
+    (void)d_in;
+    (void)d_out;
+    return T <= kSkinnyMaxT ? 0 : 1;
+}
+
+lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out, const lora_pool* pool,
+                        const lora_plan_t* plan, void* y, void* stream) {
+    if (T < 0 || d_in < 8 || d_out < 8) return LORA_EINVAL;
+    if ((d_in % 8) != 0 || (d_out % 8) != 0) return LORA_ESHAPE;
+    if (T == 0) return LORA_OK;
+    if (!x || !W || !y) return LORA_EINVAL;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y)) return LORA_EINVAL;
+    if (plan) {
+        if (!pool || !pool->A || !pool->B || !pool->rank || !pool->scale) return LORA_EINVAL;
+        if (plan->T != T || plan->S != pool->S || plan->R_max != pool->R_max || pool->d_in != d_in ||
+            pool->d_out != d_out || d_in > plan->d_in_cap)
+            return LORA_ESHAPE;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int path = lora_linear_path(T, d_in, d_out);
+    if (plan && path == 1 && !plan->x_sorted) return LORA_ESHAPE;
+
+    if (plan) {
+        ShrinkArgs sa;
+        sa.x = static_cast<const __nv_bfloat16*>(x);
+        sa.A = static_cast<const __nv_bfloat16*>(pool->A);
+        sa.scale = pool->scale;
+        sa.rank = pool->rank;
+        sa.token_order = plan->token_order;
+        sa.tiles = reinterpret_cast<const int4*>(plan->tiles);
+        sa.n_tiles = plan->n_tiles;
+        sa.U = plan->U;
+        sa.x_sorted = path == 1 ? static_cast<__nv_bfloat16*>(plan->x_sorted) : nullptr;
+        sa.T = T;
+        sa.K = d_in;
+        sa.R_max = pool->R_max;
+        sa.ks = shrink_splits(plan->max_tiles, d_in);
+        if (launch_shrink(sa, plan->max_tiles, true, st) != cudaSuccess) return LORA_ECUDA;
+    }
+
+    ExpandArgs ex;
+    ex.slot_of_token = plan ? plan->slot_of_token : nullptr;
+    ex.U = plan ? plan->U : nullptr;
+    ex.B = plan ? static_cast<const __nv_bfloat16*>(pool->B) : nullptr;
+    ex.rank = plan ? pool->rank : nullptr;
+    ex.R_max = plan ? pool->R_max : 0;
+
+    if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_start, st) != cudaSuccess) return LORA_ECUDA;
+    if (path == 0) {
+        const SkinnyConfig c = skinny_config(T, d_in, d_out);
+        CUtensorMap tmW, tmX;
+        if (!make_tmap(&tmW, W, (uint64_t)d_in, (uint64_t)d_out, 64, 128) ||
+            !make_tmap(&tmX, x, (uint64_t)d_in, (uint64_t)T, 64, (uint32_t)c.TN))
+            return LORA_ECUDA;
+        SkinnyArgs a;
+        a.y = static_cast<__nv_bfloat16*>(y);
+        a.ex = ex;
+        a.T = T;
+        a.K = d_in;
+        a.N = d_out;
+        a.TN = c.TN;
+        a.kb_total = (d_in + 63) / 64;
+        a.ks = c.ks;
+        a.stages = c.stages;
+        if (launch_skinny(tmW, tmX, a, true, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
+    } else {
+        const void* A = plan ? plan->x_sorted : x;
+        CUtensorMap tmA, tmB;
+        if (!make_tmap(&tmA, A, (uint64_t)d_in, (uint64_t)T, 64, 128) ||
+            !make_tmap(&tmB, W, (uint64_t)d_in, (uint64_t)d_out, 64, 256))
+            return LORA_ECUDA;
+        WideArgs a;
+        a.y = static_cast<__nv_bfloat16*>(y);
+        a.token_order = plan ? plan->token_order : nullptr;
+        a.ex = ex;
+        a.T = T;
+        a.K = d_in;
+        a.N = d_out;
+        a.m_tiles = (T + 127) / 128;
+        a.n_tiles = (d_out + 255) / 256;
+        a.kb_total = (d_in + 63) / 64;
+        int grid = a.m_tiles * a.n_tiles;
+        if (grid > num_sms()) grid = num_sms();
+        if (launch_wide(tmA, tmB, a, true, grid, st) != cudaSuccess) return LORA_ECUDA;
+    }
+    if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;
+    return LORA_OK;
+}
+
+lora_status lora_profile_gemm_events(void* start, void* stop) {
+    if ((start == nullptr) != (stop == nullptr)) return LORA_EINVAL;
+    g_prof_start = static_cast<cudaEvent_t>(start);
+    g_prof_stop = static_cast<cudaEvent_t>(stop);
+    return LORA_OK;
+}
+
+lora_status lora_last_device_error(int32_t* code_out) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ECUDA;
+    int a = 0, b = 0;
+    if (skinny_take_error(&a) != cudaSuccess || wide_take_error(&b) != cudaSuccess) return LORA_ECUDA;
+    const int v = a ? a : b;
+    if (code_out) *code_out = v;
+    return v ? LORA_ETIMEOUT : LORA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Internal interface between the host entry points (api.cu) and the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace lora {
+
+constexpr int kTileRows = 16;       // plan work tiles, rows (== LORA_TILE_ROWS)
+constexpr int kMaxSlots = 1024;     // one plan thread per slot in the scans
+constexpr int kMaxRank = 128;       // R_max cap: shrink keeps R_max/8 MMA column tiles
+constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 256)
+
+struct PlanArgs {
+    int32_t* slot_of_token;
+    int32_t* token_order;
+    int32_t* counts;
+    int32_t* indptr;
+    int32_t* active;
+    int32_t* n_active;
+    int32_t* tiles;
+    int32_t* n_tiles;
+    int32_t* n_invalid;
+    int S;
+};
+
+struct ShrinkArgs {
+    const __nv_bfloat16* x;      // [T, K]
+    const __nv_bfloat16* A;      // [S, R_max, K]
+    const float* scale;          // [S]
+    const int32_t* rank;         // [S]
+    const int32_t* token_order;  // [T]
+    const int4* tiles;           // [max_tiles] (slot, begin, end, 0)
+    const int32_t* n_tiles;      // [1]
+    float* U;                    // [T, R_max]
+    __nv_bfloat16* x_sorted;     // [T, K] or null
+    int T, K, R_max, ks;
+};
+
+// Epilogue operands shared by both GEMM kernels. slot_of_token == null means
+// base only (no correction anywhere).
+struct ExpandArgs {
+    const int32_t* slot_of_token;  // [T]
+    const float* U;                // [T, R_max]
+    const __nv_bfloat16* B;        // [S, N, R_max]
+    const int32_t* rank;           // [S]
+    int R_max;
+};
+
+struct SkinnyArgs {
+    __nv_bfloat16* y;  // [T, N]
+    ExpandArgs ex;
+    int T, K, N;
+    int TN;            // token columns per tile (multiple of 16, <= 256)
+    int kb_total;      // ceil(K / 64)
+    int ks;            // K splits = cluster size along y
+    int stages;
+};
+
+struct WideArgs {
+    __nv_bfloat16* y;               // [T, N]
+    const int32_t* token_order;     // [T] row of each plan position, or null (identity)
+    ExpandArgs ex;
+    int T, K, N;
+    int m_tiles, n_tiles, kb_total;
+};
+
+cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, cudaStream_t stream);
+cudaError_t launch_shrink(const ShrinkArgs& a, int max_tiles, bool pdl, cudaStream_t stream);
+cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyArgs& a,
+                          bool pdl, int num_sms, cudaStream_t stream);
+cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const WideArgs& a,
+                        bool pdl, int grid, cudaStream_t stream);
+cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);
+
+// Read and clear the bounded-wait error words of the GEMM translation units.
+cudaError_t skinny_take_error(int* code);
+cudaError_t wide_take_error(int* code);
+
+// Raise a kernel's dynamic shared memory limit once per device.
+cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
+
+// Shared-memory bytes the skinny kernel needs for a token tile of TN columns
+// and `stages` pipeline stages.
+size_t skinny_smem_bytes(int TN, int stages);
+
+}  // namespace lora

@@ -1,0 +1,171 @@
+// The per-step plan: a stable counting sort of token rows by adapter slot.
+//
+// What it produces is the metadata of the LoRA-serving page ("The metadata is
+// a sort and a unique, rebuilt every forward pass": token_indices_sorted_by_
+// lora_ids, num_tokens_per_lora, lora_token_start_loc, the active ids; worked
+// three-request example) in the mstar LoraAddressing shape (token_order plus a
+// CSR of slot ranges). The page computes it with torch.sort + torch.unique on
+// the host side of the launch; here one CTA builds it on the device, so the
+// step needs no host round trip.
+//
+// One CTA of 32 warps. Warp w owns a contiguous range of rows, so rows of
+// lower warps precede rows of higher warps, and inside a warp rows are taken
+// 32 at a time in order: the sort is stable by construction.
+//   pass 1: each warp counts its rows per slot (__match_any_sync groups lanes
+//           with equal slot; the group leader adds the group size);
+//   scan:   per slot, an exclusive prefix over warps; over slots, an
+//           exclusive prefix (segment starts = indptr);
+//   pass 2: each lane writes its row to indptr-based cursor + warp offset +
+//           rank among equal-slot lanes to its left.
+// Then the active-slot list and the work tiles (each slot's segment cut every
+// LORA_TILE_ROWS rows) come from two more prefix sums over slots.
+#include <cstdint>
+#include <cuda_runtime.h>
+#include "ptx.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanWarps = kPlanThreads / 32;
+
+// Exclusive block-wide prefix sum of one value per thread (1024 threads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += n;
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int t = warp_tot[lane];
+        int ti = t;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, ti, d);
+            if (lane >= d) ti += n;
+        }
+        warp_tot[lane] = ti - t;            // exclusive prefix of warp totals
+        if (lane == 31) warp_tot[32] = ti;  // grand total
+    }
+    __syncthreads();
+    const int r = warp_tot[warp] + inc - v;
+    total = warp_tot[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads, 1)
+plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
+    extern __shared__ int smem[];
+    const int S = p.S;
+    int* wc = smem;                       // [kPlanWarps][S] per-warp slot counts, then cursors
+    int* tot = smem + kPlanWarps * S;     // [S] per-slot totals
+    __shared__ int warp_tot[33];
+    __shared__ int s_invalid;
+
+    // The next kernel of the chain may start its prologue; it waits for this
+    // grid to finish before it reads the plan.
+    pdl_trigger();
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < kPlanWarps * S; i += kPlanThreads) wc[i] = 0;
+    if (tid == 0) s_invalid = 0;
+    __syncthreads();
+
+    // Rows [lo, hi) of this warp; chunk is a multiple of 32.
+    const int chunk = ((T + kPlanWarps * 32 - 1) / (kPlanWarps * 32)) * 32;
+    const int lo = min(T, warp * chunk), hi = min(T, lo + chunk);
+
+    int n_bad = 0;
+    for (int base = lo; base < hi; base += 32) {
+        const int t = base + lane;
+        const bool valid = t < hi;
+        int s = valid ? ids[t] : 0;
+        if (valid && (s < 0 || s >= S)) { ++n_bad; s = 0; }
+        if (valid) p.slot_of_token[t] = s;
+        const int key = valid ? s : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (valid && lane == __ffs(peers) - 1) wc[warp * S + s] += __popc(peers);
+        __syncwarp();
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) n_bad += __shfl_xor_sync(0xffffffffu, n_bad, d);
+    if (lane == 0 && n_bad) atomicAdd(&s_invalid, n_bad);
+    __syncthreads();
+
+    // Per slot: exclusive prefix over warps (in place) and the slot total.
+    for (int s = tid; s < S; s += kPlanThreads) {
+        int run = 0;
+        for (int w = 0; w < kPlanWarps; ++w) {
+            const int c = wc[w * S + s];
+            wc[w * S + s] = run;
+            run += c;
+        }
+        tot[s] = run;
+    }
+    __syncthreads();
+
+    // Segment starts: exclusive prefix over slots (S <= 1024: one slot per thread).
+    int total = 0;
+    const int my_cnt = tid < S ? tot[tid] : 0;
+    const int start = block_exclusive_scan(my_cnt, warp_tot, total);
+    if (tid < S) {
+        p.counts[tid] = my_cnt;
+        p.indptr[tid] = start;
+        for (int w = 0; w < kPlanWarps; ++w) wc[w * S + tid] += start;
+    }
+    if (tid == 0) p.indptr[S] = total;
+    __syncthreads();
+
+    // Pass 2: stable scatter of row ids.
+    for (int base = lo; base < hi; base += 32) {
+        const int t = base + lane;
+        const bool valid = t < hi;
+        int s = valid ? ids[t] : 0;
+        if (valid && (s < 0 || s >= S)) s = 0;
+        const int key = valid ? s : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (valid) {
+            const unsigned below = peers & ((1u << lane) - 1u);
+            p.token_order[wc[warp * S + s] + __popc(below)] = t;
+        }
+        __syncwarp();
+        if (valid && lane == __ffs(peers) - 1) wc[warp * S + s] += __popc(peers);
+        __syncwarp();
+    }
+
+    // Active adapter slots (s >= 1 with rows), ascending.
+    const int is_active = (tid >= 1 && tid < S && my_cnt > 0) ? 1 : 0;
+    int n_active = 0;
+    const int a_pos = block_exclusive_scan(is_active, warp_tot, n_active);
+    if (is_active) p.active[a_pos] = tid;
+
+    // Work tiles over every segment, slot 0 included.
+    const int n_t = tid < S ? (my_cnt + kTileRows - 1) / kTileRows : 0;
+    int n_tiles = 0;
+    const int t_pos = block_exclusive_scan(n_t, warp_tot, n_tiles);
+    for (int j = 0; j < n_t; ++j) {
+        const int b = start + j * kTileRows;
+        int4 tile = make_int4(tid, b, min(b + kTileRows, start + my_cnt), 0);
+        reinterpret_cast<int4*>(p.tiles)[t_pos + j] = tile;
+    }
+    if (tid == 0) {
+        *p.n_active = n_active;
+        *p.n_tiles = n_tiles;
+        *p.n_invalid = s_invalid;
+    }
+}
+
+cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, cudaStream_t stream) {
+    const size_t smem = sizeof(int) * (size_t)(kPlanWarps + 1) * p.S;
+    cudaError_t e = ensure_smem_attr((const void*)plan_kernel, 0, smem);
+    if (e != cudaSuccess) return e;
+    plan_kernel<<<1, kPlanThreads, smem, stream>>>(ids, T, p);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

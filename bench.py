@@ -1,0 +1,457 @@
+"""Benchmark of the multi-LoRA linear layer on one GB300 (or N replicas).
+
+A step is one pass of the whole hot path over one batch: the plan of the
+batch's token slot ids, then for every adapted target the layer (shrink +
+tensor-core GEMM with the fused expand). Default workload: the Llama-3-8B
+q_proj decode step (T=64 rows, 4096 -> 4096, 8 rank-16 adapters, 8 rows each).
+
+Prints one JSON line. `value` is tokens/s over all ranks with inputs resident
+in HBM; `e2e` is the same through the public API with inputs copied from
+pinned host memory and the outputs copied back inside the timed region;
+`roofline` rates the dominant kernel (the GEMM) against the measured peaks;
+`cpu_baseline` is the fp64 CPU oracle on a bounded sample of the same batch.
+
+Weight copies rotate between steps so the working set exceeds twice the L2.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tokens/s and % of roofline for base GEMM + multi-LoRA SGMV per linear layer"
+DEFAULT_CONFIG = "q_decode"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--no-graph", action="store_true", help="launch steps eagerly instead of replaying graphs")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--kernel-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def src_digest() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "adapter_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """dram read+write bytes per launch of the dominant kernel from a committed
+    ncu summary, if it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(config)
+    if not d or d.get("src_sha") != src_digest():
+        return None
+    return float(d["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thr = threading.Thread(target=self._read, daemon=True)
+            self.thr.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [r for t, r in self.rows if self.t0 is not None and self.t0 - 0.2 <= t <= (self.t1 or t) + 0.2]
+        use = inside or [self.rows[-1][1]]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            f = [v.strip() for v in r.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(use)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# --------------------------------------------------------------- oracle leg --
+
+def oracle_tokens_per_s(w, seconds: float):
+    """Time the CPU oracle, as it stands, on whole steps of the workload until
+    `seconds` of work is done; returns (tokens/s, threads, sample text)."""
+    from oracle import lora_oracle as O
+    from adapter_gemm_gb300 import workloads as WL
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [os.cpu_count()])
+    except ImportError:
+        threads = os.cpu_count()
+    prep = []
+    for t in w.targets:
+        x = WL.input_for(w, t).double().numpy()
+        prep.append((x, t.W.double().numpy(), t.A.double().numpy(), t.B.double().numpy(), t.rank, t.alpha))
+    T = w.T
+    # bounded sample: whole steps if one is cheap, else a subset of rows
+    rows = None
+    t0 = time.perf_counter()
+    x, W_, A_, B_, r_, a_ = prep[0]
+    O.lora_linear(x[:1], W_, A_, B_, r_, a_, w.ids[:1])
+    one_row = time.perf_counter() - t0
+    est_step = one_row * T * len(prep)
+    if est_step > seconds / 3:
+        n = max(1, int(T * (seconds / 3) / est_step))
+        rows = np.linspace(0, T - 1, n).astype(np.int64)
+    done_rows = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        for (x, W_, A_, B_, r_, a_) in prep:
+            O.lora_linear(x, W_, A_, B_, r_, a_, w.ids, rows=rows)
+        done_rows += T if rows is None else len(rows)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    what = "whole steps" if rows is None else f"{len(rows)} of {T} rows per step"
+    sample = f"{reps} x ({what}) of {w.name}, all {len(prep)} target(s), fp64 numpy/BLAS"
+    return done_rows / el, threads, sample
+
+
+# --------------------------------------------------------------- GPU leg ----
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    import torch
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+
+    from adapter_gemm_gb300 import build as B
+    B.build()
+    from adapter_gemm_gb300 import cost, lora as L, workloads as WL
+
+    w = WL.by_name(args.config)
+    T = w.T
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+
+    # ---- device copies: rotate weights so the working set exceeds 2x L2
+    per_copy = 0
+    for t in w.targets:
+        per_copy += t.W.numel() * 2 + t.A.numel() * 2 + t.B.numel() * 2
+    n_copies = max(2, int(np.ceil(2.0 * l2 / max(per_copy, 1))) + 1)
+    n_copies = min(n_copies, 64)
+
+    xs = {}
+    for t in w.targets:
+        k = id(WL.input_for(w, t))
+        if k not in xs:
+            xs[k] = WL.input_for(w, t).to(dev)
+    x_of = [xs[id(WL.input_for(w, t))] for t in w.targets]
+    ids = torch.from_numpy(w.ids).to(dev)
+    base_targets = []
+    for t in w.targets:
+        W = t.W.to(dev)
+        pool = L.Pool(w.S, w.R_max, t.d_in, t.d_out, device=dev)
+        pool.load_padded(t.A, t.B, t.rank, t.alpha)
+        base_targets.append((W, pool))
+    copies = [base_targets]
+    for _ in range(n_copies - 1):
+        c = []
+        for (W, pool) in base_targets:
+            p2 = L.Pool(w.S, w.R_max, pool.d_in, pool.d_out, device=dev)
+            p2.A.copy_(pool.A); p2.B.copy_(pool.B); p2.scale.copy_(pool.scale); p2.rank.copy_(pool.rank)
+            c.append((W.clone(), p2))
+        copies.append(c)
+    d_cap = max(t.d_in for t in w.targets)
+    plans = [L.Plan(T, w.S, w.R_max, d_cap, device=dev) for _ in range(n_copies)]
+    ys = [torch.empty((T, t.d_out), dtype=torch.bfloat16, device=dev) for t in w.targets]
+    torch.cuda.synchronize()
+
+    def step(i):
+        c = i % n_copies
+        plans[c].build(ids)
+        for j, (W, pool) in enumerate(copies[c]):
+            L.linear(x_of[j], W, pool, plans[c], ys[j])
+
+    launches_per_step = 1 + 2 * len(w.targets)
+
+    # ---- warmup (eager), then graphs of one step per copy
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    use_graph = not args.no_graph
+    graphs = []
+    if use_graph:
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            for c in range(n_copies):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=s):
+                    step(c)
+                graphs.append(g)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        for i in range(n_copies):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+
+    def run(i):
+        if use_graph:
+            graphs[i % n_copies].replay()
+        else:
+            step(i)
+
+    for i in range(args.warmup):
+        run(i)
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    e0.record()
+    for i in range(args.steps):
+        run(i)
+    e1.record()
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        dist.barrier()
+    clocks.stop()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tmax = torch.tensor([ms], device=dev)
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        ms = float(tmax.item())
+    ms_per_step = ms / args.steps
+    value = T * args.steps * world / (ms / 1e3)
+
+    # ---- dominant kernel: GEMM durations from events around each launch
+    ksteps = max(10, min(args.kernel_steps, args.steps))
+    per_target_ms = np.zeros(len(w.targets))
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in w.targets] for _ in range(ksteps)]
+    torch.cuda.synchronize()
+    for i in range(ksteps):
+        c = i % n_copies
+        plans[c].build(ids)
+        for j, (W, pool) in enumerate(copies[c]):
+            a, b = evs[i][j]
+            L.profile_gemm_events(a, b)
+            L.linear(x_of[j], W, pool, plans[c], ys[j])
+    L.profile_gemm_events(None, None)
+    torch.cuda.synchronize()
+    for i in range(ksteps):
+        for j in range(len(w.targets)):
+            a, b = evs[i][j]
+            per_target_ms[j] += a.elapsed_time(b)
+    per_target_ms /= ksteps
+    jdom = int(np.argmax(per_target_ms))
+    td = w.targets[jdom]
+    hbm, tf_burst, tf_sus, src = peaks()
+    gw = cost.gemm_kernel(T, td.d_in, td.d_out, w.ids, td.rank)
+    t_k = per_target_ms[jdom] / 1e3
+    _, bound = cost.roofline_time(gw, tf_sus, hbm)
+    if bound == "hbm":
+        achieved = gw.bytes / t_k / 1e9
+        peak, unit = hbm, "GB/s"
+    else:
+        achieved = gw.flops / t_k / 1e12
+        peak, unit = tf_sus, "TFLOP/s"
+    roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.config),
+            "kernel": "gemm_skinny_kernel" if L.linear_path(T, td.d_in, td.d_out) == 0 else "gemm_wide_kernel",
+            "target": td.name, "kernel_us": round(t_k * 1e6, 3),
+            "algorithmic_bytes": gw.bytes, "algorithmic_flops": gw.flops, "peak_source": src}
+    # whole-step roofline (all targets, every kernel): the spec fraction
+    t_roof = 0.0
+    for t in w.targets:
+        lw = cost.layer(T, t.d_in, t.d_out, w.ids, t.rank)
+        t_roof += cost.roofline_time(lw, tf_sus, hbm)[0]
+    step_frac = t_roof / (ms_per_step / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if rank == 0 or world > 1:
+        hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
+        hids = torch.from_numpy(w.ids).pin_memory()
+        hy = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
+        dx = {k: torch.empty_like(v) for k, v in xs.items()}
+        dids = torch.empty_like(ids)
+        keys = [id(WL.input_for(w, t)) for t in w.targets]
+        esteps = max(10, min(args.steps, 500))
+
+        def e2e_step(i):
+            c = i % n_copies
+            for k in hx:
+                dx[k].copy_(hx[k], non_blocking=True)
+            dids.copy_(hids, non_blocking=True)
+            plans[c].build(dids)
+            for j, (W, pool) in enumerate(copies[c]):
+                L.linear(dx[keys[j]], W, pool, plans[c], ys[j])
+                hy[j].copy_(ys[j], non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record()
+        for i in range(esteps):
+            e2e_step(i)
+        f1.record()
+        torch.cuda.synchronize()
+        ems = f0.elapsed_time(f1)
+        bi = sum(v.numel() * v.element_size() for v in hx.values()) + hids.numel() * 4
+        bo = sum(v.numel() * v.element_size() for v in hy)
+        e2e = {"value": round(T * esteps * world / (ems / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "steps": esteps}
+
+    assert L.last_device_error() == 0, "a kernel gave up a bounded wait"
+
+    cpu = None
+    if rank == 0 and world == 1:
+        v, cores, sample = oracle_tokens_per_s(w, args.cpu_seconds)
+        cpu = {"value": round(v, 2), "unit": "tokens/s", "cores": int(cores), "kind": "oracle", "sample": sample}
+
+    total_flops = sum(cost.layer(T, t.d_in, t.d_out, w.ids, t.rank).flops for t in w.targets)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; random-init weights and adapters)",
+        "config": {"workload": w.name, "T": T, "targets": [[t.name, t.d_in, t.d_out] for t in w.targets],
+                   "slots": w.S, "R_max": w.R_max, "parallelism": f"replicas x{world}",
+                   "l2": f"{n_copies} rotating weight/pool copies ({n_copies * per_copy / 2**20:.0f} MiB > 2x L2)",
+                   "launch": "CUDA graph per step" if use_graph else "eager"},
+        "tflops": round(total_flops / (ms_per_step / 1e3) / 1e12, 2),
+        "step_roofline_frac": round(step_frac, 4),
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank, world):
+    """The reference arm for this build is the CPU oracle, timed as it stands."""
+    if rank != 0:
+        return
+    from adapter_gemm_gb300 import workloads as WL
+    w = WL.by_name(args.config)
+    per = max(1.0, min(args.cpu_seconds, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_tokens_per_s(w, per / 4)
+    vals = []
+    t0 = time.perf_counter()
+    sample = cores = None
+    for _ in range(args.steps):
+        v, cores, sample = oracle_tokens_per_s(w, per)
+        vals.append(v)
+    el = time.perf_counter() - t0
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * el / max(1, args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "config": {"workload": w.name, "T": w.T},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": int(cores), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

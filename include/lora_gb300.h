@@ -1,0 +1,185 @@
+/*
+ * lora_gb300.h - C ABI of the multi-LoRA linear layer for GB300 (sm_103a).
+ *
+ * The layer. For token row t with adapter slot s = ids[t]:
+ *
+ *     y[t, :] = x[t, :] W^T + (alpha_s / r_s) (x[t, :] A_s^T) B_s^T
+ *
+ * ("Many adapters, one base-model batch", Chapter 43 of the inference.shantanugoel
+ * engine book: the per-row equation and "compute the base projection over all
+ * rows once, then shrink each row to its adapter's rank, expand, add"; the
+ * mlinterviewnotes LoRA-serving page: W [d_out, d_in], A [r, d_in], B [d_out, r]
+ * and the row-vector form x W^T + (alpha/r)(x A^T) B^T.) Slot 0 is the zero
+ * adapter (mstar lora.pool module docs): rows on slot 0 get the base output and
+ * no correction; the kernels skip them.
+ *
+ * Conventions shared by every entry point:
+ *  - bf16 means IEEE bfloat16 stored as 16-bit words; fp32 is IEEE float.
+ *  - All matrices are row-major and contiguous.
+ *  - "device" pointers are CUDA device memory of the current device; "host"
+ *    pointers are ordinary CPU memory.
+ *  - The library allocates no memory. The caller owns every buffer; the
+ *    lora_pool and lora_plan_t structs are views over the caller's memory.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - lora_plan and lora_linear are asynchronous and stream-ordered: they return
+ *    only errors the host can see before launching (bad arguments, launch
+ *    failures), never synchronise and never trap. lora_pool_install and
+ *    lora_plan_check synchronise their stream.
+ *  - Sizes: T >= 0 rows; d_in and d_out multiples of 8; 8 <= R_max <= 128,
+ *    a multiple of 8; 1 <= S <= 1024 slots. Every device pointer must be
+ *    16-byte aligned.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_EINVAL = -1,      /* null pointer, negative size, misaligned pointer */
+    LORA_ESLOT = -2,       /* slot out of range, or slot 0 given to install */
+    LORA_ERANK = -3,       /* rank < 1 or rank > R_max, or R_max unsupported */
+    LORA_ESHAPE = -4,      /* shapes of x / W / pool / plan do not agree */
+    LORA_ENONFINITE = -5,  /* adapter factor holds NaN or Inf; slot untouched */
+    LORA_ECUDA = -6,       /* a CUDA runtime call or launch failed */
+    LORA_EIDRANGE = -7,    /* lora_plan_check: ids outside [0, S) were seen */
+    LORA_ESPACE = -8,      /* workspace smaller than lora_plan_workspace_bytes */
+    LORA_ETIMEOUT = -9     /* a kernel gave up a bounded wait (see lora_last_device_error) */
+} lora_status;
+
+/* A slot pool for one adapted linear (the stacked A/B buffers of the vLLM
+ * LoRA-serving page; the AdapterBank buffers of Chapter 43). Slot s occupies
+ * A[s, :rank[s], :] and B[s, :, :rank[s]]; padding past the rank is zero.
+ *   A     [S, R_max, d_in]  bf16 device, unscaled
+ *   B     [S, d_out, R_max] bf16 device, unscaled
+ *   scale [S] fp32 device: alpha_s / rank_s (0 for slot 0 and empty slots)
+ *   rank  [S] int32 device: 0 for slot 0 and empty slots
+ *   work  [4] int32 device scratch used by lora_pool_install
+ */
+typedef struct {
+    void* A;
+    void* B;
+    float* scale;
+    int32_t* rank;
+    int32_t* work;
+    int32_t S, R_max, d_in, d_out;
+} lora_pool;
+
+/* The per-step plan (mstar LoraAddressing(token_order, slot_indptr); vLLM's
+ * sort + unique metadata). Built on the device by lora_plan from the step's
+ * token slot ids; every array lives in one caller-provided device workspace
+ * carved by lora_plan_init:
+ *   slot_of_token [T]     ids with out-of-range entries mapped to 0
+ *   token_order   [T]     row ids grouped by slot, slots ascending, rows
+ *                         ascending inside a slot (stable)
+ *   counts        [S]     rows per slot
+ *   indptr        [S+1]   exclusive prefix sum of counts (segment starts)
+ *   active        [S]     slots >= 1 with rows, ascending; n_active valid
+ *   tiles         [max_tiles][4] (slot, begin, end, 0): every slot's segment
+ *                         (slot 0 included) cut every LORA_TILE_ROWS rows,
+ *                         positions into token_order; n_tiles valid
+ *   n_active, n_tiles, n_invalid [1] each
+ *   U             [T, R_max] fp32: the shrink result of the last lora_linear
+ *                         call, row t = token t (scratch)
+ *   x_sorted      [T, d_in_cap] bf16: x rows in plan order (scratch, only for
+ *                         large T; NULL otherwise)
+ * A plan is only valid for the ids it was built from; rebuild it whenever the
+ * ids (or the slot an adapter sits in) change. lora_linear calls that share a
+ * plan share its scratch, so they must be ordered on one stream.
+ */
+#define LORA_TILE_ROWS 16
+typedef struct {
+    int32_t* slot_of_token;
+    int32_t* token_order;
+    int32_t* counts;
+    int32_t* indptr;
+    int32_t* active;
+    int32_t* n_active;
+    int32_t* tiles;
+    int32_t* n_tiles;
+    int32_t* n_invalid;
+    float* U;
+    void* x_sorted;
+    int32_t T, S, R_max, d_in_cap, max_tiles;
+} lora_plan_t;
+
+/* Bytes of device workspace a plan for T rows, S slots, rank cap R_max and
+ * inputs up to d_in_cap columns needs. 0 on invalid sizes. */
+size_t lora_plan_workspace_bytes(int T, int S, int R_max, int d_in_cap);
+
+/* Carve `workspace` (device, >= lora_plan_workspace_bytes, 256-byte aligned)
+ * into `plan`. Host only; launches nothing. */
+lora_status lora_plan_init(lora_plan_t* plan, void* workspace, size_t bytes,
+                           int T, int S, int R_max, int d_in_cap);
+
+/* Fill `pool` with the given views and zero all of it (every slot empty,
+ * rank 0, scale 0) on `stream`. Asynchronous. */
+lora_status lora_pool_init(lora_pool* pool, void* A, void* B, float* scale,
+                           int32_t* rank, int32_t* work, int S, int R_max,
+                           int d_in, int d_out, void* stream);
+
+/* Load one adapter into `slot` (Chapter 43, AdapterBank.load: validate before
+ * writing, refuse non-finite weights, zero the slot, copy).
+ *   A [rank, d_in] bf16 device, B [d_out, rank] bf16 device, unscaled.
+ * Refuses slot 0 or slot >= S (LORA_ESLOT), rank outside [1, R_max]
+ * (LORA_ERANK), null pointers (LORA_EINVAL) without writing anything; returns
+ * LORA_ENONFINITE, slot untouched, if A or B holds NaN/Inf. Otherwise zeroes
+ * the slot's padded block, copies the factors, sets rank[slot] = rank and
+ * scale[slot] = alpha / rank (fp32). Synchronises `stream`. */
+lora_status lora_pool_install(lora_pool* pool, int slot, const void* A,
+                              const void* B, float alpha, int rank, void* stream);
+
+/* Build the plan for this step from `ids` ([T] int32 device, T == plan->T):
+ * a one-CTA counting sort (warp match + scan), stable in row index. Ids outside
+ * [0, S) are counted in n_invalid and treated as slot 0. Asynchronous. */
+lora_status lora_plan(const int32_t* ids, int T, lora_plan_t* plan, void* stream);
+
+/* Synchronise `stream` and read n_invalid into *n_invalid_out (may be NULL).
+ * Returns LORA_EIDRANGE when it is nonzero. For tests and debugging. */
+lora_status lora_plan_check(const lora_plan_t* plan, void* stream, int32_t* n_invalid_out);
+
+/* The layer:
+ *   x [T, d_in] bf16 device, W [d_out, d_in] bf16 device (nn.Linear layout),
+ *   y [T, d_out] bf16 device, written once, round-to-nearest-even from fp32.
+ * plan == NULL (pool ignored) runs the base projection only, with the same
+ * kernels and tiling that a call with a plan uses for this (T, d_in, d_out).
+ * With a plan, pool->S == plan->S, pool->R_max == plan->R_max,
+ * pool->d_in == d_in <= plan->d_in_cap, pool->d_out == d_out, T == plan->T.
+ * Rows whose slot is 0, or whose slot has rank 0, get exactly the base result.
+ * Asynchronous; stream-ordered after the plan. W and the pool must not be
+ * written by work still running on the stream (the kernel starts streaming W
+ * before earlier kernels of the call chain finish). */
+lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out,
+                        const lora_pool* pool, const lora_plan_t* plan, void* y,
+                        void* stream);
+
+/* The kernel family lora_linear picks for these sizes: 0 = skinny (swap-AB,
+ * split-K across a thread-block cluster), 1 = wide (persistent 128x256 tiles). */
+int lora_linear_path(int T, int d_in, int d_out);
+
+/* Profiling hook: when both are non-NULL cudaEvent_t handles, every following
+ * lora_linear records `start` on its stream right before it launches the GEMM
+ * kernel and `stop` right after it, so the caller can time that kernel alone
+ * with cudaEventElapsedTime. (NULL, NULL) turns it off. Process-global; not
+ * for use while a stream is being captured. */
+lora_status lora_profile_gemm_events(void* start, void* stop);
+
+/* Error word written by kernels that gave up a bounded wait (0 = none), and
+ * reset it. Synchronises the device. */
+lora_status lora_last_device_error(int32_t* code_out);
+
+const char* lora_strerror(lora_status status);
+
+/* Library version, for diagnostics. */
+int lora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GB300_H */

@@ -1,0 +1,151 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports every
+function the header declares, and rejects bad arguments before touching the
+device."""
+import ctypes
+
+import pytest
+
+from adapter_gemm_gb300 import lora as L
+from adapter_gemm_gb300 import build as B
+
+OK, EINVAL, ESLOT, ERANK, ESHAPE, ESPACE = 0, -1, -2, -3, -4, -8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L._lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = L.header_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_strerror_and_version(lib):
+    assert lib.lora_version() >= 1
+    for code in L.STATUS:
+        assert lib.lora_strerror(code)
+    assert b"unknown" in lib.lora_strerror(42)
+
+
+def test_workspace_bytes(lib):
+    n = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)
+    assert n > 0 and n % 256 == 0
+    assert lib.lora_plan_workspace_bytes(4096, 17, 16, 4096) >= 4096 * 4096 * 2   # x_sorted
+    assert lib.lora_plan_workspace_bytes(64, 9, 16, 4096) < 4096 * 64 * 2        # no x_sorted
+    assert lib.lora_plan_workspace_bytes(-1, 9, 16, 4096) == 0
+    assert lib.lora_plan_workspace_bytes(64, 0, 16, 4096) == 0
+    assert lib.lora_plan_workspace_bytes(64, 2000, 16, 4096) == 0
+    assert lib.lora_plan_workspace_bytes(64, 9, 12, 4096) == 0      # R_max % 8
+    assert lib.lora_plan_workspace_bytes(64, 9, 256, 4096) == 0     # R_max > 128
+    assert lib.lora_plan_workspace_bytes(64, 9, 16, 100) == 0       # d_in % 8
+    assert lib.lora_plan_workspace_bytes(0, 9, 16, 4096) > 0        # empty batch is fine
+
+
+FAKE = 0x7f0000000000          # 256-aligned, never dereferenced on these paths
+
+
+def test_plan_init_carves_workspace(lib):
+    p = L.lora_plan_t()
+    n = lib.lora_plan_workspace_bytes(300, 17, 16, 4096)
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n, 300, 17, 16, 4096) == OK
+    ptrs = [p.slot_of_token, p.token_order, p.counts, p.indptr, p.active, p.n_active, p.tiles,
+            p.n_tiles, p.n_invalid, p.U, p.x_sorted]
+    assert all(q is not None and q % 256 == 0 for q in ptrs)
+    assert ptrs == sorted(ptrs) and len(set(ptrs)) == len(ptrs)
+    assert p.U + 300 * 16 * 4 <= p.x_sorted
+    assert p.x_sorted + 300 * 4096 * 2 <= FAKE + n
+    assert p.max_tiles == (300 + 15) // 16 + 17
+    # decode-sized plans carry no x_sorted
+    q = L.lora_plan_t()
+    m = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)
+    assert lib.lora_plan_init(ctypes.byref(q), FAKE, m, 64, 9, 16, 4096) == OK
+    assert q.x_sorted is None
+
+
+def test_plan_init_errors(lib):
+    p = L.lora_plan_t()
+    n = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)
+    assert lib.lora_plan_init(None, FAKE, n, 64, 9, 16, 4096) == EINVAL
+    assert lib.lora_plan_init(ctypes.byref(p), None, n, 64, 9, 16, 4096) == EINVAL
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE + 16, n, 64, 9, 16, 4096) == EINVAL
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n - 1, 64, 9, 16, 4096) == ESPACE
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n, 64, 0, 16, 4096) == ESLOT
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n, 64, 9, 0, 4096) == ERANK
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n, 64, 9, 16, 4095) == ESHAPE
+
+
+def _pool(S=4, R=8, K=256, N=256):
+    pl = L.lora_pool()
+    pl.A, pl.B, pl.scale, pl.rank, pl.work = FAKE, FAKE + 2**30, FAKE + 2**31, FAKE + 2**32, FAKE + 2**33
+    pl.S, pl.R_max, pl.d_in, pl.d_out = S, R, K, N
+    return pl
+
+
+def test_install_refuses_before_writing(lib):
+    pl = _pool()
+    st = None
+    assert lib.lora_pool_install(ctypes.byref(pl), 0, FAKE, FAKE, 16.0, 8, st) == ESLOT
+    assert lib.lora_pool_install(ctypes.byref(pl), 4, FAKE, FAKE, 16.0, 8, st) == ESLOT
+    assert lib.lora_pool_install(ctypes.byref(pl), -1, FAKE, FAKE, 16.0, 8, st) == ESLOT
+    assert lib.lora_pool_install(ctypes.byref(pl), 1, FAKE, FAKE, 16.0, 0, st) == ERANK
+    assert lib.lora_pool_install(ctypes.byref(pl), 1, FAKE, FAKE, 16.0, 9, st) == ERANK
+    assert lib.lora_pool_install(ctypes.byref(pl), 1, None, FAKE, 16.0, 8, st) == EINVAL
+    assert lib.lora_pool_install(ctypes.byref(pl), 1, FAKE, None, 16.0, 8, st) == EINVAL
+    assert lib.lora_pool_install(ctypes.byref(pl), 1, FAKE + 2, FAKE, 16.0, 8, st) == EINVAL
+    assert lib.lora_pool_install(None, 1, FAKE, FAKE, 16.0, 8, st) == EINVAL
+
+
+def test_pool_init_argument_errors(lib):
+    pl = L.lora_pool()
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE]
+    assert lib.lora_pool_init(ctypes.byref(pl), None, *args[1:], 4, 8, 256, 256, None) == EINVAL
+    assert lib.lora_pool_init(ctypes.byref(pl), *args, 0, 8, 256, 256, None) == ESLOT
+    assert lib.lora_pool_init(ctypes.byref(pl), *args, 4, 4, 256, 256, None) == ERANK
+    assert lib.lora_pool_init(ctypes.byref(pl), *args, 4, 8, 250, 256, None) == ESHAPE
+
+
+def test_linear_argument_errors(lib):
+    pl = _pool(S=9, R=16, K=4096, N=4096)
+    p = L.lora_plan_t()
+    n = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n, 64, 9, 16, 4096) == OK
+    x = W = y = FAKE
+    assert lib.lora_linear(x, W, -1, 4096, 4096, None, None, y, None) == EINVAL
+    assert lib.lora_linear(x, W, 64, 4095, 4096, None, None, y, None) == ESHAPE
+    assert lib.lora_linear(x, W, 64, 4096, 4100 - 1, None, None, y, None) == ESHAPE
+    assert lib.lora_linear(x, W, 0, 4096, 4096, None, None, y, None) == OK     # empty batch
+    assert lib.lora_linear(None, W, 64, 4096, 4096, None, None, y, None) == EINVAL
+    assert lib.lora_linear(x + 8, W, 64, 4096, 4096, None, None, y, None) == EINVAL
+    # plan / pool disagreements
+    assert lib.lora_linear(x, W, 63, 4096, 4096, ctypes.byref(pl), ctypes.byref(p), y, None) == ESHAPE
+    assert lib.lora_linear(x, W, 64, 4096, 4096, None, ctypes.byref(p), y, None) == EINVAL
+    pl2 = _pool(S=8, R=16, K=4096, N=4096)
+    assert lib.lora_linear(x, W, 64, 4096, 4096, ctypes.byref(pl2), ctypes.byref(p), y, None) == ESHAPE
+    pl3 = _pool(S=9, R=16, K=4096, N=1024)
+    assert lib.lora_linear(x, W, 64, 4096, 4096, ctypes.byref(pl3), ctypes.byref(p), y, None) == ESHAPE
+    # a wide-path call needs a plan that carries x_sorted
+    q = L.lora_plan_t()
+    m = lib.lora_plan_workspace_bytes(300, 9, 16, 4096)
+    assert lib.lora_plan_init(ctypes.byref(q), FAKE, m, 300, 9, 16, 4096) == OK
+    pl4 = _pool(S=9, R=16, K=8192, N=4096)
+    assert lib.lora_linear(x, W, 300, 8192, 4096, ctypes.byref(pl4), ctypes.byref(q), y, None) == ESHAPE
+
+
+def test_plan_argument_errors(lib):
+    p = L.lora_plan_t()
+    n = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n, 64, 9, 16, 4096) == OK
+    assert lib.lora_plan(FAKE, 63, ctypes.byref(p), None) == ESHAPE
+    assert lib.lora_plan(None, 64, ctypes.byref(p), None) == EINVAL
+    assert lib.lora_plan(FAKE, 64, None, None) == EINVAL
+
+
+def test_path_choice_depends_on_shape_only(lib):
+    assert lib.lora_linear_path(1, 4096, 4096) == 0
+    assert lib.lora_linear_path(256, 14336, 4096) == 0
+    assert lib.lora_linear_path(257, 4096, 4096) == 1
+    assert lib.lora_linear_path(4096, 4096, 14336) == 1

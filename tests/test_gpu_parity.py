@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, on the
+same seeded bf16 inputs. Plan arrays bit-exact; y within 2e-2 * (1 + |ref|);
+slot-0 rows bitwise equal to the GPU's own base-only run."""
+import numpy as np
+import pytest
+import torch
+
+from adapter_gemm_gb300 import lora as L
+from adapter_gemm_gb300 import workloads as WL
+from oracle import lora_oracle as O
+
+from _gpu_common import DeviceWorkload, assert_parity, f64, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from adapter_gemm_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+    assert L.last_device_error() == 0
+
+
+# ------------------------------------------------------------------ plan ----
+
+def _plan_case(ids, S):
+    T = len(ids)
+    plan = L.Plan(T, S, 8, 64, device=DEV)
+    plan.build(torch.tensor(np.asarray(ids, dtype=np.int32), device=DEV))
+    n_bad = plan.check()
+    ref = O.plan(ids, S, tile_rows=L.TILE_ROWS)
+    assert n_bad == ref["n_invalid"]
+    assert plan.n_invalid() == ref["n_invalid"]
+    assert plan.counts().cpu().tolist() == ref["counts"].tolist()
+    assert plan.indptr().cpu().tolist() == ref["indptr"].tolist()
+    assert plan.token_order().cpu().tolist() == ref["token_order"].tolist()
+    assert plan.slot_of_token().cpu().tolist() == ref["slot_of_token"].tolist()
+    assert plan.active().cpu().tolist() == ref["active"].tolist()
+    tiles = plan.tiles().cpu()[:, :3].tolist()
+    assert tiles == ref["tiles"].tolist()
+
+
+def test_plan_worked_example():
+    _plan_case([1] * 5 + [2] * 4 + [0] * 3, 3)
+
+
+@pytest.mark.parametrize("T,S,seed", [(0, 4, 0), (1, 2, 1), (31, 3, 2), (33, 5, 3), (64, 9, 4),
+                                      (1000, 17, 5), (1024, 1024, 6), (4096, 51, 7), (5000, 2, 8),
+                                      (70000, 300, 9)])
+def test_plan_random(T, S, seed):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(-2, S + 2, size=T)     # includes invalid ids
+    _plan_case(ids.tolist(), S)
+
+
+def test_plan_all_one_slot_and_sorted_runs():
+    _plan_case([3] * 777, 4)
+    _plan_case([0] * 100 + [1] * 100, 2)
+    _plan_case(sorted(np.random.default_rng(1).integers(0, 40, size=3000).tolist(), reverse=True), 40)
+
+
+# --------------------------------------------------------------- configs ----
+
+def _full_check(w, i=0):
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(i)
+    assert_parity(y, dw.oracle(i), w.name)
+    return dw, y
+
+
+def test_tiny_full():
+    _full_check(WL.tiny())
+
+
+def test_q_decode_full():
+    _full_check(WL.q_decode())
+
+
+def test_mixed_down_full():
+    _full_check(WL.mixed_down())
+
+
+def test_gateup_prefill_sampled():
+    w = WL.gateup_prefill()
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    rows = sample_rows(w.ids, 96)
+    assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(0, rows=rows), w.name)
+
+
+@pytest.mark.parametrize("T", WL.SWEEP_T)
+def test_layer_sweep(T):
+    w = WL.layer_sweep(T)
+    dw = DeviceWorkload(w, DEV)
+    rows = np.arange(T) if T <= 64 else sample_rows(w.ids, 48)
+    for i, t in enumerate(w.targets):
+        y = dw.run(i)
+        assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(i, rows=rows), f"{w.name}/{t.name}")
+
+
+# ------------------------------------------------------------ slot 0 rows ----
+
+@pytest.mark.parametrize("name", ["tiny", "q_decode", "mixed_down", "gateup_prefill", "layer_sweep_T512"])
+def test_slot0_rows_bitwise_equal_base_only(name):
+    w = WL.by_name(name)
+    dw = DeviceWorkload(w, DEV)
+    for i in range(min(2, len(w.targets))):
+        y = dw.run(i)
+        yb = dw.run(i, base_only=True)
+        slot0 = torch.as_tensor(w.ids == 0, device=DEV)
+        if slot0.any():
+            assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
+        # base-only run is itself the base projection
+        rows = np.arange(min(w.T, 16))
+        base = O.base_linear(f64(WL.input_for(w, w.targets[i])), f64(w.targets[i].W), rows=rows)
+        assert_parity(yb[: len(rows)], base, name + " base-only")
+
+
+# --------------------------------------------------------- exact integers ----
+
+@pytest.mark.parametrize("T,K,N,R", [(9, 16, 24, 8), (64, 64, 136, 8), (300, 64, 264, 8), (513, 32, 520, 16)])
+def test_integer_inputs_bit_exact(T, K, N, R):
+    """Small-integer inputs with power-of-two scales: every partial sum is exact
+    in fp32 and every output is an integer of magnitude <= 256, so the GPU must
+    equal the exact result bit for bit."""
+    rng = np.random.default_rng(T + K + N)
+    S = 5
+    ranks = [0, 1, 2, 2, 0]           # slot 4 stays empty (rank 0)
+    alpha = np.array([0.0, 1.0, 2.0, 4.0, 0.0], dtype=np.float32)    # scales 1, 1, 2
+    x = rng.integers(-1, 2, size=(T, K)).astype(np.float32)
+    W = rng.integers(-1, 2, size=(N, K)).astype(np.float32)
+    A = np.zeros((S, R, K), np.float32)
+    B = np.zeros((S, N, R), np.float32)
+    for s in range(1, S):
+        A[s, :ranks[s]] = rng.integers(-1, 2, size=(ranks[s], K))
+        B[s, :, :ranks[s]] = rng.integers(-1, 2, size=(N, ranks[s]))
+    ids = rng.integers(0, S, size=T).astype(np.int32)
+    ref = O.lora_linear(x, W, A, B, ranks, alpha, ids)
+    assert np.abs(ref).max() <= 256 and np.array_equal(ref, np.round(ref))
+    tgt = WL.Target("int", K, N, WL.to_bf16(W), WL.to_bf16(A), WL.to_bf16(B), np.array(ranks, np.int32), alpha)
+    w = WL.Workload("int", T, S, R, ids, WL.to_bf16(x), [tgt])
+    dw = DeviceWorkload(w, DEV)
+    y = f64(dw.run(0))
+    assert np.array_equal(y, ref)
+
+
+# ------------------------------------------------------------ ragged sizes ----
+
+RAGGED = [
+    # T, K, N, S, R_max
+    (1, 64, 8, 2, 8),
+    (5, 200, 72, 3, 8),
+    (17, 1000, 200, 6, 24),
+    (100, 4096, 520, 9, 64),
+    (256, 520, 1032, 33, 128),
+    (257, 200, 264, 4, 16),
+    (300, 1000, 520, 7, 24),
+    (700, 4104, 1288, 40, 64),
+    (1500, 2048, 776, 17, 128),
+]
+
+
+@pytest.mark.parametrize("T,K,N,S,R", RAGGED)
+def test_ragged_shapes(T, K, N, S, R):
+    w = WL.random_case(seed=T * 7 + K, T=T, K=K, N=N, S=S, R_max=R)
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    rows = np.arange(T) if T <= 400 else sample_rows(w.ids, 200)
+    assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(0, rows=rows), f"ragged {T},{K},{N}")
+    slot0 = torch.as_tensor(w.ids == 0, device=DEV)
+    yb = dw.run(0, base_only=True)
+    assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
+
+
+# ---------------------------------------------------------- wiring & edges ----
+
+def test_perturbing_a_slot_changes_exactly_its_rows():
+    """Reinstall slot s with a different B: rows on s change, no other row does."""
+    w = WL.layer_sweep(64, targets=WL.LLAMA3_8B_TARGETS[:1])
+    dw = DeviceWorkload(w, DEV)
+    y0 = dw.run(0)
+    t = w.targets[0]
+    for s in (int(w.ids[3]), int(w.ids[-1])):
+        if s == 0:
+            continue
+        r = int(t.rank[s])
+        A = t.A[s, :r].to(DEV).contiguous()
+        Bn = (t.B[s, :, :r].float() * -1.5).to(torch.bfloat16).to(DEV).contiguous()
+        dw.targets[0].pool.install(s, A, Bn, float(t.alpha[s]))
+        y1 = dw.run(0)
+        changed = (y1.view(torch.int16) != y0.view(torch.int16)).any(dim=1).cpu().numpy()
+        assert np.array_equal(changed, w.ids == s), s
+        dw.targets[0].pool.install(s, A, t.B[s, :, :r].to(DEV).contiguous(), float(t.alpha[s]))
+        assert torch.equal(dw.run(0).view(torch.int16), y0.view(torch.int16))
+
+
+def test_every_active_slot_contributes():
+    w = WL.layer_sweep(512, targets=WL.LLAMA3_8B_TARGETS[:1])
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    yb = dw.run(0, base_only=True)
+    differs = (y.view(torch.int16) != yb.view(torch.int16)).any(dim=1).cpu().numpy()
+    for s in np.unique(w.ids):
+        if s > 0:
+            assert differs[w.ids == s].all(), s
+
+
+def test_runs_are_deterministic():
+    for w in (WL.mixed_down(), WL.layer_sweep(512, targets=WL.LLAMA3_8B_TARGETS[4:5])):
+        dw = DeviceWorkload(w, DEV)
+        a = dw.run(0)
+        b = dw.run(0)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_invalid_ids_are_counted_and_get_base_rows():
+    w = WL.random_case(seed=11, T=80, K=256, N=128, S=4, R_max=8)
+    w.ids[[0, 7, 50]] = [-1, 4, 1000]
+    dw = DeviceWorkload(w, DEV)
+    assert dw.plan.check() == 3
+    y = dw.run(0)
+    assert_parity(y, dw.oracle(0), "invalid ids")
+    yb = dw.run(0, base_only=True)
+    for r in (0, 7, 50):
+        assert torch.equal(y[r].view(torch.int16), yb[r].view(torch.int16))
+
+
+def test_empty_batch_and_all_base_rows():
+    W = torch.randn(64, 128, device=DEV).to(torch.bfloat16)
+    pool = L.Pool(3, 8, 128, 64, device=DEV)
+    plan = L.Plan(0, 3, 8, 128, device=DEV).build(torch.empty(0, dtype=torch.int32, device=DEV))
+    y = L.linear(torch.empty(0, 128, dtype=torch.bfloat16, device=DEV), W, pool, plan)
+    assert y.shape == (0, 64)
+    x = torch.randn(40, 128, device=DEV).to(torch.bfloat16)
+    plan = L.Plan(40, 3, 8, 128, device=DEV).build(torch.zeros(40, dtype=torch.int32, device=DEV))
+    assert plan.n_active() == 0
+    y = L.linear(x, W, pool, plan)
+    yb = L.linear(x, W)
+    assert torch.equal(y.view(torch.int16), yb.view(torch.int16))
+
+
+def test_install_refuses_non_finite_and_keeps_slot():
+    pool = L.Pool(3, 8, 64, 32, device=DEV)
+    A = torch.randn(4, 64, device=DEV).to(torch.bfloat16)
+    B = torch.randn(32, 4, device=DEV).to(torch.bfloat16)
+    pool.install(1, A, B, 8.0)
+    before = (pool.A.clone(), pool.B.clone(), pool.rank.clone(), pool.scale.clone())
+    bad = B.clone()
+    bad[3, 1] = float("nan")
+    with pytest.raises(L.LoraError) as e:
+        pool.install(1, A, bad, 8.0)
+    assert e.value.name == "LORA_ENONFINITE"
+    bad = A.clone()
+    bad[0, 0] = float("inf")
+    with pytest.raises(L.LoraError):
+        pool.install(1, bad, B, 8.0)
+    for t0, t1 in zip(before, (pool.A, pool.B, pool.rank, pool.scale)):
+        assert torch.equal(t0, t1)
+    # a smaller reinstall zeroes the old padding
+    pool.install(1, A[:2].contiguous(), B[:, :2].contiguous(), 4.0)
+    assert int(pool.rank[1]) == 2 and float(pool.scale[1]) == 2.0
+    assert pool.A[1, 2:].abs().sum() == 0 and pool.B[1, :, 2:].abs().sum() == 0
+
+
+def test_row_offsets_beyond_int32():
+    """T * d_in > 2^31 elements: row offsets must be 64-bit everywhere
+    (the LoRA-serving page's long-context int32 overflow)."""
+    T, K, N, S, R = 150_000, 14_336, 64, 3, 8
+    assert T * K > 2**31
+    w = WL.random_case(seed=5, T=256, K=K, N=N, S=S, R_max=R)   # adapters and W only
+    t = w.targets[0]
+    g = torch.Generator(device=DEV).manual_seed(3)
+    x = torch.randn(T, K, device=DEV, generator=g).to(torch.bfloat16)
+    ids_np = np.random.default_rng(4).integers(0, S, size=T).astype(np.int32)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    Wd = t.W.to(DEV)
+    pool = L.Pool(S, R, K, N, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    plan = L.Plan(T, S, R, K, device=DEV).build(ids)
+    y = L.linear(x, Wd, pool, plan)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, T // 2, T - 2, T - 1, 149_000, 100_001])
+    xr = f64(x[torch.as_tensor(rows, device=DEV)])
+    ref = O.lora_linear(xr, f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, ids_np[rows])
+    assert_parity(y[torch.as_tensor(rows, device=DEV)], ref, "int64 offsets")
+    del x, y, plan
+    torch.cuda.empty_cache()
