@@ -195,7 +195,9 @@ lora_status lora_plan_init(lora_plan_t* plan, void* workspace, size_t bytes, int
     uint8_t* p = static_cast<uint8_t*>(workspace);
     void* ptrs[11];
     for (int i = 0; i < 11; ++i) {
-        ptrs[i] = sizes[i] ? p : nullptr;
+        // zero-sized arrays of an empty batch still get a (never read) address;
+        // only x_sorted is null when the plan carries none
+        ptrs[i] = (sizes[i] || i != 10) ? p : nullptr;
         p += align_up(sizes[i], 256);
     }
     plan->slot_of_token = static_cast<int32_t*>(ptrs[0]);
