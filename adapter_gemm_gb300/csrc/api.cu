@@ -3,7 +3,9 @@
 // The library allocates no device memory; every buffer comes from the caller.
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "lora_gb300.h"
@@ -110,38 +112,101 @@ void plan_layout(int T, int S, int R_max, int d_in_cap, size_t sizes[11]) {
     sizes[10] = plan_needs_xsorted(T) ? (size_t)T * d_in_cap * 2 : 0;   // x_sorted
 }
 
-struct SkinnyConfig { int TN, stages, ks, occ; };
+struct SkinnyConfig { int TN, stages, ks, can_stage_u; size_t smem; };
 
+// Resident clusters per (device, TN, stages, smem, ks), cached.
+int max_clusters_cached(int TN, int stages, size_t smem, int ks) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, size_t, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, TN, stages, smem, ks);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const int n = skinny_max_active_clusters(TN, smem, ks);
+    std::lock_guard<std::mutex> lock(mu);
+    cache[key] = n;
+    return n;
+}
+
+// Launch shape of the skinny kernel. It depends only on (T, d_in, d_out), so a
+// base-only call and a call with a plan split K identically: shared memory is
+// sized for U rows of rank up to kStageURank whether or not they are used.
 SkinnyConfig skinny_config(int T, int K, int N) {
     SkinnyConfig c;
     const int Tt = T < kSkinnyMaxT ? T : kSkinnyMaxT;
     c.TN = ((Tt + 15) / 16) * 16;
     if (c.TN < 16) c.TN = 16;
     const size_t stage = (size_t)128 * 64 * 2 + (size_t)c.TN * 64 * 2;
-    if (skinny_smem_bytes(c.TN, 4) <= 113 * 1024) {
+    const size_t budget = 200 * 1024;
+    c.can_stage_u = skinny_epi_bytes(c.TN, kStageURank, true) + 2048 <= budget ? 1 : 0;
+    // 2 CTAs per SM when 4 stages fit in half the shared memory, else 1 with
+    // as many stages as fit.
+    if (skinny_smem_bytes(c.TN, 4, kStageURank, c.can_stage_u) <= 113 * 1024) {
         c.stages = 4;
-        c.occ = 2;
     } else {
-        c.stages = (int)((200 * 1024) / stage);
+        c.stages = (int)(budget / stage);
         if (c.stages > 6) c.stages = 6;
         if (c.stages < 2) c.stages = 2;
-        c.occ = 1;
     }
+    c.smem = skinny_smem_bytes(c.TN, c.stages, kStageURank, c.can_stage_u);
     const int units = ((N + 127) / 128) * ((T + c.TN - 1) / c.TN);
     const int kb = (K + 63) / 64;
-    const int cap = num_sms() * c.occ;
+    // Largest split (<= 8) whose clusters all fit in one wave; every split must
+    // own at least one K block.
     c.ks = 1;
-    while (c.ks < 8 && units * c.ks * 2 <= cap && kb >= c.ks * 2) c.ks *= 2;
-    // every split must own at least one K block
-    while (c.ks > 1) {
-        const int per = (kb + c.ks - 1) / c.ks;
-        if ((c.ks - 1) * per < kb) break;
-        c.ks /= 2;
+    for (int ks = 8; ks >= 2; ks /= 2) {
+        if (kb < ks) continue;
+        const int per = (kb + ks - 1) / ks;
+        if ((ks - 1) * per >= kb) continue;
+        if (units <= max_clusters_cached(c.TN, c.stages, c.smem, ks)) {
+            c.ks = ks;
+            break;
+        }
     }
     return c;
 }
 
 cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+// The kernels of a lora_linear call start (programmatic dependent launch)
+// before the kernel ahead of them on the stream has finished, and read their
+// inputs early. The only kernels of this library that write caller-visible
+// memory are the GEMMs (y), so per stream the output range of the last
+// lora_linear is kept: an input that overlaps it is read only after the wait.
+struct Range { uintptr_t lo = 0, hi = 0; };
+std::mutex g_range_mu;
+std::map<cudaStream_t, Range> g_last_out;
+
+bool overlaps(const Range& r, const void* p, size_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p), hi = lo + bytes;
+    return p != nullptr && bytes > 0 && lo < r.hi && r.lo < hi;
+}
+
+Range last_out(cudaStream_t st) {
+    std::lock_guard<std::mutex> lock(g_range_mu);
+    auto it = g_last_out.find(st);
+    return it == g_last_out.end() ? Range() : it->second;
+}
+
+void set_last_out(cudaStream_t st, const void* p, size_t bytes) {
+    std::lock_guard<std::mutex> lock(g_range_mu);
+    Range r;
+    r.lo = reinterpret_cast<uintptr_t>(p);
+    r.hi = r.lo + bytes;
+    g_last_out[st] = r;
+}
+
+int slot_splits(int n_slots, int K) {
+    // clusters of ks CTAs, one per adapter slot; at most ~2 per SM in flight
+    const int cap = 2 * num_sms();
+    int ks = 1;
+    while (ks < 8 && n_slots * ks * 2 <= cap && K / (ks * 2) >= 256) ks *= 2;
+    return ks;
+}
 
 int shrink_splits(int max_tiles, int K) {
     const int cap = 2 * num_sms();
@@ -297,7 +362,11 @@ lora_status lora_plan(const int32_t* ids, int T, lora_plan_t* plan, void* stream
     p.n_tiles = plan->n_tiles;
     p.n_invalid = plan->n_invalid;
     p.S = plan->S;
-    return launch_plan(ids, T, p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LORA_OK : LORA_ECUDA;
+    plan->ids = ids;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (launch_plan(ids, T, p, st) != cudaSuccess) return LORA_ECUDA;
+    set_last_out(st, nullptr, 0);     // the plan kernel waits for all earlier work
+    return LORA_OK;
 }
 
 lora_status lora_plan_check(const lora_plan_t* plan, void* stream, int32_t* n_invalid_out) {
@@ -333,10 +402,24 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = lora_linear_path(T, d_in, d_out);
     if (plan && path == 1 && !plan->x_sorted) return LORA_ESHAPE;
+    if (plan && path == 0 && !plan->ids) return LORA_EINVAL;     // lora_plan was never run
+
+    // Inputs written by the previous lora_linear on this stream are read only
+    // after the wait; weights or pool aliasing it (never expected) turn the
+    // early start off altogether.
+    const Range prev = last_out(st);
+    const bool x_early = !overlaps(prev, x, (size_t)T * d_in * 2) &&
+                         !(plan && overlaps(prev, plan->ids, (size_t)T * 4));
+    bool pdl = !overlaps(prev, W, (size_t)d_out * d_in * 2);
+    if (plan)
+        pdl = pdl && !overlaps(prev, pool->A, (size_t)pool->S * pool->R_max * d_in * 2) &&
+              !overlaps(prev, pool->B, (size_t)pool->S * d_out * pool->R_max * 2) &&
+              !overlaps(prev, pool->rank, (size_t)pool->S * 4) && !overlaps(prev, pool->scale, (size_t)pool->S * 4);
 
     if (plan) {
         ShrinkArgs sa;
         sa.x = static_cast<const __nv_bfloat16*>(x);
+        sa.ids = plan->ids;
         sa.A = static_cast<const __nv_bfloat16*>(pool->A);
         sa.scale = pool->scale;
         sa.rank = pool->rank;
@@ -348,8 +431,12 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         sa.T = T;
         sa.K = d_in;
         sa.R_max = pool->R_max;
-        sa.ks = shrink_splits(plan->max_tiles, d_in);
-        if (launch_shrink(sa, plan->max_tiles, true, st) != cudaSuccess) return LORA_ECUDA;
+        sa.x_early = x_early ? 1 : 0;
+        const bool by_slot = path == 0;
+        const int grid_x = by_slot ? pool->S - 1 : plan->max_tiles;
+        sa.ks = by_slot ? slot_splits(grid_x, d_in) : shrink_splits(plan->max_tiles, d_in);
+        if (launch_shrink(sa, grid_x, by_slot, pdl, st) != cudaSuccess) return LORA_ECUDA;
+        pdl = true;                    // the GEMM follows the shrink, which waited
     }
 
     ExpandArgs ex;
@@ -376,7 +463,10 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.kb_total = (d_in + 63) / 64;
         a.ks = c.ks;
         a.stages = c.stages;
-        if (launch_skinny(tmW, tmX, a, true, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
+        a.stage_u = (plan && c.can_stage_u && pool->R_max <= kStageURank) ? 1 : 0;
+        a.smem = c.smem;
+        a.x_early = x_early ? 1 : 0;
+        if (launch_skinny(tmW, tmX, a, pdl, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;
         CUtensorMap tmA, tmB;
@@ -395,9 +485,10 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.kb_total = (d_in + 63) / 64;
         int grid = a.m_tiles * a.n_tiles;
         if (grid > num_sms()) grid = num_sms();
-        if (launch_wide(tmA, tmB, a, true, grid, st) != cudaSuccess) return LORA_ECUDA;
+        if (launch_wide(tmA, tmB, a, pdl, grid, st) != cudaSuccess) return LORA_ECUDA;
     }
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;
+    set_last_out(st, y, (size_t)T * d_out * 2);
     return LORA_OK;
 }
 

@@ -34,30 +34,40 @@ constexpr int kBK = 64;                     // K elements per stage (128 bytes o
 constexpr int kWRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kWTileBytes = kWRows * kBK * 2;
 
-size_t skinny_smem_bytes(int TN, int stages) {
+// Epilogue scratch after the K loop: the received partials [ks][TN][128/ks]
+// (128 x TN floats), per-token slot and rank [2][TN], and (when staged) U rows
+// [TN][R_max].
+size_t skinny_epi_bytes(int TN, int R_max, bool stage_u) {
+    return (size_t)kWRows * TN * 4 + (size_t)2 * TN * 4 + (stage_u ? (size_t)TN * R_max * 4 : 0);
+}
+
+size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u) {
     const size_t stage = (size_t)kWTileBytes + (size_t)TN * kBK * 2;
     const size_t pipe = stage * stages;
-    const size_t red = (size_t)kWRows * (TN + 1) * 4;
-    const size_t body = pipe > red ? pipe : red;
+    const size_t epi = skinny_epi_bytes(TN, R_max, stage_u);
+    const size_t body = pipe > epi ? pipe : epi;
     return 1024 /*alignment slack*/ + body + 256 /*barriers*/;
 }
 
-__device__ __forceinline__ float expand_dot(const float* __restrict__ u,
-                                            const __nv_bfloat16* __restrict__ brow, int r8) {
-    float d = 0.f;
-    for (int j = 0; j < r8; j += 8) {
-        const uint4 bw = __ldg(reinterpret_cast<const uint4*>(brow + j));
-        const float4 u0 = __ldg(reinterpret_cast<const float4*>(u + j));
-        const float4 u1 = __ldg(reinterpret_cast<const float4*>(u + j + 4));
-        d = fmaf(u0.x, bf16lo(bw.x), d);
-        d = fmaf(u0.y, bf16hi(bw.x), d);
-        d = fmaf(u0.z, bf16lo(bw.y), d);
-        d = fmaf(u0.w, bf16hi(bw.y), d);
-        d = fmaf(u1.x, bf16lo(bw.z), d);
-        d = fmaf(u1.y, bf16hi(bw.z), d);
-        d = fmaf(u1.z, bf16lo(bw.w), d);
-        d = fmaf(u1.w, bf16hi(bw.w), d);
-    }
+// d + u[0..7] . b[0..7] (b = 8 packed bf16), j ascending.
+__device__ __forceinline__ float dot8(const float* __restrict__ u, const uint4 b, float d) {
+    const float4 u0 = *reinterpret_cast<const float4*>(u);
+    const float4 u1 = *reinterpret_cast<const float4*>(u + 4);
+    d = fmaf(u0.x, bf16lo(b.x), d);
+    d = fmaf(u0.y, bf16hi(b.x), d);
+    d = fmaf(u0.z, bf16lo(b.y), d);
+    d = fmaf(u0.w, bf16hi(b.y), d);
+    d = fmaf(u1.x, bf16lo(b.z), d);
+    d = fmaf(u1.y, bf16hi(b.z), d);
+    d = fmaf(u1.z, bf16lo(b.w), d);
+    d = fmaf(u1.w, bf16hi(b.w), d);
+    return d;
+}
+
+// d + sum_{j0 <= j < r8} u[j] b[j], in chunks of 8.
+__device__ __forceinline__ float expand_dot_from(const float* __restrict__ u, const __nv_bfloat16* __restrict__ brow,
+                                                 int j0, int r8, float d) {
+    for (int j = j0; j < r8; j += 8) d = dot8(u + j, __ldg(reinterpret_cast<const uint4*>(brow + j)), d);
     return d;
 }
 
@@ -71,13 +81,14 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const uint32_t x_tile_bytes = (uint32_t)TN * kBK * 2;
     const uint32_t stage_bytes = kWTileBytes + x_tile_bytes;
     const size_t pipe = (size_t)stage_bytes * stages;
-    const size_t red_bytes = (size_t)kWRows * (TN + 1) * 4;
-    uint8_t* tail = base + (pipe > red_bytes ? pipe : red_bytes);
+    const size_t epi_bytes = (size_t)kWRows * TN * 4 + (size_t)2 * TN * 4 +
+                             (a.stage_u ? (size_t)TN * a.ex.R_max * 4 : 0);
+    uint8_t* tail = base + (pipe > epi_bytes ? pipe : epi_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(tail);          // [stages]
     uint64_t* empty = full + stages;                              // [stages]
     uint64_t* accf = empty + stages;                              // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
-    float* red = reinterpret_cast<float*>(base);                  // [128][TN+1], after the K loop
+    float* red = reinterpret_cast<float*>(base);                  // received partials, after the K loop
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x;
@@ -109,29 +120,43 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // Everything above overlapped the previous kernel; inputs are read below.
-    pdl_wait();
+    // The next kernel of the stream may start its prologue now.
     pdl_trigger();
 
     bool ok = true;
     if (warp == 0 && lane == 0) {
-        // TMA producer.
+        // TMA producer. Weights are never written by the kernels this one waits
+        // for, so the first `stages` weight tiles go to shared memory and the rest
+        // of this CTA's weight range to L2 before the wait. x is loaded before
+        // the wait too unless the host saw that the previous kernel writes it.
+        const int pre = min(nkb, stages);
+        for (int i = 0; i < pre; ++i) {
+            const uint32_t fb = smem_u32(&full[i]);
+            const uint32_t sW = smem_u32(base + (size_t)i * stage_bytes);
+            mbar_arrive_expect_tx(fb, stage_bytes);
+            tma_load_2d(sW, &tmW, fb, (kb_lo + i) * kBK, n0);
+            if (a.x_early) tma_load_2d(sW + kWTileBytes, &tmX, fb, (kb_lo + i) * kBK, t0);
+        }
+        for (int i = pre; i < nkb; ++i) tma_prefetch_l2_2d(&tmW, (kb_lo + i) * kBK, n0);
+        if (!a.x_early) pdl_wait();
         int issued = 0;
         for (int i = 0; i < nkb && ok; ++i) {
             const int st = i % stages;
             const uint32_t ph = (uint32_t)(i / stages) & 1u;
-            if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
             const uint32_t sW = smem_u32(base + (size_t)st * stage_bytes);
-            const uint32_t sX = sW + kWTileBytes;
             const uint32_t fb = smem_u32(&full[st]);
-            mbar_arrive_expect_tx(fb, stage_bytes);
-            const int kx = (kb_lo + i) * kBK;
-            tma_load_2d(sW, &tmW, fb, kx, n0);
-            tma_load_2d(sX, &tmX, fb, kx, t0);
+            if (i >= pre) {
+                if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
+                mbar_arrive_expect_tx(fb, stage_bytes);
+                tma_load_2d(sW, &tmW, fb, (kb_lo + i) * kBK, n0);
+                tma_load_2d(sW + kWTileBytes, &tmX, fb, (kb_lo + i) * kBK, t0);
+            } else if (!a.x_early) {
+                tma_load_2d(sW + kWTileBytes, &tmX, fb, (kb_lo + i) * kBK, t0);
+            }
             ++issued;
         }
         // Let every copy this thread started land before the buffers are reused.
-        for (int i = max(0, issued - stages); i < issued; ++i)
+        for (int i = max(0, max(issued, pre) - stages); i < max(issued, pre); ++i)
             mbar_wait(smem_u32(&full[i % stages]), (uint32_t)(i / stages) & 1u, kErrFullWait);
     } else if (warp == 1 && lane == 0) {
         // MMA issuer.
@@ -153,64 +178,110 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         tc_commit(smem_u32(accf));     // fires once every MMA above has completed
     }
     __syncwarp();
+    pdl_wait();                        // slot ids and U come from the kernels before this one
 
-    // Drain the accumulator: row (weight row) = 32*warp + lane, columns = tokens.
+    // Split-K reduction. CTA rank c owns weight rows [c*rows_per, (c+1)*rows_per)
+    // of the tile. Once every CTA of the cluster is past its K loop, each one
+    // pushes its partial rows straight from TMEM into the owner's shared memory
+    // (recv[src rank][token][row], plain stores into the peer), then each owner
+    // sums what it received in rank order: a fixed order, and no remote loads.
     const int row = warp * 32 + lane;
+    const int rows_per = kWRows / a.ks;
     bool have = nkb > 0;
     if (have) {
         if (!mbar_wait(smem_u32(accf), 0, kErrAccWait)) have = false;
         tc_fence_after();
     }
-    __syncthreads();                   // stage buffers are free once the MMAs are done
-    for (int c = 0; c < TN; c += 16) {
-        float v[16];
-        if (have) {
-            tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-        } else {
+    __syncthreads();                   // this CTA's stage buffers are free
+    cg::cluster_group cluster = cg::this_cluster();
+    if (a.ks > 1) cluster.sync();      // ... and every peer's
+    const uint32_t recv = smem_u32(red);
+    {
+        const int owner = row / rows_per, ln = row % rows_per;
+        const uint32_t dst0 = (a.ks > 1) ? mapa_shared(recv, (uint32_t)owner) : recv;
+        for (int c = 0; c < TN; c += 16) {
+            float v[16];
+            if (have) {
+                tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                for (int i = 0; i < 16; ++i) v[i] = 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                st_cluster_f32(dst0 + (uint32_t)((((kz * TN) + c + i) * rows_per + ln) * 4), v[i]);
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) red[row * (TN + 1) + c + i] = v[i];
     }
     tc_fence_before();
-    __syncthreads();
 
-    // Split-K reduction across the cluster, then the correction and the store.
-    cg::cluster_group cluster = cg::this_cluster();
-    if (a.ks > 1) cluster.sync();
-    const int rows_per = kWRows / a.ks;
+    // Per-token slot, rank (rounded up to 8) and U row, staged once for the tile.
+    int* tok_s = reinterpret_cast<int*>(red + (size_t)kWRows * TN);
+    int* tok_r8 = tok_s + TN;
+    float* tok_u = reinterpret_cast<float*>(tok_r8 + TN);
+    const bool with_ex = a.ex.slot_of_token != nullptr;
+    const int R = a.ex.R_max;
+    pdl_wait();                        // slot ids and U come from the kernels before this one
+    for (int tl = threadIdx.x; tl < TN; tl += kSkThreads) {
+        const int t = t0 + tl;
+        int s = 0, r8 = 0;
+        if (with_ex && t < a.T) {
+            s = a.ex.slot_of_token[t];
+            if (s > 0) {
+                const int r = min(a.ex.rank[s], R);
+                r8 = r > 0 ? (r + 7) & ~7 : 0;
+            }
+        }
+        tok_s[tl] = s;
+        tok_r8[tl] = r8;
+    }
+    __syncthreads();
+    if (with_ex && a.stage_u) {
+        for (int q = threadIdx.x; q < TN * (R / 4); q += kSkThreads) {
+            const int tl = q / (R / 4), j4 = q % (R / 4);
+            if (tok_r8[tl] > j4 * 4)
+                reinterpret_cast<float4*>(tok_u)[q] =
+                    __ldg(reinterpret_cast<const float4*>(a.ex.U + (size_t)(t0 + tl) * R) + j4);
+        }
+    }
+    if (a.ks > 1) cluster.sync();      // every push into this CTA has landed
+    else __syncthreads();
+
     const int r_lo = kz * rows_per;
     const int n_el = rows_per * TN;
-    for (int el = threadIdx.x; el < n_el; el += kSkThreads) {
-        const int nl = r_lo + el % rows_per;
-        const int tl = el / rows_per;
-        const int t = t0 + tl, n = n0 + nl;
-        if (t >= a.T || n >= a.N) continue;
-        float acc;
-        if (a.ks > 1) {
-            acc = 0.f;
-            for (int c = 0; c < a.ks; ++c) {
-                const float* rr = cluster.map_shared_rank(red, c);
-                acc += rr[nl * (TN + 1) + tl];
-            }
-        } else {
-            acc = red[nl * (TN + 1) + tl];
-        }
-        if (a.ex.slot_of_token != nullptr) {
-            const int s = a.ex.slot_of_token[t];
-            if (s > 0) {
-                const int r = min(__ldg(&a.ex.rank[s]), a.ex.R_max);
-                if (r > 0) {
-                    const int r8 = (r + 7) & ~7;
-                    acc += expand_dot(a.ex.U + (size_t)t * a.ex.R_max,
-                                      a.ex.B + ((size_t)s * a.N + n) * a.ex.R_max, r8);
-                }
+    constexpr int E = 4;               // elements per thread whose B loads are in flight together
+    for (int e0 = threadIdx.x; e0 < n_el; e0 += E * kSkThreads) {
+        uint4 b0[E], b1[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int el = e0 + e * kSkThreads;
+            const int ln = el % rows_per, tl = el / rows_per;
+            const int n = n0 + r_lo + ln;
+            b0[e] = b1[e] = make_uint4(0, 0, 0, 0);
+            if (el < n_el && t0 + tl < a.T && n < a.N && tok_r8[tl] > 0) {
+                const __nv_bfloat16* brow = a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R;
+                b0[e] = __ldg(reinterpret_cast<const uint4*>(brow));
+                if (tok_r8[tl] > 8) b1[e] = __ldg(reinterpret_cast<const uint4*>(brow + 8));
             }
         }
-        a.y[(size_t)t * a.N + n] = __float2bfloat16_rn(acc);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int el = e0 + e * kSkThreads;
+            const int ln = el % rows_per, tl = el / rows_per;
+            const int t = t0 + tl, n = n0 + r_lo + ln;
+            if (el >= n_el || t >= a.T || n >= a.N) continue;
+            float acc = red[(size_t)tl * rows_per + ln];
+            for (int z = 1; z < a.ks; ++z) acc += red[((size_t)z * TN + tl) * rows_per + ln];
+            const int r8 = tok_r8[tl];
+            if (r8 > 0) {
+                const float* u = a.stage_u ? tok_u + (size_t)tl * R : a.ex.U + (size_t)t * R;
+                float d = dot8(u, b0[e], 0.f);
+                if (r8 > 8) d = dot8(u + 8, b1[e], d);
+                if (r8 > 16) d = expand_dot_from(u, a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R, 16, r8, d);
+                acc += d;
+            }
+            a.y[(size_t)t * a.N + n] = __float2bfloat16_rn(acc);
+        }
     }
-    if (a.ks > 1) cluster.sync();      // peers may still read this CTA's partial
 
     if (warp == 1) {
         tc_fence_after();
@@ -221,7 +292,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyArgs& a,
                           bool pdl, int num_sms, cudaStream_t stream) {
     (void)num_sms;
-    const size_t smem = skinny_smem_bytes(a.TN, a.stages);
+    const size_t smem = a.smem;
     cudaError_t e = ensure_smem_attr((const void*)gemm_skinny_kernel, 1, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -244,6 +315,29 @@ cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
     cfg.attrs = attr;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel, tmW, tmX, a);
+}
+
+// How many clusters of `ks` CTAs of this configuration can be resident at once.
+int skinny_max_active_clusters(int TN, size_t smem, int ks) {
+    (void)TN;
+    if (ensure_smem_attr((const void*)gemm_skinny_kernel, 1, smem) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, ks, 1);
+    cfg.blockDim = dim3(kSkThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = ks;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)gemm_skinny_kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 cudaError_t skinny_take_error(int* code) {

@@ -30,21 +30,34 @@ constexpr uint32_t kWdBBytes = kWdBN * kWdBK * 2;     // 32 KB
 constexpr uint32_t kWdStageBytes = kWdABytes + kWdBBytes;
 constexpr size_t kWdSmem = 1024 + (size_t)kWdStageBytes * kWdStages + 256;
 
-__device__ __forceinline__ float wd_expand_dot(const float* __restrict__ u,
-                                               const __nv_bfloat16* __restrict__ brow, int r8) {
-    float d = 0.f;
-    for (int j = 0; j < r8; j += 8) {
-        const uint4 bw = __ldg(reinterpret_cast<const uint4*>(brow + j));
+// d + u[off..off+8) . b (8 packed bf16), j ascending; u held in registers.
+__device__ __forceinline__ float dot8r(const float (&u)[16], const int off, const uint4 b, float d) {
+    d = fmaf(u[off + 0], bf16lo(b.x), d);
+    d = fmaf(u[off + 1], bf16hi(b.x), d);
+    d = fmaf(u[off + 2], bf16lo(b.y), d);
+    d = fmaf(u[off + 3], bf16hi(b.y), d);
+    d = fmaf(u[off + 4], bf16lo(b.z), d);
+    d = fmaf(u[off + 5], bf16hi(b.z), d);
+    d = fmaf(u[off + 6], bf16lo(b.w), d);
+    d = fmaf(u[off + 7], bf16hi(b.w), d);
+    return d;
+}
+
+// d + sum_{j0 <= j < r8} u[j] b[j] for ranks beyond the register-held 16.
+__device__ __noinline__ float wd_expand_dot_from(const float* __restrict__ u, const __nv_bfloat16* __restrict__ brow,
+                                                 int j0, int r8, float d) {
+    for (int j = j0; j < r8; j += 8) {
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(brow + j));
         const float4 u0 = __ldg(reinterpret_cast<const float4*>(u + j));
         const float4 u1 = __ldg(reinterpret_cast<const float4*>(u + j + 4));
-        d = fmaf(u0.x, bf16lo(bw.x), d);
-        d = fmaf(u0.y, bf16hi(bw.x), d);
-        d = fmaf(u0.z, bf16lo(bw.y), d);
-        d = fmaf(u0.w, bf16hi(bw.y), d);
-        d = fmaf(u1.x, bf16lo(bw.z), d);
-        d = fmaf(u1.y, bf16hi(bw.z), d);
-        d = fmaf(u1.z, bf16lo(bw.w), d);
-        d = fmaf(u1.w, bf16hi(bw.w), d);
+        d = fmaf(u0.x, bf16lo(b.x), d);
+        d = fmaf(u0.y, bf16hi(b.x), d);
+        d = fmaf(u0.z, bf16lo(b.y), d);
+        d = fmaf(u0.w, bf16hi(b.y), d);
+        d = fmaf(u1.x, bf16lo(b.z), d);
+        d = fmaf(u1.y, bf16hi(b.z), d);
+        d = fmaf(u1.z, bf16lo(b.w), d);
+        d = fmaf(u1.w, bf16hi(b.w), d);
     }
     return d;
 }
@@ -85,8 +98,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    pdl_wait();
     pdl_trigger();
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -169,6 +182,14 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             }
             const float* urow = a.ex.U + (size_t)t * a.ex.R_max;
             __nv_bfloat16* yrow = a.y + (size_t)t * a.N;
+            // The row's first 16 U values stay in registers for the whole tile.
+            float u[16];
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+                const float4 f = (r8 > j4 * 4) ? __ldg(reinterpret_cast<const float4*>(urow) + j4)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                u[4 * j4] = f.x; u[4 * j4 + 1] = f.y; u[4 * j4 + 2] = f.z; u[4 * j4 + 3] = f.w;
+            }
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(as * kWdBN);
             for (int c = 0; c < kWdBN; c += 16) {
                 float v[16];
@@ -178,8 +199,25 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     if (r8 > 0) {
                         const __nv_bfloat16* bblk = a.ex.B + ((size_t)s * a.N + n) * a.ex.R_max;
 #pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            if (n + q < a.N) v[q] += wd_expand_dot(urow, bblk + (size_t)q * a.ex.R_max, r8);
+                        for (int q0 = 0; q0 < 16; q0 += 4) {
+                            uint4 b0[4], b1[4];
+#pragma unroll
+                            for (int qq = 0; qq < 4; ++qq) {
+                                const bool in = n + q0 + qq < a.N;
+                                const __nv_bfloat16* br = bblk + (size_t)(q0 + qq) * a.ex.R_max;
+                                b0[qq] = in ? __ldg(reinterpret_cast<const uint4*>(br)) : make_uint4(0, 0, 0, 0);
+                                b1[qq] = (in && r8 > 8) ? __ldg(reinterpret_cast<const uint4*>(br + 8))
+                                                        : make_uint4(0, 0, 0, 0);
+                            }
+#pragma unroll
+                            for (int qq = 0; qq < 4; ++qq) {
+                                float d = dot8r(u, 0, b0[qq], 0.f);
+                                d = dot8r(u, 8, b1[qq], d);
+                                if (r8 > 16)
+                                    d = wd_expand_dot_from(urow, bblk + (size_t)(q0 + qq) * a.ex.R_max, 16, r8, d);
+                                v[q0 + qq] += d;
+                            }
+                        }
                     }
                     uint4 o0, o1;
                     o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);

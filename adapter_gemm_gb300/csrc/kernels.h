@@ -11,6 +11,7 @@ constexpr int kTileRows = 16;       // plan work tiles, rows (== LORA_TILE_ROWS)
 constexpr int kMaxSlots = 1024;     // one plan thread per slot in the scans
 constexpr int kMaxRank = 128;       // R_max cap: shrink keeps R_max/8 MMA column tiles
 constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 256)
+constexpr int kStageURank = 64;     // the skinny epilogue stages U rows of rank <= 64
 
 struct PlanArgs {
     int32_t* slot_of_token;
@@ -27,6 +28,7 @@ struct PlanArgs {
 
 struct ShrinkArgs {
     const __nv_bfloat16* x;      // [T, K]
+    const int32_t* ids;          // [T] the step's raw slot ids (by-slot grid)
     const __nv_bfloat16* A;      // [S, R_max, K]
     const float* scale;          // [S]
     const int32_t* rank;         // [S]
@@ -36,6 +38,7 @@ struct ShrinkArgs {
     float* U;                    // [T, R_max]
     __nv_bfloat16* x_sorted;     // [T, K] or null
     int T, K, R_max, ks;
+    int x_early;                 // x is not written by the kernel this one follows
 };
 
 // Epilogue operands shared by both GEMM kernels. slot_of_token == null means
@@ -56,6 +59,9 @@ struct SkinnyArgs {
     int kb_total;      // ceil(K / 64)
     int ks;            // K splits = cluster size along y
     int stages;
+    int stage_u;       // copy the tile's U rows into shared memory for the epilogue
+    int x_early;       // x may be loaded before the wait for the previous kernel
+    size_t smem;       // dynamic shared memory of the launch
 };
 
 struct WideArgs {
@@ -67,7 +73,7 @@ struct WideArgs {
 };
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, cudaStream_t stream);
-cudaError_t launch_shrink(const ShrinkArgs& a, int max_tiles, bool pdl, cudaStream_t stream);
+cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream);
 cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyArgs& a,
                           bool pdl, int num_sms, cudaStream_t stream);
 cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const WideArgs& a,
@@ -83,6 +89,8 @@ cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
 
 // Shared-memory bytes the skinny kernel needs for a token tile of TN columns
 // and `stages` pipeline stages.
-size_t skinny_smem_bytes(int TN, int stages);
+size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u);
+size_t skinny_epi_bytes(int TN, int R_max, bool stage_u);
+int skinny_max_active_clusters(int TN, size_t smem, int ks);
 
 }  // namespace lora

@@ -21,17 +21,11 @@ enum : int {
     kErrAccFreeWait = 4,   // waiting for the epilogue to drain an accumulator
 };
 
-// A wait gives up after this many nanoseconds of %globaltimer.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// A wait gives up after this many SM cycles (about 2 s at 2 GHz).
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
 }
 
 __device__ __forceinline__ bool elect_one() {
@@ -66,15 +60,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for phase `parity` of the barrier to complete. Returns false
-// (and records `err`) when the limit runs out.
+// (and records `err`) when the limit runs out. The limit is counted in SM
+// cycles (cheap to read) and only checked every 1024 tries, so the common
+// short waits cost nothing beyond the try_wait itself.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
+    long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
-            atomicCAS(&g_lora_error, 0, err);
-            return false;
+        if ((i & 1023u) == 1023u) {
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitCycles) {
+                atomicCAS(&g_lora_error, 0, err);
+                return false;
+            }
         }
     }
 }
@@ -93,6 +93,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4}], [%2];"
         :: "r"(dst), "l"(tmap), "r"(bar), "r"(c0), "r"(c1) : "memory");
+}
+
+// Prefetch a 2-D tile into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 :: "l"(tmap), "r"(c0), "r"(c1) : "memory");
+}
+
+// ---------------------------------------------------------------- cluster ---
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Store into (possibly another CTA's) shared memory of the cluster.
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- PDL -------

@@ -3,12 +3,13 @@
 // inputs [num_tokens, hidden], lora_a [num_loras, rank, hidden], an fp32
 // [tokens, rank] output; Chapter 43's "shrink each row to its adapter's rank").
 //
-// One CTA per plan work tile: up to 16 rows of one slot's segment, so the
-// slot's A block is read once for the tile and the rows share it (the SGMV
-// segment idea). The tile's K range is split over the CTAs of a thread-block
-// cluster (ks of them) and over the 4 warps of each CTA; partial sums are
-// reduced in a fixed order (warps 0..3, then cluster ranks 0..ks-1 through
-// distributed shared memory), so the result is deterministic.
+// A CTA works on up to 16 rows of one slot, so the slot's A block is read once
+// for those rows and they share it (the SGMV segment idea). The K range is
+// split over the CTAs of a thread-block cluster (ks of them) and over the 4
+// warps of each CTA; partial sums are reduced in a fixed order (warps 0..3,
+// then cluster ranks 0..ks-1 through distributed shared memory), so the
+// result is deterministic. Two grids use this: one CTA per plan work tile (for
+// the wide GEMM), and one cluster per slot (for decode-sized batches).
 //
 // The contraction runs on mma.sync m16n8k16 (bf16 in, fp32 accumulate): the
 // shrink is a small, bandwidth-bound part of the layer (r/d_out of its FLOPs),
@@ -18,8 +19,7 @@
 // which leaves the sum unchanged.
 //
 // For the wide GEMM path the same pass also writes x_sorted, the rows of x in
-// plan order, so the GEMM can load contiguous plan-ordered tiles with TMA;
-// tiles of slot 0 and of rank-0 slots then only copy.
+// plan order, so the GEMM can load contiguous plan-ordered tiles with TMA.
 #include <cstdint>
 #include <cooperative_groups.h>
 #include "ptx.cuh"
@@ -40,60 +40,31 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int NT>   // NT = number of 8-column MMA tiles covering R_max
-__global__ void __launch_bounds__(kShrinkThreads)
-shrink_kernel(ShrinkArgs a) {
-    constexpr int RC = NT * 8;                       // columns held per row
-    __shared__ float part[4][16][RC + 1];            // per-warp partials
-    __shared__ float cta_sum[16][RC + 1];            // this CTA's partial
-
-    // The plan and the previous call's readers of U / x_sorted must be done.
-    pdl_wait();
-    pdl_trigger();
-
-    const int n_tiles = *a.n_tiles;
-    const int tile_idx = blockIdx.x;
-    if (tile_idx >= n_tiles) return;                 // the whole cluster shares tile_idx
-
-    const int4 tile = a.tiles[tile_idx];
-    const int s = tile.x, b = tile.y, e = tile.z;
-    const int r = (s > 0) ? min(a.rank[s], a.R_max) : 0;
-    const bool do_mma = r > 0;
-    const bool do_copy = a.x_sorted != nullptr;
-    if (!do_mma && !do_copy) return;
-
+// Partial U of one 16-row group over this CTA's K range [k_lo, k_hi): each of
+// the 4 warps takes every 4th 32-wide K step. Lane (g, q) loads 8 consecutive
+// k of rows g and g+8 and of A rows nt*8+g, and feeds them to two MMAs. Rows
+// the group does not have are read as zeros. When xs0/xs1 are given, the rows
+// are also copied there (the plan-ordered copy of x).
+template <int NT>
+__device__ __forceinline__ void shrink_accumulate(float (&acc)[NT][4], const __nv_bfloat16* xr0,
+                                                  const __nv_bfloat16* xr1, bool v0, bool v1,
+                                                  __nv_bfloat16* xs0, __nv_bfloat16* xs1,
+                                                  const __nv_bfloat16* Ablk, int K, int nt_used,
+                                                  int k_lo, int k_hi, bool do_mma) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
-    const int K = a.K;
-    const int kz = (a.ks > 1) ? (int)blockIdx.y : 0;
-    const int kc = ((K + a.ks * 32 - 1) / (a.ks * 32)) * 32;
-    const int k_lo = kz * kc, k_hi = min(K, k_lo + kc);
-
-    const int i0 = b + g, i1 = b + g + 8;            // plan positions of this lane's rows
-    const bool v0 = i0 < e, v1 = i1 < e;
-    const int t0 = v0 ? a.token_order[i0] : 0;
-    const int t1 = v1 ? a.token_order[i1] : 0;
-    const __nv_bfloat16* xr0 = a.x + (size_t)t0 * K;
-    const __nv_bfloat16* xr1 = a.x + (size_t)t1 * K;
-    __nv_bfloat16* xs0 = do_copy ? a.x_sorted + (size_t)i0 * K : nullptr;
-    __nv_bfloat16* xs1 = do_copy ? a.x_sorted + (size_t)i1 * K : nullptr;
-    const __nv_bfloat16* Ablk = a.A + (size_t)(do_mma ? s : 0) * a.R_max * K;
-    const int nt_used = (r + 7) >> 3;
-
-    float acc[NT][4];
+    const uint4 zero4 = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-
-    const uint4 zero4 = make_uint4(0, 0, 0, 0);
 #pragma unroll 2
     for (int k = k_lo + warp * 32; k < k_hi; k += 4 * 32) {
         const int kk = k + 8 * q;
         const bool kv = kk < k_hi;
         const uint4 xa = (v0 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr0 + kk)) : zero4;
         const uint4 xb = (v1 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr1 + kk)) : zero4;
-        if (do_copy && kv) {
-            if (v0) *reinterpret_cast<uint4*>(xs0 + kk) = xa;
-            if (v1) *reinterpret_cast<uint4*>(xs1 + kk) = xb;
+        if (kv) {
+            if (xs0 && v0) *reinterpret_cast<uint4*>(xs0 + kk) = xa;
+            if (xs1 && v1) *reinterpret_cast<uint4*>(xs1 + kk) = xb;
         }
         if (do_mma) {
 #pragma unroll
@@ -107,10 +78,19 @@ shrink_kernel(ShrinkArgs a) {
             }
         }
     }
-    if (!do_mma) return;                              // copy-only tiles are done
+}
 
-    // Per-warp partials -> shared memory. Fragment: c0,c1 at (row g, col 2q..),
-    // c2,c3 at (row g+8, col 2q..) of each 8-column tile.
+// Sum the group's partials over the 4 warps and the cluster's ks CTAs, in a
+// fixed order, scale, and store U rows: row i of the group is token tok[i]
+// (i < n). The caller must have waited for earlier readers of U.
+template <int NT>
+__device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], float (*part)[16][NT * 8 + 1],
+                                                    float (*cta_sum)[NT * 8 + 1], const int* tok, int n,
+                                                    int rc8, float sc, float* U, int R_max, int ks) {
+    constexpr int RC = NT * 8;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, q = lane & 3;
+    // Fragment: c0,c1 at (row g, col 2q..), c2,c3 at (row g+8, col 2q..).
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         const int col = nt * 8 + 2 * q;
@@ -120,42 +100,163 @@ shrink_kernel(ShrinkArgs a) {
         part[warp][g + 8][col + 1] = acc[nt][3];
     }
     __syncthreads();
-    const int n_el = 16 * RC;
-    for (int el = threadIdx.x; el < n_el; el += kShrinkThreads) {
+    for (int el = threadIdx.x; el < 16 * RC; el += kShrinkThreads) {
         const int row = el / RC, col = el % RC;
         cta_sum[row][col] = ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) + part[3][row][col];
     }
     __syncthreads();
-
-    const int rc8 = nt_used * 8;                      // rank rounded up to 8: U is zero past r
-    const float sc = a.scale[s];
-    if (a.ks > 1) {
+    if (ks > 1) {
+        // Rank c finishes rows [c*16/ks, (c+1)*16/ks): it requests every rank's
+        // partial of those rows at once, then sums in rank order.
         cg::cluster_group cluster = cg::this_cluster();
         cluster.sync();                               // every rank's cta_sum is complete
-        if (cluster.block_rank() == 0) {
-            for (int el = threadIdx.x; el < 16 * rc8; el += kShrinkThreads) {
-                const int row = el / rc8, col = el % rc8;
-                float v = 0.f;
-                for (int c = 0; c < a.ks; ++c) {
-                    const float* remote = cluster.map_shared_rank(&cta_sum[0][0], c);
-                    v += remote[row * (RC + 1) + col];
-                }
-                if (b + row < e) a.U[(size_t)a.token_order[b + row] * a.R_max + col] = sc * v;
-            }
+        const float* peer[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) peer[c] = c < ks ? cluster.map_shared_rank(&cta_sum[0][0], c) : &cta_sum[0][0];
+        const int rows_per = 16 / ks;
+        const int row0 = (int)cluster.block_rank() * rows_per;
+        for (int el = threadIdx.x; el < rows_per * rc8; el += kShrinkThreads) {
+            const int row = row0 + el / rc8, col = el % rc8;
+            float p[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) p[c] = c < ks ? peer[c][row * (RC + 1) + col] : 0.f;
+            float v = p[0];
+#pragma unroll
+            for (int c = 1; c < 8; ++c)
+                if (c < ks) v += p[c];
+            if (row < n) U[(size_t)tok[row] * R_max + col] = sc * v;
         }
-        cluster.sync();                               // keep shared memory alive for rank 0
+        cluster.sync();                               // keep shared memory alive for the peers
     } else {
         for (int el = threadIdx.x; el < 16 * rc8; el += kShrinkThreads) {
             const int row = el / rc8, col = el % rc8;
-            if (b + row < e) a.U[(size_t)a.token_order[b + row] * a.R_max + col] = sc * cta_sum[row][col];
+            if (row < n) U[(size_t)tok[row] * R_max + col] = sc * cta_sum[row][col];
         }
+        __syncthreads();
+    }
+}
+
+// One CTA (cluster of ks CTAs along K) per plan work tile: up to 16 rows of
+// one slot's segment. Used with the wide GEMM, so it also writes x_sorted;
+// tiles of slot 0 and of rank-0 slots only copy.
+template <int NT>
+__global__ void __launch_bounds__(kShrinkThreads)
+shrink_tiles_kernel(ShrinkArgs a) {
+    constexpr int RC = NT * 8;
+    __shared__ float part[4][16][RC + 1];
+    __shared__ float cta_sum[16][RC + 1];
+    __shared__ int tok[16];
+
+    // The next kernel may start its prologue; this one needs the plan, and the
+    // previous call's readers of U / x_sorted must be done, before it goes on.
+    pdl_trigger();
+    pdl_wait();
+
+    const int n_tiles = *a.n_tiles;
+    const int tile_idx = blockIdx.x;
+    if (tile_idx >= n_tiles) return;                 // the whole cluster shares tile_idx
+    const int4 tile = a.tiles[tile_idx];
+    const int s = tile.x, b = tile.y, e = tile.z;
+    const int r = (s > 0) ? min(a.rank[s], a.R_max) : 0;
+    const bool do_mma = r > 0;
+    const bool do_copy = a.x_sorted != nullptr;
+    if (!do_mma && !do_copy) return;
+
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;
+    const int K = a.K;
+    const int kz = (a.ks > 1) ? (int)blockIdx.y : 0;
+    const int kc = ((K + a.ks * 32 - 1) / (a.ks * 32)) * 32;
+    const int k_lo = kz * kc, k_hi = min(K, k_lo + kc);
+    if (threadIdx.x < 16) tok[threadIdx.x] = (b + (int)threadIdx.x < e) ? a.token_order[b + threadIdx.x] : 0;
+    const int i0 = b + g, i1 = b + g + 8;            // plan positions of this lane's rows
+    const bool v0 = i0 < e, v1 = i1 < e;
+    const int t0 = v0 ? a.token_order[i0] : 0;
+    const int t1 = v1 ? a.token_order[i1] : 0;
+    float acc[NT][4];
+    shrink_accumulate<NT>(acc, a.x + (size_t)t0 * K, a.x + (size_t)t1 * K, v0, v1,
+                          do_copy ? a.x_sorted + (size_t)i0 * K : nullptr,
+                          do_copy ? a.x_sorted + (size_t)i1 * K : nullptr,
+                          a.A + (size_t)(do_mma ? s : 0) * a.R_max * K, K, (r + 7) >> 3, k_lo, k_hi, do_mma);
+    if (!do_mma) return;                              // copy-only tiles are done
+    __syncthreads();                                  // tok[] is visible
+    shrink_reduce_store<NT>(acc, part, cta_sum, tok, e - b, ((r + 7) >> 3) * 8, a.scale[s], a.U, a.R_max, a.ks);
+}
+
+// Decode-sized batches (T <= 256): one cluster of ks CTAs (split along K) per
+// adapter slot s >= 1. The CTA finds the rows on its slot from the step's ids
+// itself (ascending, so the same grouping the plan would give), which lets it
+// run before the plan kernel has finished: it reads only inputs (ids, x, the
+// pool) until it stores U, and waits for the kernels before it only then.
+template <int NT>
+__global__ void __launch_bounds__(kShrinkThreads)
+shrink_by_slot_kernel(ShrinkArgs a) {
+    constexpr int RC = NT * 8;
+    __shared__ float part[4][16][RC + 1];
+    __shared__ float cta_sum[16][RC + 1];
+    __shared__ int rows[kSkinnyMaxT];
+    __shared__ int wtot[4];
+
+    pdl_trigger();
+    const int s = blockIdx.x + 1;
+    const int r = min(a.rank[s], a.R_max);           // written only by the synchronous install
+    // rows on slot s, ascending: two ids per thread, then a block prefix sum
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t_a = 2 * tid, t_b = 2 * tid + 1;
+    const int f_a = (r > 0 && t_a < a.T && a.ids[t_a] == s) ? 1 : 0;
+    const int f_b = (r > 0 && t_b < a.T && a.ids[t_b] == s) ? 1 : 0;
+    int inc = f_a + f_b;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += v;
+    }
+    if (lane == 31) wtot[warp] = inc;
+    __syncthreads();
+    int before = 0, n_rows = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        before += (w < warp) ? wtot[w] : 0;
+        n_rows += wtot[w];
+    }
+    const int pos = before + inc - f_a - f_b;
+    if (f_a) rows[pos] = t_a;
+    if (f_b) rows[pos + f_a] = t_b;
+    if (n_rows == 0) {                 // no rows (or rank 0): same for the whole cluster
+        pdl_wait();
+        return;
+    }
+    if (!a.x_early) pdl_wait();        // x may come from the kernel before this one
+    __syncthreads();
+
+    const int g = lane >> 2;
+    const int K = a.K;
+    const int kz = (a.ks > 1) ? (int)blockIdx.y : 0;
+    const int kc = ((K + a.ks * 32 - 1) / (a.ks * 32)) * 32;
+    const int k_lo = kz * kc, k_hi = min(K, k_lo + kc);
+    const int nt_used = (r + 7) >> 3;
+    const float sc = a.scale[s];
+    const __nv_bfloat16* Ablk = a.A + (size_t)s * a.R_max * K;
+    bool waited = !a.x_early;
+    for (int g0 = 0; g0 < n_rows; g0 += 16) {
+        const bool v0 = g0 + g < n_rows, v1 = g0 + g + 8 < n_rows;
+        const int t0 = v0 ? rows[g0 + g] : 0, t1 = v1 ? rows[g0 + g + 8] : 0;
+        float acc[NT][4];
+        shrink_accumulate<NT>(acc, a.x + (size_t)t0 * K, a.x + (size_t)t1 * K, v0, v1, nullptr, nullptr,
+                              Ablk, K, nt_used, k_lo, k_hi, true);
+        if (!waited) {                 // earlier readers of U must be done before it is written
+            pdl_wait();
+            waited = true;
+        }
+        shrink_reduce_store<NT>(acc, part, cta_sum, rows + g0, min(16, n_rows - g0), nt_used * 8, sc, a.U,
+                                a.R_max, a.ks);
     }
 }
 
 template <int NT>
-static cudaError_t launch_shrink_nt(const ShrinkArgs& a, int max_tiles, bool pdl, cudaStream_t stream) {
+static cudaError_t launch_shrink_nt(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(max_tiles, a.ks, 1);
+    cfg.gridDim = dim3(grid_x, a.ks, 1);
     cfg.blockDim = dim3(kShrinkThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -175,17 +276,18 @@ static cudaError_t launch_shrink_nt(const ShrinkArgs& a, int max_tiles, bool pdl
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, shrink_kernel<NT>, a);
+    return by_slot ? cudaLaunchKernelEx(&cfg, shrink_by_slot_kernel<NT>, a)
+                   : cudaLaunchKernelEx(&cfg, shrink_tiles_kernel<NT>, a);
 }
 
-cudaError_t launch_shrink(const ShrinkArgs& a, int max_tiles, bool pdl, cudaStream_t stream) {
-    if (max_tiles <= 0) return cudaSuccess;
+cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream) {
+    if (grid_x <= 0) return cudaSuccess;
     const int nt = (a.R_max + 7) / 8;
-    if (nt <= 1) return launch_shrink_nt<1>(a, max_tiles, pdl, stream);
-    if (nt <= 2) return launch_shrink_nt<2>(a, max_tiles, pdl, stream);
-    if (nt <= 4) return launch_shrink_nt<4>(a, max_tiles, pdl, stream);
-    if (nt <= 8) return launch_shrink_nt<8>(a, max_tiles, pdl, stream);
-    return launch_shrink_nt<16>(a, max_tiles, pdl, stream);
+    if (nt <= 1) return launch_shrink_nt<1>(a, grid_x, by_slot, pdl, stream);
+    if (nt <= 2) return launch_shrink_nt<2>(a, grid_x, by_slot, pdl, stream);
+    if (nt <= 4) return launch_shrink_nt<4>(a, grid_x, by_slot, pdl, stream);
+    if (nt <= 8) return launch_shrink_nt<8>(a, grid_x, by_slot, pdl, stream);
+    return launch_shrink_nt<16>(a, grid_x, by_slot, pdl, stream);
 }
 
 // Count bf16 words that encode Inf or NaN (exponent bits all ones).

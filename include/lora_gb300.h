@@ -88,9 +88,13 @@ typedef struct {
  *                         call, row t = token t (scratch)
  *   x_sorted      [T, d_in_cap] bf16: x rows in plan order (scratch, only for
  *                         large T; NULL otherwise)
+ *   ids           the caller's ids buffer the plan was built from (recorded by
+ *                         lora_plan; decode-sized lora_linear calls read it)
  * A plan is only valid for the ids it was built from; rebuild it whenever the
- * ids (or the slot an adapter sits in) change. lora_linear calls that share a
- * plan share its scratch, so they must be ordered on one stream.
+ * ids (or the slot an adapter sits in) change, and keep the ids buffer
+ * unchanged while lora_linear calls that use the plan are in flight.
+ * lora_linear calls that share a plan share its scratch, so they must be
+ * ordered on one stream.
  */
 #define LORA_TILE_ROWS 16
 typedef struct {
@@ -105,6 +109,7 @@ typedef struct {
     int32_t* n_invalid;
     float* U;
     void* x_sorted;
+    const int32_t* ids;
     int32_t T, S, R_max, d_in_cap, max_tiles;
 } lora_plan_t;
 
