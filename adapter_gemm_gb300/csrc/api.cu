@@ -233,6 +233,7 @@ const char* lora_strerror(lora_status s) {
         case LORA_EIDRANGE: return "token slot ids outside [0, S) were seen";
         case LORA_ESPACE: return "workspace too small";
         case LORA_ETIMEOUT: return "a kernel gave up a bounded wait";
+        case LORA_ESCRATCH: return "sizes exceed the fixed scratch of lora_linear_static_scratch (T <= 256, S <= 64, R_max <= 64)";
     }
     return "unknown status";
 }

@@ -23,7 +23,7 @@ _c_size_t = ctypes.c_size_t
 STATUS = {
     0: "LORA_OK", -1: "LORA_EINVAL", -2: "LORA_ESLOT", -3: "LORA_ERANK", -4: "LORA_ESHAPE",
     -5: "LORA_ENONFINITE", -6: "LORA_ECUDA", -7: "LORA_EIDRANGE", -8: "LORA_ESPACE",
-    -9: "LORA_ETIMEOUT",
+    -9: "LORA_ETIMEOUT", -10: "LORA_ESCRATCH",
 }
 TILE_ROWS = 16
 
@@ -65,6 +65,8 @@ _SIGS = {
                              ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p]),
     "lora_linear_path": (_c_int, [_c_int, _c_int, _c_int]),
     "lora_profile_gemm_events": (_c_int, [_c_void_p, _c_void_p]),
+    "lora_linear_static_scratch": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(lora_pool),
+                                            _c_void_p, _c_void_p, _c_void_p]),
     "lora_last_device_error": (_c_int, [ctypes.POINTER(_c_int32)]),
     "lora_strerror": (ctypes.c_char_p, [_c_int]),
     "lora_version": (_c_int, []),

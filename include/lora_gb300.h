@@ -49,7 +49,8 @@ typedef enum {
     LORA_ECUDA = -6,       /* a CUDA runtime call or launch failed */
     LORA_EIDRANGE = -7,    /* lora_plan_check: ids outside [0, S) were seen */
     LORA_ESPACE = -8,      /* workspace smaller than lora_plan_workspace_bytes */
-    LORA_ETIMEOUT = -9     /* a kernel gave up a bounded wait (see lora_last_device_error) */
+    LORA_ETIMEOUT = -9,    /* a kernel gave up a bounded wait (see lora_last_device_error) */
+    LORA_ESCRATCH = -10    /* sizes beyond the fixed scratch of lora_linear_static_scratch */
 } lora_status;
 
 /* A slot pool for one adapted linear (the stacked A/B buffers of the vLLM
@@ -173,6 +174,25 @@ int lora_linear_path(int T, int d_in, int d_out);
  * with cudaEventElapsedTime. (NULL, NULL) turns it off. Process-global; not
  * for use while a stream is being captured. */
 lora_status lora_profile_gemm_events(void* start, void* stop);
+
+/* The layer for callers that cannot allocate device memory (no counterpart on
+ * the pages: a convenience of this library). lora_plan + lora_linear need a
+ * caller-allocated plan workspace; some callers cannot provide one - a program
+ * that hands out device memory only from its own arena, a C caller without a
+ * device allocator, a decode loop that cannot pay for cudaMalloc/cudaFree
+ * (which may synchronize the device). This entry point builds the plan from
+ * `ids` ([T] int32 device) and runs the layer with its per-step state kept in
+ * one fixed array inside this library instead: 72 KiB of device memory on every
+ * GPU that loads the library, held until the process exits. Limits: T <= 256,
+ * pool->S <= 64, pool->R_max <= 64; larger sizes return LORA_ESCRATCH and
+ * nothing runs. Other arguments and the result are those of lora_linear with a
+ * plan. The first call on a device looks up the array's device address (with
+ * that device current); make that first call before any stream capture. Every
+ * call shares the one array: calls whose work overlaps on the GPU (different
+ * streams or host threads) race on it. Allocates nothing. */
+lora_status lora_linear_static_scratch(const void* x, const void* W, int T, int d_in, int d_out,
+                                       const lora_pool* pool, const int32_t* ids, void* y,
+                                       void* stream);
 
 /* Error word written by kernels that gave up a bounded wait (0 = none), and
  * reset it. Synchronises the device. */
