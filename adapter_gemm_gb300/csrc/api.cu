@@ -365,8 +365,10 @@ lora_status lora_plan(const int32_t* ids, int T, lora_plan_t* plan, void* stream
     p.S = plan->S;
     plan->ids = ids;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (launch_plan(ids, T, p, st) != cudaSuccess) return LORA_ECUDA;
-    set_last_out(st, nullptr, 0);     // the plan kernel waits for all earlier work
+    // The plan kernel reads the ids before it waits for the kernels ahead of it,
+    // unless they alias the output of the previous lora_linear on this stream.
+    const bool pdl = !overlaps(last_out(st), ids, (size_t)T * 4);
+    if (launch_plan(ids, T, p, pdl, st) != cudaSuccess) return LORA_ECUDA;
     return LORA_OK;
 }
 
@@ -433,7 +435,10 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         sa.K = d_in;
         sa.R_max = pool->R_max;
         sa.x_early = x_early ? 1 : 0;
-        const bool by_slot = path == 0;
+        // Small decode batches group rows by slot inside the shrink, so it need
+        // not wait for the plan kernel; larger ones use the plan's work tiles,
+        // which spread a heavily used adapter's rows over many CTAs.
+        const bool by_slot = path == 0 && T <= kBySlotMaxT;
         const int grid_x = by_slot ? pool->S - 1 : plan->max_tiles;
         sa.ks = by_slot ? slot_splits(grid_x, d_in) : shrink_splits(plan->max_tiles, d_in);
         if (launch_shrink(sa, grid_x, by_slot, pdl, st) != cudaSuccess) return LORA_ECUDA;

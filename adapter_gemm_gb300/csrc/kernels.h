@@ -12,6 +12,7 @@ constexpr int kMaxSlots = 1024;     // one plan thread per slot in the scans
 constexpr int kMaxRank = 128;       // R_max cap: shrink keeps R_max/8 MMA column tiles
 constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 256)
 constexpr int kStageURank = 64;     // the skinny epilogue stages U rows of rank <= 64
+constexpr int kBySlotMaxT = 64;     // up to this many rows the shrink groups rows by slot itself
 
 struct PlanArgs {
     int32_t* slot_of_token;
@@ -72,7 +73,7 @@ struct WideArgs {
     int m_tiles, n_tiles, kb_total;
 };
 
-cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, cudaStream_t stream);
+cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream);
 cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyArgs& a,
                           bool pdl, int num_sms, cudaStream_t stream);

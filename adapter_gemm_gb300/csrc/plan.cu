@@ -86,7 +86,6 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
         const bool valid = t < hi;
         int s = valid ? ids[t] : 0;
         if (valid && (s < 0 || s >= S)) { ++n_bad; s = 0; }
-        if (valid) p.slot_of_token[t] = s;
         const int key = valid ? s : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (valid && lane == __ffs(peers) - 1) wc[warp * S + s] += __popc(peers);
@@ -95,6 +94,9 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) n_bad += __shfl_xor_sync(0xffffffffu, n_bad, d);
     if (lane == 0 && n_bad) atomicAdd(&s_invalid, n_bad);
+    // Everything so far read only the ids; the plan arrays may still be read by
+    // the kernels ahead of this one, so wait for them before writing any.
+    pdl_wait();
     __syncthreads();
 
     // Per slot: exclusive prefix over warps (in place) and the slot total.
@@ -127,6 +129,7 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
         const bool valid = t < hi;
         int s = valid ? ids[t] : 0;
         if (valid && (s < 0 || s >= S)) s = 0;
+        if (valid) p.slot_of_token[t] = s;
         const int key = valid ? s : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (valid) {
@@ -160,12 +163,21 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     }
 }
 
-cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, cudaStream_t stream) {
+cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream) {
     const size_t smem = sizeof(int) * (size_t)(kPlanWarps + 1) * p.S;
     cudaError_t e = ensure_smem_attr((const void*)plan_kernel, 0, smem);
     if (e != cudaSuccess) return e;
-    plan_kernel<<<1, kPlanThreads, smem, stream>>>(ids, T, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kPlanThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, plan_kernel, ids, T, p);
 }
 
 }  // namespace lora

@@ -54,26 +54,39 @@ __device__ __forceinline__ void shrink_accumulate(float (&acc)[NT][4], const __n
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
     const uint4 zero4 = make_uint4(0, 0, 0, 0);
+    // KU K steps per batch: every load of the batch is issued before its MMAs,
+    // so one batch costs one memory round trip.
+    constexpr int KU = NT >= 8 ? 1 : 8 / NT;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll 2
-    for (int k = k_lo + warp * 32; k < k_hi; k += 4 * 32) {
-        const int kk = k + 8 * q;
-        const bool kv = kk < k_hi;
-        const uint4 xa = (v0 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr0 + kk)) : zero4;
-        const uint4 xb = (v1 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr1 + kk)) : zero4;
-        if (kv) {
-            if (xs0 && v0) *reinterpret_cast<uint4*>(xs0 + kk) = xa;
-            if (xs1 && v1) *reinterpret_cast<uint4*>(xs1 + kk) = xb;
-        }
-        if (do_mma) {
+    for (int k = k_lo + warp * 32; k < k_hi; k += 4 * 32 * KU) {
+        uint4 xa[KU], xb[KU], bw[KU][NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                if (nt < nt_used) {
-                    const __nv_bfloat16* arow = Ablk + (size_t)(nt * 8 + g) * K;
-                    const uint4 bw = kv ? __ldg(reinterpret_cast<const uint4*>(arow + kk)) : zero4;
-                    mma_bf16_16816(acc[nt], xa.x, xb.x, xa.y, xb.y, bw.x, bw.y);
-                    mma_bf16_16816(acc[nt], xa.z, xb.z, xa.w, xb.w, bw.z, bw.w);
+        for (int u = 0; u < KU; ++u) {
+            const int kk = k + u * 4 * 32 + 8 * q;
+            const bool kv = kk < k_hi;
+            xa[u] = (v0 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr0 + kk)) : zero4;
+            xb[u] = (v1 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr1 + kk)) : zero4;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                bw[u][nt] = (do_mma && nt < nt_used && kv)
+                                ? __ldg(reinterpret_cast<const uint4*>(Ablk + (size_t)(nt * 8 + g) * K + kk))
+                                : zero4;
+        }
+#pragma unroll
+        for (int u = 0; u < KU; ++u) {
+            const int kk = k + u * 4 * 32 + 8 * q;
+            if (kk < k_hi) {
+                if (xs0 && v0) *reinterpret_cast<uint4*>(xs0 + kk) = xa[u];
+                if (xs1 && v1) *reinterpret_cast<uint4*>(xs1 + kk) = xb[u];
+            }
+            if (do_mma) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    if (nt < nt_used) {
+                        mma_bf16_16816(acc[nt], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bw[u][nt].x, bw[u][nt].y);
+                        mma_bf16_16816(acc[nt], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bw[u][nt].z, bw[u][nt].w);
+                    }
                 }
             }
         }
@@ -82,11 +95,14 @@ __device__ __forceinline__ void shrink_accumulate(float (&acc)[NT][4], const __n
 
 // Sum the group's partials over the 4 warps and the cluster's ks CTAs, in a
 // fixed order, scale, and store U rows: row i of the group is token tok[i]
-// (i < n). The caller must have waited for earlier readers of U.
+// (i < n). Rank c of the cluster owns rows [c*16/ks, (c+1)*16/ks): every CTA
+// pushes its partial of those rows into the owner's `recv` (plain stores into
+// the peer's shared memory), then the owner sums what it received in rank
+// order. The caller must have waited for earlier readers of U.
 template <int NT>
 __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], float (*part)[16][NT * 8 + 1],
-                                                    float (*cta_sum)[NT * 8 + 1], const int* tok, int n,
-                                                    int rc8, float sc, float* U, int R_max, int ks) {
+                                                    float* recv, const int* tok, int n, int rc8, float sc,
+                                                    float* U, int R_max, int ks) {
     constexpr int RC = NT * 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -100,40 +116,34 @@ __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], f
         part[warp][g + 8][col + 1] = acc[nt][3];
     }
     __syncthreads();
-    for (int el = threadIdx.x; el < 16 * RC; el += kShrinkThreads) {
-        const int row = el / RC, col = el % RC;
-        cta_sum[row][col] = ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) + part[3][row][col];
-    }
-    __syncthreads();
     if (ks > 1) {
-        // Rank c finishes rows [c*16/ks, (c+1)*16/ks): it requests every rank's
-        // partial of those rows at once, then sums in rank order.
         cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();                               // every rank's cta_sum is complete
-        const float* peer[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) peer[c] = c < ks ? cluster.map_shared_rank(&cta_sum[0][0], c) : &cta_sum[0][0];
         const int rows_per = 16 / ks;
-        const int row0 = (int)cluster.block_rank() * rows_per;
+        const int me = (int)cluster.block_rank();
+        cluster.sync();                               // owners are done with recv of an earlier group
+        const uint32_t rbase = smem_u32(recv);
+        for (int el = threadIdx.x; el < 16 * rc8; el += kShrinkThreads) {
+            const int row = el / rc8, col = el % rc8;
+            const float v = ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) + part[3][row][col];
+            const int owner = row / rows_per, lr = row % rows_per;
+            st_cluster_f32(mapa_shared(rbase, (uint32_t)owner) + (uint32_t)(((me * rows_per + lr) * RC + col) * 4), v);
+        }
+        cluster.sync();                               // every push has landed
         for (int el = threadIdx.x; el < rows_per * rc8; el += kShrinkThreads) {
-            const int row = row0 + el / rc8, col = el % rc8;
-            float p[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) p[c] = c < ks ? peer[c][row * (RC + 1) + col] : 0.f;
-            float v = p[0];
-#pragma unroll
-            for (int c = 1; c < 8; ++c)
-                if (c < ks) v += p[c];
+            const int lr = el / rc8, col = el % rc8;
+            float v = recv[lr * RC + col];
+            for (int z = 1; z < ks; ++z) v += recv[(z * rows_per + lr) * RC + col];
+            const int row = me * rows_per + lr;
             if (row < n) U[(size_t)tok[row] * R_max + col] = sc * v;
         }
-        cluster.sync();                               // keep shared memory alive for the peers
     } else {
         for (int el = threadIdx.x; el < 16 * rc8; el += kShrinkThreads) {
             const int row = el / rc8, col = el % rc8;
-            if (row < n) U[(size_t)tok[row] * R_max + col] = sc * cta_sum[row][col];
+            const float v = ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) + part[3][row][col];
+            if (row < n) U[(size_t)tok[row] * R_max + col] = sc * v;
         }
-        __syncthreads();
     }
+    __syncthreads();                                  // part / recv are reused by the next group
 }
 
 // One CTA (cluster of ks CTAs along K) per plan work tile: up to 16 rows of
@@ -144,7 +154,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
 shrink_tiles_kernel(ShrinkArgs a) {
     constexpr int RC = NT * 8;
     __shared__ float part[4][16][RC + 1];
-    __shared__ float cta_sum[16][RC + 1];
+    __shared__ float recv[16 * RC];
     __shared__ int tok[16];
 
     // The next kernel may start its prologue; this one needs the plan, and the
@@ -180,7 +190,7 @@ shrink_tiles_kernel(ShrinkArgs a) {
                           a.A + (size_t)(do_mma ? s : 0) * a.R_max * K, K, (r + 7) >> 3, k_lo, k_hi, do_mma);
     if (!do_mma) return;                              // copy-only tiles are done
     __syncthreads();                                  // tok[] is visible
-    shrink_reduce_store<NT>(acc, part, cta_sum, tok, e - b, ((r + 7) >> 3) * 8, a.scale[s], a.U, a.R_max, a.ks);
+    shrink_reduce_store<NT>(acc, part, recv, tok, e - b, ((r + 7) >> 3) * 8, a.scale[s], a.U, a.R_max, a.ks);
 }
 
 // Decode-sized batches (T <= 256): one cluster of ks CTAs (split along K) per
@@ -193,7 +203,7 @@ __global__ void __launch_bounds__(kShrinkThreads)
 shrink_by_slot_kernel(ShrinkArgs a) {
     constexpr int RC = NT * 8;
     __shared__ float part[4][16][RC + 1];
-    __shared__ float cta_sum[16][RC + 1];
+    __shared__ float recv[16 * RC];
     __shared__ int rows[kSkinnyMaxT];
     __shared__ int wtot[4];
 
@@ -203,8 +213,10 @@ shrink_by_slot_kernel(ShrinkArgs a) {
     // rows on slot s, ascending: two ids per thread, then a block prefix sum
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t_a = 2 * tid, t_b = 2 * tid + 1;
-    const int f_a = (r > 0 && t_a < a.T && a.ids[t_a] == s) ? 1 : 0;
-    const int f_b = (r > 0 && t_b < a.T && a.ids[t_b] == s) ? 1 : 0;
+    const int id_a = t_a < a.T ? a.ids[t_a] : -1;   // loaded alongside the rank, not after it
+    const int id_b = t_b < a.T ? a.ids[t_b] : -1;
+    const int f_a = (r > 0 && id_a == s) ? 1 : 0;
+    const int f_b = (r > 0 && id_b == s) ? 1 : 0;
     int inc = f_a + f_b;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -248,7 +260,7 @@ shrink_by_slot_kernel(ShrinkArgs a) {
             pdl_wait();
             waited = true;
         }
-        shrink_reduce_store<NT>(acc, part, cta_sum, rows + g0, min(16, n_rows - g0), nt_used * 8, sc, a.U,
+        shrink_reduce_store<NT>(acc, part, recv, rows + g0, min(16, n_rows - g0), nt_used * 8, sc, a.U,
                                 a.R_max, a.ks);
     }
 }
