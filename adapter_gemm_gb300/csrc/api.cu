@@ -83,6 +83,24 @@ bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 tensor of rank 2 or 3 (dims innermost first, row pitches in bytes),
+// tiled in boxes `box`, with the given swizzle, zero fill outside the tensor.
+bool make_tmap_nd(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* pitches,
+                  const uint32_t* box, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t d[3], st[2];
+    cuuint32_t b[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) st[i] = pitches[i];
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), d, st, b, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -97,7 +115,9 @@ int max_tiles_for(int T, int S) { return (T + kTileRows - 1) / kTileRows + S; }
 bool plan_needs_xsorted(int T) { return T > kSkinnyMaxT; }
 
 // Sub-buffer sizes of the plan workspace, in carve order.
-void plan_layout(int T, int S, int R_max, int d_in_cap, size_t sizes[11]) {
+constexpr int kPlanParts = 14;
+
+void plan_layout(int T, int S, int R_max, int d_in_cap, size_t sizes[kPlanParts]) {
     const int mt = max_tiles_for(T, S);
     sizes[0] = (size_t)T * 4;                 // slot_of_token
     sizes[1] = (size_t)T * 4;                 // token_order
@@ -110,6 +130,12 @@ void plan_layout(int T, int S, int R_max, int d_in_cap, size_t sizes[11]) {
     sizes[8] = 4;                             // n_invalid
     sizes[9] = (size_t)T * R_max * 4;         // U
     sizes[10] = plan_needs_xsorted(T) ? (size_t)T * d_in_cap * 2 : 0;   // x_sorted
+    const bool wide = plan_needs_xsorted(T);
+    const int m_blocks = (T + 127) / 128;
+    const int r16 = (R_max + 15) / 16 * 16;
+    sizes[11] = wide ? (size_t)T * 2 * r16 * 2 : 0;                       // U_hl
+    sizes[12] = wide ? (size_t)(m_blocks + 1) * 4 : 0;                    // mt_ptr
+    sizes[13] = wide ? (size_t)(m_blocks + S) * 16 : 0;                   // mt_seg
 }
 
 struct SkinnyConfig { int TN, stages, ks, can_stage_u; size_t smem; };
@@ -240,10 +266,10 @@ const char* lora_strerror(lora_status s) {
 
 size_t lora_plan_workspace_bytes(int T, int S, int R_max, int d_in_cap) {
     if (T < 0 || !valid_sizes(S, R_max, d_in_cap)) return 0;
-    size_t sizes[11];
+    size_t sizes[kPlanParts];
     plan_layout(T, S, R_max, d_in_cap, sizes);
     size_t total = 0;
-    for (int i = 0; i < 11; ++i) total += align_up(sizes[i], 256);
+    for (int i = 0; i < kPlanParts; ++i) total += align_up(sizes[i], 256);
     return total;
 }
 
@@ -256,14 +282,14 @@ lora_status lora_plan_init(lora_plan_t* plan, void* workspace, size_t bytes, int
     if (d_in_cap < 8 || (d_in_cap % 8) != 0) return LORA_ESHAPE;
     const size_t need = lora_plan_workspace_bytes(T, S, R_max, d_in_cap);
     if (bytes < need) return LORA_ESPACE;
-    size_t sizes[11];
+    size_t sizes[kPlanParts];
     plan_layout(T, S, R_max, d_in_cap, sizes);
     uint8_t* p = static_cast<uint8_t*>(workspace);
-    void* ptrs[11];
-    for (int i = 0; i < 11; ++i) {
+    void* ptrs[kPlanParts];
+    for (int i = 0; i < kPlanParts; ++i) {
         // zero-sized arrays of an empty batch still get a (never read) address;
-        // only x_sorted is null when the plan carries none
-        ptrs[i] = (sizes[i] || i != 10) ? p : nullptr;
+        // the arrays of the wide path (x_sorted onwards) are null when absent
+        ptrs[i] = (sizes[i] || i < 10) ? p : nullptr;
         p += align_up(sizes[i], 256);
     }
     plan->slot_of_token = static_cast<int32_t*>(ptrs[0]);
@@ -277,6 +303,10 @@ lora_status lora_plan_init(lora_plan_t* plan, void* workspace, size_t bytes, int
     plan->n_invalid = static_cast<int32_t*>(ptrs[8]);
     plan->U = static_cast<float*>(ptrs[9]);
     plan->x_sorted = ptrs[10];
+    plan->U_hl = ptrs[11];
+    plan->mt_ptr = static_cast<int32_t*>(ptrs[12]);
+    plan->mt_seg = static_cast<int32_t*>(ptrs[13]);
+    plan->ids = nullptr;
     plan->T = T;
     plan->S = S;
     plan->R_max = R_max;
@@ -362,6 +392,8 @@ lora_status lora_plan(const int32_t* ids, int T, lora_plan_t* plan, void* stream
     p.tiles = plan->tiles;
     p.n_tiles = plan->n_tiles;
     p.n_invalid = plan->n_invalid;
+    p.mt_ptr = plan->mt_ptr;
+    p.mt_seg = plan->mt_seg;
     p.S = plan->S;
     plan->ids = ids;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -429,7 +461,9 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         sa.token_order = plan->token_order;
         sa.tiles = reinterpret_cast<const int4*>(plan->tiles);
         sa.n_tiles = plan->n_tiles;
-        sa.U = plan->U;
+        sa.U = path == 1 ? nullptr : plan->U;
+        sa.U_hl = path == 1 ? static_cast<__nv_bfloat16*>(plan->U_hl) : nullptr;
+        sa.R16 = (pool->R_max + 15) / 16 * 16;
         sa.x_sorted = path == 1 ? static_cast<__nv_bfloat16*>(plan->x_sorted) : nullptr;
         sa.T = T;
         sa.K = d_in;
@@ -475,14 +509,33 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         if (launch_skinny(tmW, tmX, a, pdl, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;
-        CUtensorMap tmA, tmB;
+        CUtensorMap tmA, tmB, tmU, tmBs;
         if (!make_tmap(&tmA, A, (uint64_t)d_in, (uint64_t)T, 64, 128) ||
             !make_tmap(&tmB, W, (uint64_t)d_in, (uint64_t)d_out, 64, 256))
             return LORA_ECUDA;
+        const int R16 = plan ? (pool->R_max + 15) / 16 * 16 : 16;
+        if (plan) {
+            // expand operands: U hi|lo [T][2*R16] in plan order, B_pool [S][N][R_max]
+            const uint64_t du[2] = {(uint64_t)2 * R16, (uint64_t)T}, pu[1] = {(uint64_t)2 * R16 * 2};
+            const uint32_t bu[2] = {16, 128};
+            const uint64_t db[3] = {(uint64_t)pool->R_max, (uint64_t)d_out, (uint64_t)pool->S};
+            const uint64_t pb[2] = {(uint64_t)pool->R_max * 2, (uint64_t)d_out * pool->R_max * 2};
+            const uint32_t bb[3] = {16, 256, 1};
+            if (!make_tmap_nd(&tmU, plan->U_hl, 2, du, pu, bu, CU_TENSOR_MAP_SWIZZLE_32B) ||
+                !make_tmap_nd(&tmBs, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B))
+                return LORA_ECUDA;
+        } else {
+            tmU = tmA;                 // unused without a plan
+            tmBs = tmB;
+        }
         WideArgs a;
         a.y = static_cast<__nv_bfloat16*>(y);
         a.token_order = plan ? plan->token_order : nullptr;
-        a.ex = ex;
+        a.mt_ptr = plan ? plan->mt_ptr : nullptr;
+        a.mt_seg = plan ? reinterpret_cast<const int4*>(plan->mt_seg) : nullptr;
+        a.rank = plan ? pool->rank : nullptr;
+        a.R_max = plan ? pool->R_max : 0;
+        a.R16 = R16;
         a.T = T;
         a.K = d_in;
         a.N = d_out;
@@ -491,7 +544,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.kb_total = (d_in + 63) / 64;
         int grid = a.m_tiles * a.n_tiles;
         if (grid > num_sms()) grid = num_sms();
-        if (launch_wide(tmA, tmB, a, pdl, grid, st) != cudaSuccess) return LORA_ECUDA;
+        if (launch_wide(tmA, tmB, tmU, tmBs, a, pdl, grid, st) != cudaSuccess) return LORA_ECUDA;
     }
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;
     set_last_out(st, y, (size_t)T * d_out * 2);

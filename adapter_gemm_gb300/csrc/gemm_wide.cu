@@ -1,21 +1,28 @@
 // The layer for prefill-sized batches: a persistent tcgen05 GEMM over 128x256
-// output tiles with the expand half of SGMV fused into its epilogue.
+// output tiles, with the expand half of SGMV done on the tensor cores too.
 //
-//   acc[i, n] = sum_k xs[i, k] W[n, k]            (tensor cores, TMEM, fp32)
-//   y[t_i, n] = bf16(acc[i, n] + [s != 0] sum_j U[t_i, j] B[s, n, j])
+//   acc[i, n]  = sum_k xs[i, k] W[n, k]                          (K loop)
+//   acc[i, n] += sum_j U[i, j] B[s, n, j]   for rows i of slot s  (expand steps)
+//   y[t_i, n]  = bf16(acc[i, n])
 //
-// With a plan, xs is x_sorted (rows in plan order, written by the shrink pass)
-// and t_i = token_order[i]: rows of one adapter are contiguous, so a 128-row
-// tile touches few adapters and the epilogue's B reads stay in L1. The row's
-// result is scattered back to its original position, written once. Without a
-// plan xs = x and t_i = i (the base-only run the slot-0 rows are compared with).
+// With a plan, xs is x_sorted (rows in plan order, written by the shrink pass),
+// t_i = token_order[i], and the rows of one adapter are contiguous. After a
+// tile's K loop, each adapter segment that crosses the tile adds its low-rank
+// term with one extra MMA pair per 16 ranks: A = the tile's U rows (the shrink's
+// fp32 result split into bf16 hi + lo, so the product keeps about 16 bits of
+// U), B = the adapter's B rows for the tile's 256 output columns, and the MMA's
+// output-lane mask switched on only for the segment's rows, so every other row
+// of the accumulator - slot 0 included - is left exactly as the K loop made it.
+// The epilogue then only rounds and scatters each row back to its token, once.
+// Without a plan xs = x, t_i = i, and there are no expand steps.
 //
-// One CTA per SM. Warp 0 lane 0 streams A (128 x 64) and B (256 x 64) tiles
-// with TMA into a 4-stage ring; warp 1 lane 0 issues tcgen05.mma (M=128,
-// N=256, K=16) into one of two 256-column TMEM accumulators; warp 2 owns the
-// 512-column TMEM allocation; warps 4..7 drain the other accumulator (warp w
-// reads TMEM lanes 32(w-4)..), add the correction, round and store, while the
-// next tile's MMAs run.
+// One CTA per SM. Warp 0 lane 0 streams A (128 x 64) and B (256 x 64) tiles,
+// and the expand operands (U 128 x 16 hi and lo, B_s 256 x 16, 32-byte
+// swizzle), with TMA into a 4-stage ring; warp 1 lane 0 issues tcgen05.mma
+// (M=128, N=256, K=16) into one of two 256-column TMEM accumulators; warp 2
+// owns the 512-column TMEM allocation; warps 4..7 drain the other accumulator
+// (warp w reads TMEM lanes 32(w-4)..), round and store, while the next tile's
+// MMAs run.
 #include <cstdint>
 #include "ptx.cuh"
 #include "kernels.h"
@@ -28,57 +35,39 @@ constexpr int kWdStages = 4;
 constexpr uint32_t kWdABytes = kWdBM * kWdBK * 2;     // 16 KB
 constexpr uint32_t kWdBBytes = kWdBN * kWdBK * 2;     // 32 KB
 constexpr uint32_t kWdStageBytes = kWdABytes + kWdBBytes;
-constexpr size_t kWdSmem = 1024 + (size_t)kWdStageBytes * kWdStages + 256;
-
-// d + u[off..off+8) . b (8 packed bf16), j ascending; u held in registers.
-__device__ __forceinline__ float dot8r(const float (&u)[16], const int off, const uint4 b, float d) {
-    d = fmaf(u[off + 0], bf16lo(b.x), d);
-    d = fmaf(u[off + 1], bf16hi(b.x), d);
-    d = fmaf(u[off + 2], bf16lo(b.y), d);
-    d = fmaf(u[off + 3], bf16hi(b.y), d);
-    d = fmaf(u[off + 4], bf16lo(b.z), d);
-    d = fmaf(u[off + 5], bf16hi(b.z), d);
-    d = fmaf(u[off + 6], bf16lo(b.w), d);
-    d = fmaf(u[off + 7], bf16hi(b.w), d);
-    return d;
-}
-
-// d + sum_{j0 <= j < r8} u[j] b[j] for ranks beyond the register-held 16.
-__device__ __noinline__ float wd_expand_dot_from(const float* __restrict__ u, const __nv_bfloat16* __restrict__ brow,
-                                                 int j0, int r8, float d) {
-    for (int j = j0; j < r8; j += 8) {
-        const uint4 b = __ldg(reinterpret_cast<const uint4*>(brow + j));
-        const float4 u0 = __ldg(reinterpret_cast<const float4*>(u + j));
-        const float4 u1 = __ldg(reinterpret_cast<const float4*>(u + j + 4));
-        d = fmaf(u0.x, bf16lo(b.x), d);
-        d = fmaf(u0.y, bf16hi(b.x), d);
-        d = fmaf(u0.z, bf16lo(b.y), d);
-        d = fmaf(u0.w, bf16hi(b.y), d);
-        d = fmaf(u1.x, bf16lo(b.z), d);
-        d = fmaf(u1.y, bf16hi(b.z), d);
-        d = fmaf(u1.z, bf16lo(b.w), d);
-        d = fmaf(u1.w, bf16hi(b.w), d);
-    }
-    return d;
-}
+constexpr uint32_t kXuBytes = kWdBM * 16 * 2;         // expand step: U tile, 4 KB (hi or lo)
+constexpr uint32_t kXbBytes = kWdBN * 16 * 2;         // expand step: B_s tile, 8 KB
+constexpr int kMaxSegs = kWdBM;                       // segments crossing one 128-row tile
+// ring | barriers (256 B) | two expand lists of kMaxSegs int4 + counts
+constexpr size_t kWdSmem = 1024 + (size_t)kWdStageBytes * kWdStages + 256 + 2 * (size_t)kMaxSegs * 16 + 16;
 
 __global__ void __launch_bounds__(kWdThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmBs,
                  WideArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)kWdStageBytes * kWdStages);
     uint64_t* empty = full + kWdStages;
     uint64_t* tfull = empty + kWdStages;      // [2] accumulator ready
     uint64_t* tempty = tfull + 2;             // [2] accumulator drained
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* lfull = tempty + 2;             // [2] expand list written
+    uint64_t* lempty = lfull + 2;             // [2] expand list consumed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lempty + 2);
+    int4* xlist = reinterpret_cast<int4*>(base + (size_t)kWdStageBytes * kWdStages + 256);   // [2][kMaxSegs]
+    int* xcount = reinterpret_cast<int*>(xlist + 2 * kMaxSegs);                               // [2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles_total = a.m_tiles * a.n_tiles;
+    const bool expand = a.mt_ptr != nullptr;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (expand) {
+            tma_prefetch_desc(&tmU);
+            tma_prefetch_desc(&tmBs);
+        }
         for (int i = 0; i < kWdStages; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
             mbar_init(smem_u32(&empty[i]), 1);
@@ -86,6 +75,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&tfull[i]), 1);
             mbar_init(smem_u32(&tempty[i]), 128);
+            mbar_init(smem_u32(&lfull[i]), 1);
+            mbar_init(smem_u32(&lempty[i]), 1);
         }
         fence_mbar_init();
     }
@@ -104,22 +95,52 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0) {
         if (lane == 0) {
             // TMA producer over this CTA's tiles.
-            int it = 0, issued = 0;
+            int it = 0, issued = 0, lt = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x) {
-                const int m0 = (tile % a.m_tiles) * kWdBM;
+            for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x, ++lt) {
+                const int mt = tile % a.m_tiles;
+                const int m0 = mt * kWdBM;
                 const int n0 = (tile / a.m_tiles) * kWdBN;
                 for (int kb = 0; kb < a.kb_total; ++kb, ++it) {
                     const int st = it % kWdStages;
                     const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                     if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
                     const uint32_t sA = smem_u32(base + (size_t)st * kWdStageBytes);
-                    const uint32_t sB = sA + kWdABytes;
                     const uint32_t fb = smem_u32(&full[st]);
                     mbar_arrive_expect_tx(fb, kWdStageBytes);
                     tma_load_2d(sA, &tmA, fb, kb * kWdBK, m0);
-                    tma_load_2d(sB, &tmB, fb, kb * kWdBK, n0);
+                    tma_load_2d(sA + kWdABytes, &tmB, fb, kb * kWdBK, n0);
                     ++issued;
+                }
+                if (!expand || !ok) continue;
+                // The tile's expand list: adapter segments crossing rows
+                // [m0, m0 + 128) with a nonzero rank, and 16-rank steps each.
+                const int as = lt & 1;
+                const uint32_t use = (uint32_t)(lt >> 1);
+                if (!mbar_wait(smem_u32(&lempty[as]), (use & 1u) ^ 1u, kErrEmptyWait)) { ok = false; break; }
+                const int e0 = a.mt_ptr[mt], e1 = a.mt_ptr[mt + 1];
+                int ns = 0;
+                for (int e = e0; e < e1 && ns < kMaxSegs; ++e) {
+                    const int4 sg = a.mt_seg[e];
+                    const int r = min(a.rank[sg.x], a.R_max);
+                    if (r > 0) xlist[as * kMaxSegs + ns++] = make_int4(sg.x, sg.y, sg.z, (r + 15) >> 4);
+                }
+                xcount[as] = ns;
+                mbar_arrive(smem_u32(&lfull[as]));
+                for (int q = 0; q < ns && ok; ++q) {
+                    const int4 sg = xlist[as * kMaxSegs + q];
+                    for (int ks = 0; ks < sg.w; ++ks, ++it) {
+                        const int st = it % kWdStages;
+                        const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
+                        if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
+                        const uint32_t sU = smem_u32(base + (size_t)st * kWdStageBytes);
+                        const uint32_t fb = smem_u32(&full[st]);
+                        mbar_arrive_expect_tx(fb, 2 * kXuBytes + kXbBytes);
+                        tma_load_2d(sU, &tmU, fb, ks * 16, m0);                       // U hi
+                        tma_load_2d(sU + kXuBytes, &tmU, fb, a.R16 + ks * 16, m0);    // U lo
+                        tma_load_3d(sU + 2 * kXuBytes, &tmBs, fb, ks * 16, n0, sg.x);  // B_s
+                        ++issued;
+                    }
                 }
             }
             // Let every copy this thread started land before the CTA can exit.
@@ -152,12 +173,41 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                                     (kb > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(smem_u32(&empty[st]));
                 }
+                if (expand && ok) {
+                    if (!mbar_wait(smem_u32(&lfull[as]), use & 1u, kErrFullWait)) { ok = false; break; }
+                    const int ns = xcount[as];
+                    for (int q = 0; q < ns && ok; ++q) {
+                        const int4 sg = xlist[as * kMaxSegs + q];
+                        // lanes (rows) outside [sg.y, sg.z) keep their value
+                        uint32_t dis[4];
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int lo = max(sg.y, 32 * w), hi = min(sg.z, 32 * w + 32);
+                            const uint32_t on = (hi <= lo) ? 0u
+                                               : (hi - lo == 32 ? 0xFFFFFFFFu
+                                                                : (((1u << (hi - lo)) - 1u) << (lo - 32 * w)));
+                            dis[w] = ~on;
+                        }
+                        for (int ks = 0; ks < sg.w; ++ks, ++it) {
+                            const int st = it % kWdStages;
+                            const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
+                            if (!mbar_wait(smem_u32(&full[st]), ph, kErrFullWait)) { ok = false; break; }
+                            tc_fence_after();
+                            const uint32_t sU = smem_u32(base + (size_t)st * kWdStageBytes);
+                            const uint64_t bdesc = sdesc_sw32(sU + 2 * kXuBytes);
+                            tc_mma_bf16_masked(d, sdesc_sw32(sU), bdesc, idesc, dis);
+                            tc_mma_bf16_masked(d, sdesc_sw32(sU + kXuBytes), bdesc, idesc, dis);
+                            tc_commit(smem_u32(&empty[st]));
+                        }
+                    }
+                    mbar_arrive(smem_u32(&lempty[as]));
+                }
                 tc_commit(smem_u32(&tfull[as]));
             }
         }
         __syncwarp();
     } else if (warp >= 4) {
-        // Epilogue warps.
+        // Epilogue warps: TMEM -> bf16 -> the row's token in y.
         const int ew = warp - 4;
         const int row = ew * 32 + lane;
         int lt = 0;
@@ -170,55 +220,15 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (!ready) break;     // the MMA side gave up; the error word is set
             tc_fence_after();
             const int i = m0 + row;
-            const bool valid = ready && i < a.T;
+            const bool valid = i < a.T;
             const int t = valid ? (a.token_order ? a.token_order[i] : i) : 0;
-            int s = 0, r8 = 0;
-            if (valid && a.ex.slot_of_token != nullptr) {
-                s = a.ex.slot_of_token[t];
-                if (s > 0) {
-                    const int r = min(__ldg(&a.ex.rank[s]), a.ex.R_max);
-                    r8 = r > 0 ? (r + 7) & ~7 : 0;
-                }
-            }
-            const float* urow = a.ex.U + (size_t)t * a.ex.R_max;
             __nv_bfloat16* yrow = a.y + (size_t)t * a.N;
-            // The row's first 16 U values stay in registers for the whole tile.
-            float u[16];
-#pragma unroll
-            for (int j4 = 0; j4 < 4; ++j4) {
-                const float4 f = (r8 > j4 * 4) ? __ldg(reinterpret_cast<const float4*>(urow) + j4)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                u[4 * j4] = f.x; u[4 * j4 + 1] = f.y; u[4 * j4 + 2] = f.z; u[4 * j4 + 3] = f.w;
-            }
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(as * kWdBN);
             for (int c = 0; c < kWdBN; c += 16) {
                 float v[16];
                 tc_ld16(tbase + (uint32_t)c, v);
                 const int n = n0 + c;
                 if (valid && n < a.N) {
-                    if (r8 > 0) {
-                        const __nv_bfloat16* bblk = a.ex.B + ((size_t)s * a.N + n) * a.ex.R_max;
-#pragma unroll
-                        for (int q0 = 0; q0 < 16; q0 += 4) {
-                            uint4 b0[4], b1[4];
-#pragma unroll
-                            for (int qq = 0; qq < 4; ++qq) {
-                                const bool in = n + q0 + qq < a.N;
-                                const __nv_bfloat16* br = bblk + (size_t)(q0 + qq) * a.ex.R_max;
-                                b0[qq] = in ? __ldg(reinterpret_cast<const uint4*>(br)) : make_uint4(0, 0, 0, 0);
-                                b1[qq] = (in && r8 > 8) ? __ldg(reinterpret_cast<const uint4*>(br + 8))
-                                                        : make_uint4(0, 0, 0, 0);
-                            }
-#pragma unroll
-                            for (int qq = 0; qq < 4; ++qq) {
-                                float d = dot8r(u, 0, b0[qq], 0.f);
-                                d = dot8r(u, 8, b1[qq], d);
-                                if (r8 > 16)
-                                    d = wd_expand_dot_from(urow, bblk + (size_t)(q0 + qq) * a.ex.R_max, 16, r8, d);
-                                v[q0 + qq] += d;
-                            }
-                        }
-                    }
                     uint4 o0, o1;
                     o0.x = pack_bf16x2(v[0], v[1]);   o0.y = pack_bf16x2(v[2], v[3]);
                     o0.z = pack_bf16x2(v[4], v[5]);   o0.w = pack_bf16x2(v[6], v[7]);
@@ -241,8 +251,8 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
-cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const WideArgs& a,
-                        bool pdl, int grid, cudaStream_t stream) {
+cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
+                        const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attr((const void*)gemm_wide_kernel, 2, kWdSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -259,7 +269,7 @@ cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const Wi
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, tmA, tmB, a);
+    return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, tmA, tmB, tmU, tmBs, a);
 }
 
 cudaError_t wide_take_error(int* code) {

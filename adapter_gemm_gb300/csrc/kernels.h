@@ -24,6 +24,8 @@ struct PlanArgs {
     int32_t* tiles;
     int32_t* n_tiles;
     int32_t* n_invalid;
+    int32_t* mt_ptr;        // [ceil(T/128)+1] or null: per 128-row block, first entry of mt_seg
+    int32_t* mt_seg;        // [ceil(T/128)+S][4]: (slot, first row, end row, block), rows block-local
     int S;
 };
 
@@ -36,7 +38,9 @@ struct ShrinkArgs {
     const int32_t* token_order;  // [T]
     const int4* tiles;           // [max_tiles] (slot, begin, end, 0)
     const int32_t* n_tiles;      // [1]
-    float* U;                    // [T, R_max]
+    float* U;                    // [T, R_max] by token (decode kernels), or null
+    __nv_bfloat16* U_hl;         // [T, 2*R16] bf16 hi | lo in plan order (wide kernel), or null
+    int R16;                     // R_max rounded up to 16
     __nv_bfloat16* x_sorted;     // [T, K] or null
     int T, K, R_max, ks;
     int x_early;                 // x is not written by the kernel this one follows
@@ -68,7 +72,10 @@ struct SkinnyArgs {
 struct WideArgs {
     __nv_bfloat16* y;               // [T, N]
     const int32_t* token_order;     // [T] row of each plan position, or null (identity)
-    ExpandArgs ex;
+    const int32_t* mt_ptr;          // per 128-row block, first adapter segment (null: base only)
+    const int4* mt_seg;             // adapter segments per block (slot, row begin, row end, block)
+    const int32_t* rank;            // [S]
+    int R_max, R16;
     int T, K, N;
     int m_tiles, n_tiles, kb_total;
 };
@@ -77,8 +84,8 @@ cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, 
 cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream);
 cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyArgs& a,
                           bool pdl, int num_sms, cudaStream_t stream);
-cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const WideArgs& a,
-                        bool pdl, int grid, cudaStream_t stream);
+cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
+                        const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
 cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);
 
 // Read and clear the bounded-wait error words of the GEMM translation units.

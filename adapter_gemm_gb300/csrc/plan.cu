@@ -161,6 +161,33 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
         *p.n_tiles = n_tiles;
         *p.n_invalid = s_invalid;
     }
+
+    // For the wide GEMM: per block of 128 plan positions, the adapter segments
+    // that cross it. Each adapter slot contributes one entry per block it
+    // spans; entries follow slot order, so they are also ordered by block.
+    if (p.mt_ptr != nullptr) {
+        const int m_blocks = (T + 127) / 128;
+        const int b = start, e = start + my_cnt;
+        const int n_e = (tid >= 1 && tid < S && my_cnt > 0) ? ((e - 1) / 128 - b / 128 + 1) : 0;
+        int n_ent = 0;
+        const int e_pos = block_exclusive_scan(n_e, warp_tot, n_ent);
+        for (int j = 0; j < n_e; ++j) {
+            const int m = b / 128 + j;
+            reinterpret_cast<int4*>(p.mt_seg)[e_pos + j] =
+                make_int4(tid, max(b, m * 128) - m * 128, min(e, m * 128 + 128) - m * 128, m);
+        }
+        __syncthreads();
+        // mt_ptr[m] = first entry whose block is >= m
+        for (int m = tid; m <= m_blocks; m += kPlanThreads) {
+            int lo = 0, hi = n_ent;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (p.mt_seg[4 * mid + 3] < m) lo = mid + 1;
+                else hi = mid;
+            }
+            p.mt_ptr[m] = lo;
+        }
+    }
 }
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream) {

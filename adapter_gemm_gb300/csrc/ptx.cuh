@@ -95,6 +95,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
         :: "r"(dst), "l"(tmap), "r"(bar), "r"(c0), "r"(c1) : "memory");
 }
 
+// 3-D tiled load of box (c0 innermost, c1, c2) into shared memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar,
+                                            int32_t c0, int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];"
+        :: "r"(dst), "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
 // Prefetch a 2-D tile into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0, int32_t c1) {
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
@@ -137,6 +146,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Same for a K-major operand in the 32-byte swizzle layout written by TMA with
+// CU_TENSOR_MAP_SWIZZLE_32B and a 32-byte (16 x bf16) inner box: rows of 32
+// bytes, 8-row groups 256 bytes apart, swizzle mode 6 (32B).
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+    d |= (uint64_t)(16u >> 4) << 16;                   // leading byte offset (unused)
+    d |= (uint64_t)(256u >> 4) << 32;                  // stride byte offset
+    d |= (uint64_t)1 << 46;                            // descriptor version
+    d |= (uint64_t)6 << 61;                            // 32-byte swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, both
 // operands K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
@@ -173,6 +195,19 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// D[tmem] += A[smem] * B[smem]^T for the rows (TMEM lanes) whose bit in
+// `disable` (4 x 32 bits, lane 32w+i <-> bit i of word w) is clear; the other
+// rows of D are left exactly as they are.
+__device__ __forceinline__ void tc_mma_bf16_masked(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                   uint32_t idesc, const uint32_t (&disable)[4]) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %8, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, {%4, %5, %6, %7}, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc),
+           "r"(disable[0]), "r"(disable[1]), "r"(disable[2]), "r"(disable[3]), "r"(1u) : "memory");
 }
 
 // Arrive once on the barrier when every MMA issued so far by this thread is done.

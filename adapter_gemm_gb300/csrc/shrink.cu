@@ -93,6 +93,22 @@ __device__ __forceinline__ void shrink_accumulate(float (&acc)[NT][4], const __n
     }
 }
 
+// Store U[row, col] = v (already scaled): as fp32 by token into U, or, for the
+// wide GEMM, as a bf16 high part and a bf16 low part (v - high) by plan
+// position into U_hl (columns [0, R16) and [R16, 2*R16)).
+__device__ __forceinline__ void store_u(float* U, __nv_bfloat16* U_hl, const int* tok, int row, int col, float v,
+                                        int R_max, int R16, int pos0) {
+    if (U_hl) {
+        const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+        __nv_bfloat16* dst = U_hl + (size_t)(pos0 + row) * 2 * R16 + col;
+        dst[0] = hi;
+        dst[R16] = lo;
+    } else {
+        U[(size_t)tok[row] * R_max + col] = v;
+    }
+}
+
 // Sum the group's partials over the 4 warps and the cluster's ks CTAs, in a
 // fixed order, scale, and store U rows: row i of the group is token tok[i]
 // (i < n). Rank c of the cluster owns rows [c*16/ks, (c+1)*16/ks): every CTA
@@ -102,7 +118,8 @@ __device__ __forceinline__ void shrink_accumulate(float (&acc)[NT][4], const __n
 template <int NT>
 __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], float (*part)[16][NT * 8 + 1],
                                                     float* recv, const int* tok, int n, int rc8, float sc,
-                                                    float* U, int R_max, int ks) {
+                                                    float* U, int R_max, int ks, __nv_bfloat16* U_hl = nullptr,
+                                                    int R16 = 0, int pos0 = 0) {
     constexpr int RC = NT * 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -129,18 +146,25 @@ __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], f
             st_cluster_f32(mapa_shared(rbase, (uint32_t)owner) + (uint32_t)(((me * rows_per + lr) * RC + col) * 4), v);
         }
         cluster.sync();                               // every push has landed
-        for (int el = threadIdx.x; el < rows_per * rc8; el += kShrinkThreads) {
-            const int lr = el / rc8, col = el % rc8;
-            float v = recv[lr * RC + col];
-            for (int z = 1; z < ks; ++z) v += recv[(z * rows_per + lr) * RC + col];
+        const int wc = U_hl ? R16 : rc8;
+        for (int el = threadIdx.x; el < rows_per * wc; el += kShrinkThreads) {
+            const int lr = el / wc, col = el % wc;
+            float v = 0.f;
+            if (col < rc8) {
+                v = recv[lr * RC + col];
+                for (int z = 1; z < ks; ++z) v += recv[(z * rows_per + lr) * RC + col];
+            }
             const int row = me * rows_per + lr;
-            if (row < n) U[(size_t)tok[row] * R_max + col] = sc * v;
+            if (row < n) store_u(U, U_hl, tok, row, col, col < rc8 ? sc * v : 0.f, R_max, R16, pos0);
         }
     } else {
-        for (int el = threadIdx.x; el < 16 * rc8; el += kShrinkThreads) {
-            const int row = el / rc8, col = el % rc8;
-            const float v = ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) + part[3][row][col];
-            if (row < n) U[(size_t)tok[row] * R_max + col] = sc * v;
+        const int wc = U_hl ? R16 : rc8;
+        for (int el = threadIdx.x; el < 16 * wc; el += kShrinkThreads) {
+            const int row = el / wc, col = el % wc;
+            const float v = col < rc8 ? ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) +
+                                            part[3][row][col]
+                                      : 0.f;
+            if (row < n) store_u(U, U_hl, tok, row, col, sc * v, R_max, R16, pos0);
         }
     }
     __syncthreads();                                  // part / recv are reused by the next group
@@ -190,7 +214,8 @@ shrink_tiles_kernel(ShrinkArgs a) {
                           a.A + (size_t)(do_mma ? s : 0) * a.R_max * K, K, (r + 7) >> 3, k_lo, k_hi, do_mma);
     if (!do_mma) return;                              // copy-only tiles are done
     __syncthreads();                                  // tok[] is visible
-    shrink_reduce_store<NT>(acc, part, recv, tok, e - b, ((r + 7) >> 3) * 8, a.scale[s], a.U, a.R_max, a.ks);
+    shrink_reduce_store<NT>(acc, part, recv, tok, e - b, ((r + 7) >> 3) * 8, a.scale[s], a.U, a.R_max, a.ks,
+                            a.U_hl, a.R16, b);
 }
 
 // Decode-sized batches (T <= 256): one cluster of ks CTAs (split along K) per

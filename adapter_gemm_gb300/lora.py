@@ -45,7 +45,8 @@ class lora_plan_t(ctypes.Structure):
     _fields_ = [("slot_of_token", _c_void_p), ("token_order", _c_void_p), ("counts", _c_void_p),
                 ("indptr", _c_void_p), ("active", _c_void_p), ("n_active", _c_void_p),
                 ("tiles", _c_void_p), ("n_tiles", _c_void_p), ("n_invalid", _c_void_p),
-                ("U", _c_void_p), ("x_sorted", _c_void_p), ("ids", _c_void_p), ("T", _c_int32), ("S", _c_int32),
+                ("U", _c_void_p), ("x_sorted", _c_void_p), ("ids", _c_void_p), ("U_hl", _c_void_p),
+                ("mt_ptr", _c_void_p), ("mt_seg", _c_void_p), ("T", _c_int32), ("S", _c_int32),
                 ("R_max", _c_int32), ("d_in_cap", _c_int32), ("max_tiles", _c_int32)]
 
 

@@ -91,6 +91,13 @@ typedef struct {
  *                         large T; NULL otherwise)
  *   ids           the caller's ids buffer the plan was built from (recorded by
  *                         lora_plan; decode-sized lora_linear calls read it)
+ *   U_hl          [T, 2*R16] bf16: the shrink result in plan order as a bf16
+ *                         high part (columns 0..R16-1) and low part (R16..),
+ *                         R16 = R_max rounded up to 16 (scratch, large T only)
+ *   mt_ptr, mt_seg        per block of 128 plan positions, the adapter
+ *                         segments crossing it: mt_seg[mt_ptr[b] .. mt_ptr[b+1])
+ *                         of (slot, first row, end row, block), rows relative
+ *                         to the block (large T only; NULL otherwise)
  * A plan is only valid for the ids it was built from; rebuild it whenever the
  * ids (or the slot an adapter sits in) change, and keep the ids buffer
  * unchanged while lora_linear calls that use the plan are in flight.
@@ -111,6 +118,9 @@ typedef struct {
     float* U;
     void* x_sorted;
     const int32_t* ids;
+    void* U_hl;
+    int32_t* mt_ptr;
+    int32_t* mt_seg;
     int32_t T, S, R_max, d_in_cap, max_tiles;
 } lora_plan_t;
 
