@@ -74,8 +74,10 @@ __device__ __forceinline__ float expand_dot_from(const float* __restrict__ u, co
 __global__ void __launch_bounds__(kSkThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    SkinnyArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte aligned base, derived by offsetting the shared array itself so
+    // the compiler keeps every pointer below in the shared address space.
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int TN = a.TN;
     const int stages = a.stages;
     const uint32_t x_tile_bytes = (uint32_t)TN * kBK * 2;
@@ -187,12 +189,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     // sums what it received in rank order: a fixed order, and no remote loads.
     const int row = warp * 32 + lane;
     const int rows_per = kWRows / a.ks;
-    bool have = nkb > 0;
-    if (have) {
-        if (!mbar_wait(smem_u32(accf), 0, kErrAccWait)) have = false;
-        tc_fence_after();
-    }
-    __syncthreads();                   // this CTA's stage buffers are free
+    // One thread waits for the K loop (sleeping between tries); the others
+    // park on the block barrier and take no issue slots meanwhile.
+    int got = 1;
+    if (threadIdx.x == 0 && nkb > 0) got = mbar_wait_sleep(smem_u32(accf), 0, kErrAccWait) ? 1 : 0;
+    const bool have = nkb > 0 && __syncthreads_and(got);   // also: this CTA's stage buffers are free
+    tc_fence_after();
     cg::cluster_group cluster = cg::this_cluster();
     if (a.ks > 1) cluster.sync();      // ... and every peer's
     const uint32_t recv = smem_u32(red);
@@ -246,40 +248,80 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     if (a.ks > 1) cluster.sync();      // every push into this CTA has landed
     else __syncthreads();
 
+    // Thread (ln, sub) owns weight row n = n0 + r_lo + ln and tokens sub,
+    // sub + tpr, ...; four of them per step. Every rank's partial of the four
+    // is requested at once (the rank loop is unrolled and predicated), and the
+    // rows of B the next step needs are requested while this one is computed,
+    // so each step pays one shared-memory and no global round trip.
     const int r_lo = kz * rows_per;
-    const int n_el = rows_per * TN;
-    constexpr int E = 4;               // elements per thread whose B loads are in flight together
-    for (int e0 = threadIdx.x; e0 < n_el; e0 += E * kSkThreads) {
-        uint4 b0[E], b1[E];
+    const int lg = __ffs(rows_per) - 1;               // rows_per = 128 / ks is a power of two
+    const int ln = threadIdx.x & (rows_per - 1), sub = threadIdx.x >> lg;
+    const int tpr = kSkThreads >> lg;
+    const int n = n0 + r_lo + ln;
+    const int n_tok = min(TN, a.T - t0);
+    const int ks = a.ks;
+    __nv_bfloat16* __restrict__ yp = a.y;
+    if (n < a.N) {
+        uint4 bc[4][2], bn[4][2];
+        auto load_b = [&](int tl0, uint4 (&b)[4][2]) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int el = e0 + e * kSkThreads;
-            const int ln = el % rows_per, tl = el / rows_per;
-            const int n = n0 + r_lo + ln;
-            b0[e] = b1[e] = make_uint4(0, 0, 0, 0);
-            if (el < n_el && t0 + tl < a.T && n < a.N && tok_r8[tl] > 0) {
-                const __nv_bfloat16* brow = a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R;
-                b0[e] = __ldg(reinterpret_cast<const uint4*>(brow));
-                if (tok_r8[tl] > 8) b1[e] = __ldg(reinterpret_cast<const uint4*>(brow + 8));
+            for (int q = 0; q < 4; ++q) {
+                const int tl = tl0 + q * tpr;
+                b[q][0] = b[q][1] = make_uint4(0, 0, 0, 0);
+                if (tl < n_tok) {
+                    const int r8 = tok_r8[tl];
+                    if (r8 > 0) {
+                        const __nv_bfloat16* brow = a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R;
+                        b[q][0] = __ldg(reinterpret_cast<const uint4*>(brow));
+                        if (r8 > 8) b[q][1] = __ldg(reinterpret_cast<const uint4*>(brow + 8));
+                    }
+                }
             }
-        }
+        };
+        if (with_ex) load_b(sub, bc);
+        for (int tl0 = sub; tl0 < n_tok; tl0 += 4 * tpr) {
+            if (with_ex && tl0 + 4 * tpr < n_tok) load_b(tl0 + 4 * tpr, bn);
+            float acc[4];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int el = e0 + e * kSkThreads;
-            const int ln = el % rows_per, tl = el / rows_per;
-            const int t = t0 + tl, n = n0 + r_lo + ln;
-            if (el >= n_el || t >= a.T || n >= a.N) continue;
-            float acc = red[(size_t)tl * rows_per + ln];
-            for (int z = 1; z < a.ks; ++z) acc += red[((size_t)z * TN + tl) * rows_per + ln];
-            const int r8 = tok_r8[tl];
-            if (r8 > 0) {
-                const float* u = a.stage_u ? tok_u + (size_t)tl * R : a.ex.U + (size_t)t * R;
-                float d = dot8(u, b0[e], 0.f);
-                if (r8 > 8) d = dot8(u + 8, b1[e], d);
-                if (r8 > 16) d = expand_dot_from(u, a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R, 16, r8, d);
-                acc += d;
+            for (int q = 0; q < 4; ++q) {
+                const int tl = min(tl0 + q * tpr, n_tok - 1);
+                // unconditional loads (rank index clamped), so all of them are
+                // in flight together; ranks past ks are then left out of the sum
+                float pz[8];
+#pragma unroll
+                for (int z = 0; z < 8; ++z) pz[z] = red[(min(z, ks - 1) * TN + tl) * rows_per + ln];
+                float v = pz[0];
+#pragma unroll
+                for (int z = 1; z < 8; ++z) v = (z < ks) ? v + pz[z] : v;
+                acc[q] = v;
             }
-            a.y[(size_t)t * a.N + n] = __float2bfloat16_rn(acc);
+            if (with_ex) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int tl = tl0 + q * tpr;
+                    if (tl < n_tok) {
+                        const int r8 = tok_r8[tl];
+                        if (r8 > 0) {
+                            const float* u = a.stage_u ? tok_u + (size_t)tl * R : a.ex.U + (size_t)(t0 + tl) * R;
+                            float d = dot8(u, bc[q][0], 0.f);
+                            if (r8 > 8) d = dot8(u + 8, bc[q][1], d);
+                            if (r8 > 16)
+                                d = expand_dot_from(u, a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R, 16, r8, d);
+                            acc[q] += d;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    bc[q][0] = bn[q][0];
+                    bc[q][1] = bn[q][1];
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int tl = tl0 + q * tpr;
+                if (tl < n_tok) yp[(size_t)(t0 + tl) * a.N + n] = __float2bfloat16_rn(acc[q]);
+            }
         }
     }
 

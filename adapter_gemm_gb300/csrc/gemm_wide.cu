@@ -216,7 +216,10 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const uint32_t use = (uint32_t)(lt >> 1);
             const int m0 = (tile % a.m_tiles) * kWdBM;
             const int n0 = (tile / a.m_tiles) * kWdBN;
-            const bool ready = __all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull[as]), use & 1u, kErrAccWait));
+            // lane 0 of each epilogue warp waits (sleeping between tries)
+            bool got = true;
+            if (lane == 0) got = mbar_wait_sleep(smem_u32(&tfull[as]), use & 1u, kErrAccWait);
+            const bool ready = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
             if (!ready) break;     // the MMA side gave up; the error word is set
             tc_fence_after();
             const int i = m0 + row;

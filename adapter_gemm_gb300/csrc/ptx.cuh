@@ -79,6 +79,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int err
     }
 }
 
+// The same wait for threads whose wait is long and not latency-critical (an
+// epilogue waiting for a whole K loop): after a few failed tries the thread
+// sleeps between tries, so it does not take issue slots from the warps that
+// feed the tensor cores or finish another tile.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, int err) {
+    long long t0 = 0;
+    uint32_t ns = 32;
+    for (uint32_t i = 0;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i >= 8) {
+            __nanosleep(ns);
+            if (ns < 512) ns <<= 1;
+        }
+        if ((i & 63u) == 63u) {
+            const long long now = clock64();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > kWaitLimitCycles) {
+                atomicCAS(&g_lora_error, 0, err);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- TMA -------
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
