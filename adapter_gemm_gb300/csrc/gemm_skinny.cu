@@ -9,10 +9,12 @@
 // MMA is "swap-AB": M = 128 rows of W, N = the token tile (16..256 columns).
 //
 // d_out / 128 weight tiles are too few to fill 152 SMs, so K is split over the
-// CTAs of a thread-block cluster (ks = 1..8). After the K loop each CTA parks
-// its partial tile in shared memory; CTA rank c then owns 128/ks weight rows,
-// sums the ks partials in rank order through distributed shared memory (a
-// fixed order, so results do not depend on timing), adds the row's low-rank
+// CTAs of a thread-block cluster (ks = 1..8). CTA rank c owns 128/ks weight
+// rows of the tile. After the K loop every CTA reads its partial tile out of
+// TMEM and pushes each owner's rows into that owner's shared memory
+// (distributed shared memory stores, one slot per sender); the owner then sums
+// the ks partials in rank order (a fixed order, so results do not depend on
+// timing), adds the row's low-rank
 // correction (the expand half of SGMV: U[t, :r] . B[s, n, :r], fp32, j
 // ascending) unless the token is on slot 0 or a rank-0 slot, rounds to bf16
 // and writes y once. No fp32 atomics, no extra pass over y.
