@@ -25,6 +25,11 @@ cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes) {
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev][slot] >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    // The whole unified L1 as shared memory: the occupancy queries (and the
+    // launches) then count every CTA that fits by shared memory.
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(func, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) done[dev][slot] = bytes;
     return e;
 }
@@ -430,6 +435,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     if (!aligned16(x) || !aligned16(W) || !aligned16(y)) return LORA_EINVAL;
     if (plan) {
         if (!pool || !pool->A || !pool->B || !pool->rank || !pool->scale) return LORA_EINVAL;
+        if (!aligned16(pool->A) || !aligned16(pool->B)) return LORA_EINVAL;
         if (plan->T != T || plan->S != pool->S || plan->R_max != pool->R_max || pool->d_in != d_in ||
             pool->d_out != d_out || d_in > plan->d_in_cap)
             return LORA_ESHAPE;
@@ -480,11 +486,12 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     }
 
     ExpandArgs ex;
-    ex.slot_of_token = plan ? plan->slot_of_token : nullptr;
+    ex.ids = plan ? plan->ids : nullptr;
     ex.U = plan ? plan->U : nullptr;
     ex.B = plan ? static_cast<const __nv_bfloat16*>(pool->B) : nullptr;
     ex.rank = plan ? pool->rank : nullptr;
     ex.R_max = plan ? pool->R_max : 0;
+    ex.S = plan ? pool->S : 0;
 
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_start, st) != cudaSuccess) return LORA_ECUDA;
     if (path == 0) {
@@ -506,6 +513,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.stage_u = (plan && c.can_stage_u && pool->R_max <= kStageURank) ? 1 : 0;
         a.smem = c.smem;
         a.x_early = x_early ? 1 : 0;
+        a.ids_early = (!plan || !overlaps(prev, plan->ids, (size_t)T * 4)) ? 1 : 0;
         if (launch_skinny(tmW, tmX, a, pdl, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;

@@ -20,8 +20,9 @@
 // and writes y once. No fp32 atomics, no extra pass over y.
 //
 // Roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warp 1 owns the
-// TMEM allocation; all four warps drain the accumulator (warp w reads TMEM
-// lanes 32w..32w+31) and do the reduction.
+// TMEM allocation; warps 2..7 group the tile's tokens by slot during the K
+// loop; all eight warps drain the accumulator (warp w reads TMEM lanes
+// 32 (w % 4).. and half of the token columns) and do the reduction and expand.
 #include <cstdint>
 #include <cooperative_groups.h>
 #include "ptx.cuh"
@@ -31,24 +32,30 @@ namespace cg = cooperative_groups;
 
 namespace lora {
 
-constexpr int kSkThreads = 128;
+constexpr int kSkThreads = 256;             // 8 warps: TMA, MMA, then six that only work outside the K loop
 constexpr int kBK = 64;                     // K elements per stage (128 bytes of bf16)
 constexpr int kWRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kWTileBytes = kWRows * kBK * 2;
 
-// Epilogue scratch after the K loop: the received partials [ks][TN][128/ks]
-// (128 x TN floats), per-token slot and rank [2][TN], and (when staged) U rows
+// Epilogue scratch after the K loop, in the pipeline's buffers: the received
+// partials [ks][TN][128/ks] (128 x TN floats) and (when staged) U rows
 // [TN][R_max].
 size_t skinny_epi_bytes(int TN, int R_max, bool stage_u) {
-    return (size_t)kWRows * TN * 4 + (size_t)2 * TN * 4 + (stage_u ? (size_t)TN * R_max * 4 : 0);
+    return (size_t)kWRows * TN * 4 + (stage_u ? (size_t)TN * R_max * 4 : 0);
 }
+
+// The tile's tokens grouped by slot (kept apart from the pipeline's buffers,
+// since it is built during the K loop): per token its slot and rank rounded up
+// to 8, the tokens in slot order, and per group its slot, rank and first
+// position, plus the group count.
+size_t skinny_grp_bytes(int TN) { return ((size_t)6 * TN + 4) * 4; }
 
 size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u) {
     const size_t stage = (size_t)kWTileBytes + (size_t)TN * kBK * 2;
     const size_t pipe = stage * stages;
     const size_t epi = skinny_epi_bytes(TN, R_max, stage_u);
     const size_t body = pipe > epi ? pipe : epi;
-    return 1024 /*alignment slack*/ + body + 256 /*barriers*/;
+    return 1024 /*alignment slack*/ + body + 256 /*barriers*/ + skinny_grp_bytes(TN);
 }
 
 // d + u[0..7] . b[0..7] (b = 8 packed bf16), j ascending.
@@ -73,6 +80,96 @@ __device__ __forceinline__ float expand_dot_from(const float* __restrict__ u, co
     return d;
 }
 
+struct TileGroups {
+    int* tslot;   // [TN] slot of each token (0: no correction)
+    int* tr8;     // [TN] its rank rounded up to 8 (0 with slot 0)
+    int* order;   // [TN] tokens, stably sorted by slot
+    int* gslot;   // [TN] slot of each group (a group is at most P tokens of one slot)
+    int* gr8;     // [TN] rank of each group, rounded up to 8
+    int* gbeg;    // [TN + 1] first position of each group in `order`, then n_tok
+    int* n_groups;
+};
+
+__device__ __forceinline__ void grp_barrier(int nthr) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+}
+
+// Group the tile's tokens by adapter slot, with the `nthr` threads (whole
+// warps) numbered i0 = 0.. that run it, and send this CTA's rows of B for
+// every group to L2. Invalid ids, slot 0 and rank-0 slots all map to slot 0:
+// those tokens get the base output only. Reads the ids, the pool's ranks and B.
+__device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, int n_tok, int i0, int nthr,
+                             int n_lo, int n_rows, int n_rows_per) {
+    const bool with_ex = a.ex.ids != nullptr;
+    const int lane = threadIdx.x & 31;
+    for (int t = i0; t < n_tok; t += nthr) {
+        int s = 0, r8 = 0;
+        if (with_ex) {
+            const int id = a.ex.ids[t0 + t];
+            if (id >= 1 && id < a.ex.S) {
+                const int r = min(a.ex.rank[id], a.ex.R_max);
+                if (r > 0) {
+                    s = id;
+                    r8 = (r + 7) & ~7;
+                }
+            }
+        }
+        gp.tslot[t] = s;
+        gp.tr8[t] = r8;
+    }
+    grp_barrier(nthr);
+    // stable sort: a token's position is the number of tokens with a smaller
+    // (slot, index)
+    for (int t = i0; t < n_tok; t += nthr) {
+        const int s = gp.tslot[t];
+        int pos = 0;
+        for (int u = 0; u < n_tok; ++u) {
+            const int su = gp.tslot[u];
+            pos += (su < s || (su == s && u < t)) ? 1 : 0;
+        }
+        gp.order[pos] = t;
+    }
+    grp_barrier(nthr);
+    if (i0 < 32) {
+        // Group boundaries, by the first warp. A group longer than P tokens is
+        // cut into pieces of P, so that the epilogue has about two (row, piece)
+        // items per thread even when one slot holds every token.
+        const int P = max(1, (n_tok * n_rows_per + 2 * kSkThreads - 1) / (2 * kSkThreads));
+        int G = 0, cur = 0;            // pieces so far; start of the group open at `base`
+        for (int base = 0; base < n_tok; base += 32) {
+            const int p = base + lane;
+            const bool valid = p < n_tok;
+            const int s = valid ? gp.tslot[gp.order[p]] : -1;
+            const bool first = valid && (p == 0 || gp.tslot[gp.order[p - 1]] != s);
+            const unsigned m = __ballot_sync(0xffffffffu, first);
+            const unsigned upto = m & (0xffffffffu >> (31 - lane));
+            const int gstart = upto ? base + 31 - __clz(upto) : cur;
+            const bool cut = valid && (first || ((p - gstart) % P) == 0);
+            const unsigned mc = __ballot_sync(0xffffffffu, cut);
+            if (cut) {
+                const int g = G + __popc(mc & ((1u << lane) - 1u));
+                gp.gbeg[g] = p;
+                gp.gslot[g] = s;
+                gp.gr8[g] = gp.tr8[gp.order[p]];
+            }
+            G += __popc(mc);
+            cur = __shfl_sync(0xffffffffu, gstart, 31);
+        }
+        if (lane == 0) {
+            gp.gbeg[G] = n_tok;
+            *gp.n_groups = G;
+        }
+    }
+    grp_barrier(nthr);
+    if (with_ex && n_rows > 0) {       // rows [n_lo, n_lo + n_rows) of B_s are contiguous
+        const int G = *gp.n_groups;
+        for (int g = i0; g < G; g += nthr)
+            if (gp.gr8[g] > 0)
+                prefetch_l2_bulk(a.ex.B + ((size_t)gp.gslot[g] * a.N + n_lo) * a.ex.R_max,
+                                 (uint32_t)n_rows * (uint32_t)a.ex.R_max * 2u);
+    }
+}
+
 __global__ void __launch_bounds__(kSkThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    SkinnyArgs a) {
@@ -85,14 +182,17 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const uint32_t x_tile_bytes = (uint32_t)TN * kBK * 2;
     const uint32_t stage_bytes = kWTileBytes + x_tile_bytes;
     const size_t pipe = (size_t)stage_bytes * stages;
-    const size_t epi_bytes = (size_t)kWRows * TN * 4 + (size_t)2 * TN * 4 +
-                             (a.stage_u ? (size_t)TN * a.ex.R_max * 4 : 0);
+    const size_t epi_bytes = (size_t)kWRows * TN * 4 + (a.stage_u ? (size_t)TN * a.ex.R_max * 4 : 0);
     uint8_t* tail = base + (pipe > epi_bytes ? pipe : epi_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(tail);          // [stages]
     uint64_t* empty = full + stages;                              // [stages]
     uint64_t* accf = empty + stages;                              // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
     float* red = reinterpret_cast<float*>(base);                  // received partials, after the K loop
+    float* sU = red + (size_t)kWRows * TN;                        // staged U rows, after the K loop
+    int* gmem = reinterpret_cast<int*>(tail + 256);
+    const TileGroups gp{gmem, gmem + TN, gmem + 2 * TN, gmem + 3 * TN, gmem + 4 * TN, gmem + 5 * TN,
+                        gmem + 6 * TN + 1};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x;
@@ -103,6 +203,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int kb_lo = kz * per;
     const int kb_hi = min(a.kb_total, kb_lo + per);
     const int nkb = max(0, kb_hi - kb_lo);
+    const int rows_per = kWRows / a.ks;                           // weight rows this CTA finishes
+    const int n_lo = n0 + kz * rows_per;
+    const int n_rows = max(0, min(rows_per, a.N - n_lo));
+    const int n_tok = min(TN, a.T - t0);
     const uint32_t tmem_cols = TN <= 32 ? 32u : (TN <= 64 ? 64u : (TN <= 128 ? 128u : 256u));
 
     if (warp == 0 && lane == 0) {
@@ -130,8 +234,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     bool ok = true;
     if (warp == 0 && lane == 0) {
         // TMA producer. Weights are never written by the kernels this one waits
-        // for, so the first `stages` weight tiles go to shared memory and the rest
-        // of this CTA's weight range to L2 before the wait. x is loaded before
+        // for, so the first `stages` weight tiles go to shared memory and the next
+        // `stages` to L2 before the wait. x is loaded before
         // the wait too unless the host saw that the previous kernel writes it.
         const int pre = min(nkb, stages);
         for (int i = 0; i < pre; ++i) {
@@ -141,7 +245,9 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             tma_load_2d(sW, &tmW, fb, (kb_lo + i) * kBK, n0);
             if (a.x_early) tma_load_2d(sW + kWTileBytes, &tmX, fb, (kb_lo + i) * kBK, t0);
         }
-        for (int i = pre; i < nkb; ++i) tma_prefetch_l2_2d(&tmW, (kb_lo + i) * kBK, n0);
+        // One more ring's worth to L2: enough bytes in flight to cover the wait,
+        // without queueing this CTA's whole range ahead of other kernels' loads.
+        for (int i = pre; i < min(nkb, 2 * stages); ++i) tma_prefetch_l2_2d(&tmW, (kb_lo + i) * kBK, n0);
         if (!a.x_early) pdl_wait();
         int issued = 0;
         for (int i = 0; i < nkb && ok; ++i) {
@@ -180,17 +286,17 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             tc_commit(smem_u32(&empty[st]));
         }
         tc_commit(smem_u32(accf));     // fires once every MMA above has completed
+    } else if (warp >= 2 && a.ids_early) {
+        // Idle during the K loop: group the tokens and fetch B's rows to L2.
+        group_tokens(a, gp, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64, n_lo, n_rows, rows_per);
     }
     __syncwarp();
-    pdl_wait();                        // slot ids and U come from the kernels before this one
-
     // Split-K reduction. CTA rank c owns weight rows [c*rows_per, (c+1)*rows_per)
     // of the tile. Once every CTA of the cluster is past its K loop, each one
     // pushes its partial rows straight from TMEM into the owner's shared memory
     // (recv[src rank][token][row], plain stores into the peer), then each owner
     // sums what it received in rank order: a fixed order, and no remote loads.
-    const int row = warp * 32 + lane;
-    const int rows_per = kWRows / a.ks;
+    const int row = (warp & 3) * 32 + lane;         // the accumulator row (weight row) this thread moves
     // One thread waits for the K loop (sleeping between tries); the others
     // park on the block barrier and take no issue slots meanwhile.
     int got = 1;
@@ -201,12 +307,14 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     if (a.ks > 1) cluster.sync();      // ... and every peer's
     const uint32_t recv = smem_u32(red);
     {
+        // warp w reads TMEM lanes 32 (w % 4) .. (the lanes its quadrant may
+        // access) and every other 16-column chunk, starting at 16 (w / 4)
         const int owner = row / rows_per, ln = row % rows_per;
         const uint32_t dst0 = (a.ks > 1) ? mapa_shared(recv, (uint32_t)owner) : recv;
-        for (int c = 0; c < TN; c += 16) {
+        for (int c = 16 * (warp >> 2); c < TN; c += 32) {
             float v[16];
             if (have) {
-                tc_ld16(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
+                tc_ld16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)c, v);
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = 0.f;
@@ -218,113 +326,108 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     }
     tc_fence_before();
 
-    // Per-token slot, rank (rounded up to 8) and U row, staged once for the tile.
-    int* tok_s = reinterpret_cast<int*>(red + (size_t)kWRows * TN);
-    int* tok_r8 = tok_s + TN;
-    float* tok_u = reinterpret_cast<float*>(tok_r8 + TN);
-    const bool with_ex = a.ex.slot_of_token != nullptr;
+    // U comes from the kernels before this one, and so do the ids when the
+    // host could not rule that out: only from here on does the epilogue depend
+    // on them.
+    pdl_wait();
+    const bool with_ex = a.ex.ids != nullptr;
+    if (!a.ids_early) group_tokens(a, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
     const int R = a.ex.R_max;
-    pdl_wait();                        // slot ids and U come from the kernels before this one
-    for (int tl = threadIdx.x; tl < TN; tl += kSkThreads) {
-        const int t = t0 + tl;
-        int s = 0, r8 = 0;
-        if (with_ex && t < a.T) {
-            s = a.ex.slot_of_token[t];
-            if (s > 0) {
-                const int r = min(a.ex.rank[s], R);
-                r8 = r > 0 ? (r + 7) & ~7 : 0;
-            }
-        }
-        tok_s[tl] = s;
-        tok_r8[tl] = r8;
-    }
-    __syncthreads();
     if (with_ex && a.stage_u) {
-        for (int q = threadIdx.x; q < TN * (R / 4); q += kSkThreads) {
-            const int tl = q / (R / 4), j4 = q % (R / 4);
-            if (tok_r8[tl] > j4 * 4)
-                reinterpret_cast<float4*>(tok_u)[q] =
+        const int R4 = R >> 2;
+        for (int q = threadIdx.x; q < n_tok * R4; q += kSkThreads) {
+            const int tl = q / R4, j4 = q - tl * R4;
+            if (gp.tr8[tl] > j4 * 4)
+                reinterpret_cast<float4*>(sU)[q] =
                     __ldg(reinterpret_cast<const float4*>(a.ex.U + (size_t)(t0 + tl) * R) + j4);
         }
     }
     if (a.ks > 1) cluster.sync();      // every push into this CTA has landed
     else __syncthreads();
 
-    // Thread (ln, sub) owns weight row n = n0 + r_lo + ln and tokens sub,
-    // sub + tpr, ...; four of them per step. Every rank's partial of the four
-    // is requested at once (the rank loop is unrolled and predicated), and the
-    // rows of B the next step needs are requested while this one is computed,
-    // so each step pays one shared-memory and no global round trip.
-    const int r_lo = kz * rows_per;
+    // Work items are (weight row, slot group) pairs: an item loads its row of
+    // B_s once (the next item's is requested while this one is computed) and
+    // finishes every token of the group:
+    //   y[t, n] = bf16( sum_z partial_z[t, n] + sum_j U[t, j] B[s, n, j] ),
+    // z in rank order, j ascending; slot-0 groups only sum the partials.
     const int lg = __ffs(rows_per) - 1;               // rows_per = 128 / ks is a power of two
-    const int ln = threadIdx.x & (rows_per - 1), sub = threadIdx.x >> lg;
-    const int tpr = kSkThreads >> lg;
-    const int n = n0 + r_lo + ln;
-    const int n_tok = min(TN, a.T - t0);
+    const int n_items = *gp.n_groups << lg;
     const int ks = a.ks;
     __nv_bfloat16* __restrict__ yp = a.y;
-    if (n < a.N) {
-        uint4 bc[4][2], bn[4][2];
-        auto load_b = [&](int tl0, uint4 (&b)[4][2]) {
+    const __nv_bfloat16* __restrict__ Bp = a.ex.B;
+    auto load_b = [&](int item, uint4 (&b)[8]) {
+        const int g = item >> lg, ln = item & (rows_per - 1);
+        const int r8 = gp.gr8[g];
+        const uint4* brow = reinterpret_cast<const uint4*>(Bp + ((size_t)gp.gslot[g] * a.N + (n_lo + ln)) * R);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tl = tl0 + q * tpr;
-                b[q][0] = b[q][1] = make_uint4(0, 0, 0, 0);
-                if (tl < n_tok) {
-                    const int r8 = tok_r8[tl];
-                    if (r8 > 0) {
-                        const __nv_bfloat16* brow = a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R;
-                        b[q][0] = __ldg(reinterpret_cast<const uint4*>(brow));
-                        if (r8 > 8) b[q][1] = __ldg(reinterpret_cast<const uint4*>(brow + 8));
-                    }
-                }
-            }
-        };
-        if (with_ex) load_b(sub, bc);
-        for (int tl0 = sub; tl0 < n_tok; tl0 += 4 * tpr) {
-            if (with_ex && tl0 + 4 * tpr < n_tok) load_b(tl0 + 4 * tpr, bn);
-            float acc[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tl = min(tl0 + q * tpr, n_tok - 1);
+        for (int c = 0; c < 8; ++c)
+            b[c] = (c * 8 < r8 && ln < n_rows) ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
+    };
+    uint4 bc[8], bn[8];
+    if ((int)threadIdx.x < n_items) load_b(threadIdx.x, bc);
+    for (int item = threadIdx.x; item < n_items; item += kSkThreads) {
+        if (item + kSkThreads < n_items) load_b(item + kSkThreads, bn);
+        const int g = item >> lg, ln = item & (rows_per - 1);
+        if (ln < n_rows) {
+            const int n = n_lo + ln;
+            const int r8 = gp.gr8[g];
+            const int pe = gp.gbeg[g + 1];
+            // two tokens at a time: independent chains, each B element
+            // unpacked once for both
+            for (int p = gp.gbeg[g]; p < pe; p += 2) {
+                const bool two = p + 1 < pe;
+                const int ta = gp.order[p], tb = two ? gp.order[p + 1] : ta;
                 // unconditional loads (rank index clamped), so all of them are
                 // in flight together; ranks past ks are then left out of the sum
-                float pz[8];
+                float pa[8], pb[8];
 #pragma unroll
-                for (int z = 0; z < 8; ++z) pz[z] = red[(min(z, ks - 1) * TN + tl) * rows_per + ln];
-                float v = pz[0];
+                for (int z = 0; z < 8; ++z) {
+                    pa[z] = red[(min(z, ks - 1) * TN + ta) * rows_per + ln];
+                    pb[z] = red[(min(z, ks - 1) * TN + tb) * rows_per + ln];
+                }
+                float va = pa[0], vb = pb[0];
 #pragma unroll
-                for (int z = 1; z < 8; ++z) v = (z < ks) ? v + pz[z] : v;
-                acc[q] = v;
-            }
-            if (with_ex) {
+                for (int z = 1; z < 8; ++z) {
+                    va = (z < ks) ? va + pa[z] : va;
+                    vb = (z < ks) ? vb + pb[z] : vb;
+                }
+                if (r8 > 0) {
+                    const float* ua = a.stage_u ? sU + (size_t)ta * R : a.ex.U + (size_t)(t0 + ta) * R;
+                    const float* ub = a.stage_u ? sU + (size_t)tb * R : a.ex.U + (size_t)(t0 + tb) * R;
+                    float da = 0.f, db = 0.f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int tl = tl0 + q * tpr;
-                    if (tl < n_tok) {
-                        const int r8 = tok_r8[tl];
-                        if (r8 > 0) {
-                            const float* u = a.stage_u ? tok_u + (size_t)tl * R : a.ex.U + (size_t)(t0 + tl) * R;
-                            float d = dot8(u, bc[q][0], 0.f);
-                            if (r8 > 8) d = dot8(u + 8, bc[q][1], d);
-                            if (r8 > 16)
-                                d = expand_dot_from(u, a.ex.B + ((size_t)tok_s[tl] * a.N + n) * R, 16, r8, d);
-                            acc[q] += d;
+                    for (int c = 0; c < 8; ++c) {
+                        if (c * 8 < r8) {
+                            const float4 a0 = *reinterpret_cast<const float4*>(ua + c * 8);
+                            const float4 a1 = *reinterpret_cast<const float4*>(ua + c * 8 + 4);
+                            const float4 b0 = *reinterpret_cast<const float4*>(ub + c * 8);
+                            const float4 b1 = *reinterpret_cast<const float4*>(ub + c * 8 + 4);
+                            const uint4 w = bc[c];
+                            float e;
+                            e = bf16lo(w.x); da = fmaf(a0.x, e, da); db = fmaf(b0.x, e, db);
+                            e = bf16hi(w.x); da = fmaf(a0.y, e, da); db = fmaf(b0.y, e, db);
+                            e = bf16lo(w.y); da = fmaf(a0.z, e, da); db = fmaf(b0.z, e, db);
+                            e = bf16hi(w.y); da = fmaf(a0.w, e, da); db = fmaf(b0.w, e, db);
+                            e = bf16lo(w.z); da = fmaf(a1.x, e, da); db = fmaf(b1.x, e, db);
+                            e = bf16hi(w.z); da = fmaf(a1.y, e, da); db = fmaf(b1.y, e, db);
+                            e = bf16lo(w.w); da = fmaf(a1.z, e, da); db = fmaf(b1.z, e, db);
+                            e = bf16hi(w.w); da = fmaf(a1.w, e, da); db = fmaf(b1.w, e, db);
                         }
                     }
+                    if (r8 > 64) {
+                        const __nv_bfloat16* brow = Bp + ((size_t)gp.gslot[g] * a.N + n) * R;
+                        da = expand_dot_from(ua, brow, 64, r8, da);
+                        db = expand_dot_from(ub, brow, 64, r8, db);
+                    }
+                    va += da;
+                    vb += db;
                 }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    bc[q][0] = bn[q][0];
-                    bc[q][1] = bn[q][1];
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int tl = tl0 + q * tpr;
-                if (tl < n_tok) yp[(size_t)(t0 + tl) * a.N + n] = __float2bfloat16_rn(acc[q]);
+                yp[(size_t)(t0 + ta) * a.N + n] = __float2bfloat16_rn(va);
+                if (two) yp[(size_t)(t0 + tb) * a.N + n] = __float2bfloat16_rn(vb);
             }
         }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) bc[c] = bn[c];
     }
 
     if (warp == 1) {

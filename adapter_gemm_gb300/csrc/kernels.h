@@ -27,6 +27,7 @@ struct PlanArgs {
     int32_t* mt_ptr;        // [ceil(T/128)+1] or null: per 128-row block, first entry of mt_seg
     int32_t* mt_seg;        // [ceil(T/128)+S][4]: (slot, first row, end row, block), rows block-local
     int S;
+    int stage;              // build the row arrays in shared memory, store them after the wait
 };
 
 struct ShrinkArgs {
@@ -46,14 +47,15 @@ struct ShrinkArgs {
     int x_early;                 // x is not written by the kernel this one follows
 };
 
-// Epilogue operands shared by both GEMM kernels. slot_of_token == null means
-// base only (no correction anywhere).
+// Expand operands of the decode GEMM's epilogue. ids == null means base only
+// (no correction anywhere).
 struct ExpandArgs {
-    const int32_t* slot_of_token;  // [T]
-    const float* U;                // [T, R_max]
+    const int32_t* ids;            // [T] the step's raw slot ids (invalid ones mean slot 0)
+    const float* U;                // [T, R_max] by token
     const __nv_bfloat16* B;        // [S, N, R_max]
     const int32_t* rank;           // [S]
     int R_max;
+    int S;
 };
 
 struct SkinnyArgs {
@@ -66,6 +68,7 @@ struct SkinnyArgs {
     int stages;
     int stage_u;       // copy the tile's U rows into shared memory for the epilogue
     int x_early;       // x may be loaded before the wait for the previous kernel
+    int ids_early;     // the ids may be read before that wait
     size_t smem;       // dynamic shared memory of the launch
 };
 

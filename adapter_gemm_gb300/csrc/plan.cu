@@ -19,6 +19,11 @@
 //           rank among equal-slot lanes to its left.
 // Then the active-slot list and the work tiles (each slot's segment cut every
 // LORA_TILE_ROWS rows) come from two more prefix sums over slots.
+//
+// The kernel is launched as a dependent of the previous kernel of the stream,
+// whose kernels may still read the plan arrays. It reads only the ids before
+// it waits for them, and, when the batch's row arrays fit in shared memory,
+// builds the whole plan before the wait, so that after it only stores remain.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include "ptx.cuh"
@@ -64,6 +69,8 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     const int S = p.S;
     int* wc = smem;                       // [kPlanWarps][S] per-warp slot counts, then cursors
     int* tot = smem + kPlanWarps * S;     // [S] per-slot totals
+    int* st_order = tot + S;              // [T] token_order, staged (p.stage)
+    int* st_slot = st_order + T;          // [T] slot_of_token, staged (p.stage)
     __shared__ int warp_tot[33];
     __shared__ int s_invalid;
 
@@ -94,9 +101,11 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) n_bad += __shfl_xor_sync(0xffffffffu, n_bad, d);
     if (lane == 0 && n_bad) atomicAdd(&s_invalid, n_bad);
-    // Everything so far read only the ids; the plan arrays may still be read by
-    // the kernels ahead of this one, so wait for them before writing any.
-    pdl_wait();
+    // The plan arrays may still be read by the kernels ahead of this one, so no
+    // global write comes before the wait. With staging, the whole plan is built
+    // in shared memory and registers first and only stored after the wait;
+    // without it (batches too large to stage) the wait comes here.
+    if (!p.stage) pdl_wait();
     __syncthreads();
 
     // Per slot: exclusive prefix over warps (in place) and the slot total.
@@ -115,42 +124,53 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     int total = 0;
     const int my_cnt = tid < S ? tot[tid] : 0;
     const int start = block_exclusive_scan(my_cnt, warp_tot, total);
-    if (tid < S) {
-        p.counts[tid] = my_cnt;
-        p.indptr[tid] = start;
+    if (tid < S)
         for (int w = 0; w < kPlanWarps; ++w) wc[w * S + tid] += start;
-    }
-    if (tid == 0) p.indptr[S] = total;
     __syncthreads();
 
     // Pass 2: stable scatter of row ids.
+    int32_t* order_out = p.stage ? st_order : p.token_order;
+    int32_t* slot_out = p.stage ? st_slot : p.slot_of_token;
     for (int base = lo; base < hi; base += 32) {
         const int t = base + lane;
         const bool valid = t < hi;
         int s = valid ? ids[t] : 0;
         if (valid && (s < 0 || s >= S)) s = 0;
-        if (valid) p.slot_of_token[t] = s;
+        if (valid) slot_out[t] = s;
         const int key = valid ? s : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
         if (valid) {
             const unsigned below = peers & ((1u << lane) - 1u);
-            p.token_order[wc[warp * S + s] + __popc(below)] = t;
+            order_out[wc[warp * S + s] + __popc(below)] = t;
         }
         __syncwarp();
         if (valid && lane == __ffs(peers) - 1) wc[warp * S + s] += __popc(peers);
         __syncwarp();
     }
 
-    // Active adapter slots (s >= 1 with rows), ascending.
+    // Active adapter slots (s >= 1 with rows), ascending, and the work tiles
+    // over every segment, slot 0 included: positions from two prefix sums.
     const int is_active = (tid >= 1 && tid < S && my_cnt > 0) ? 1 : 0;
     int n_active = 0;
     const int a_pos = block_exclusive_scan(is_active, warp_tot, n_active);
-    if (is_active) p.active[a_pos] = tid;
-
-    // Work tiles over every segment, slot 0 included.
     const int n_t = tid < S ? (my_cnt + kTileRows - 1) / kTileRows : 0;
     int n_tiles = 0;
     const int t_pos = block_exclusive_scan(n_t, warp_tot, n_tiles);
+
+    if (p.stage) {
+        pdl_wait();
+        __syncthreads();
+        for (int i = tid; i < T; i += kPlanThreads) {
+            p.token_order[i] = st_order[i];
+            p.slot_of_token[i] = st_slot[i];
+        }
+    }
+    if (tid < S) {
+        p.counts[tid] = my_cnt;
+        p.indptr[tid] = start;
+    }
+    if (tid == 0) p.indptr[S] = total;
+    if (is_active) p.active[a_pos] = tid;
     for (int j = 0; j < n_t; ++j) {
         const int b = start + j * kTileRows;
         int4 tile = make_int4(tid, b, min(b + kTileRows, start + my_cnt), 0);
@@ -190,8 +210,21 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     }
 }
 
-cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream) {
-    const size_t smem = sizeof(int) * (size_t)(kPlanWarps + 1) * p.S;
+// Shared memory of the plan kernel; `stage` says whether the row arrays are
+// staged there too (batches whose arrays fit).
+size_t plan_smem_bytes(int T, int S, bool* stage) {
+    const size_t counts = sizeof(int) * (size_t)(kPlanWarps + 1) * S;
+    const size_t rows = sizeof(int) * (size_t)2 * T;
+    const bool st = counts + rows <= (size_t)160 * 1024;
+    if (stage) *stage = st;
+    return counts + (st ? rows : 0);
+}
+
+cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p_in, bool pdl, cudaStream_t stream) {
+    PlanArgs p = p_in;
+    bool stage = false;
+    const size_t smem = plan_smem_bytes(T, p.S, &stage);
+    p.stage = stage ? 1 : 0;
     cudaError_t e = ensure_smem_attr((const void*)plan_kernel, 0, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

@@ -135,6 +135,12 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t c0,
                  :: "l"(tmap), "r"(c0), "r"(c1) : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16) of global memory from a 16-byte aligned
+// address into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
 // ---------------------------------------------------------------- cluster ---
 // Address of the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {

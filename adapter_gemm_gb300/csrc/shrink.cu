@@ -114,12 +114,14 @@ __device__ __forceinline__ void store_u(float* U, __nv_bfloat16* U_hl, const int
 // (i < n). Rank c of the cluster owns rows [c*16/ks, (c+1)*16/ks): every CTA
 // pushes its partial of those rows into the owner's `recv` (plain stores into
 // the peer's shared memory), then the owner sums what it received in rank
-// order. The caller must have waited for earlier readers of U.
+// order. Earlier readers of U must be done before the stores: the caller has
+// waited for them, or passes wait_first and the wait comes right before the
+// stores, after the reduction.
 template <int NT>
 __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], float (*part)[16][NT * 8 + 1],
                                                     float* recv, const int* tok, int n, int rc8, float sc,
                                                     float* U, int R_max, int ks, __nv_bfloat16* U_hl = nullptr,
-                                                    int R16 = 0, int pos0 = 0) {
+                                                    int R16 = 0, int pos0 = 0, bool wait_first = false) {
     constexpr int RC = NT * 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -146,6 +148,7 @@ __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], f
             st_cluster_f32(mapa_shared(rbase, (uint32_t)owner) + (uint32_t)(((me * rows_per + lr) * RC + col) * 4), v);
         }
         cluster.sync();                               // every push has landed
+        if (wait_first) pdl_wait();
         const int wc = U_hl ? R16 : rc8;
         for (int el = threadIdx.x; el < rows_per * wc; el += kShrinkThreads) {
             const int lr = el / wc, col = el % wc;
@@ -158,6 +161,7 @@ __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], f
             if (row < n) store_u(U, U_hl, tok, row, col, col < rc8 ? sc * v : 0.f, R_max, R16, pos0);
         }
     } else {
+        if (wait_first) pdl_wait();
         const int wc = U_hl ? R16 : rc8;
         for (int el = threadIdx.x; el < 16 * wc; el += kShrinkThreads) {
             const int row = el / wc, col = el % wc;
@@ -274,19 +278,16 @@ shrink_by_slot_kernel(ShrinkArgs a) {
     const int nt_used = (r + 7) >> 3;
     const float sc = a.scale[s];
     const __nv_bfloat16* Ablk = a.A + (size_t)s * a.R_max * K;
-    bool waited = !a.x_early;
     for (int g0 = 0; g0 < n_rows; g0 += 16) {
         const bool v0 = g0 + g < n_rows, v1 = g0 + g + 8 < n_rows;
         const int t0 = v0 ? rows[g0 + g] : 0, t1 = v1 ? rows[g0 + g + 8] : 0;
         float acc[NT][4];
         shrink_accumulate<NT>(acc, a.x + (size_t)t0 * K, a.x + (size_t)t1 * K, v0, v1, nullptr, nullptr,
                               Ablk, K, nt_used, k_lo, k_hi, true);
-        if (!waited) {                 // earlier readers of U must be done before it is written
-            pdl_wait();
-            waited = true;
-        }
+        // earlier readers of U must be done before it is written: the wait
+        // comes after the cluster's reduction, right before the stores
         shrink_reduce_store<NT>(acc, part, recv, rows + g0, min(16, n_rows - g0), nt_used * 8, sc, a.U,
-                                a.R_max, a.ks);
+                                a.R_max, a.ks, nullptr, 0, 0, true);
     }
 }
 
