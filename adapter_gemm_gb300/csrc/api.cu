@@ -88,14 +88,14 @@ bool make_tmap(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// bf16 tensor of rank 2 or 3 (dims innermost first, row pitches in bytes),
-// tiled in boxes `box`, with the given swizzle, zero fill outside the tensor.
+// bf16 tensor of rank 2 to 4 (dims innermost first, pitches in bytes), tiled
+// in boxes `box`, with the given swizzle, zero fill outside the tensor.
 bool make_tmap_nd(CUtensorMap* m, const void* ptr, int rank, const uint64_t* dims, const uint64_t* pitches,
                   const uint32_t* box, CUtensorMapSwizzle swz) {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t d[3], st[2];
-    cuuint32_t b[3], es[3] = {1, 1, 1};
+    if (!fn || rank < 2 || rank > 4) return false;
+    cuuint64_t d[4], st[3];
+    cuuint32_t b[4], es[4] = {1, 1, 1, 1};
     for (int i = 0; i < rank; ++i) {
         d[i] = dims[i];
         b[i] = box[i];
@@ -143,7 +143,7 @@ void plan_layout(int T, int S, int R_max, int d_in_cap, size_t sizes[kPlanParts]
     sizes[13] = wide ? (size_t)(m_blocks + S) * 16 : 0;                   // mt_seg
 }
 
-struct SkinnyConfig { int TN, stages, ks, can_stage_u; size_t smem; };
+struct SkinnyConfig { int TN, stages, ks, stage_u, kk; size_t smem; };
 
 // Resident clusters per (device, TN, stages, smem, ks), cached.
 int max_clusters_cached(int TN, int stages, size_t smem, int ks) {
@@ -163,41 +163,53 @@ int max_clusters_cached(int TN, int stages, size_t smem, int ks) {
     return n;
 }
 
-// Launch shape of the skinny kernel. It depends only on (T, d_in, d_out), so a
-// base-only call and a call with a plan split K identically: shared memory is
-// sized for U rows of rank up to kStageURank whether or not they are used.
-SkinnyConfig skinny_config(int T, int K, int N) {
+int skinny_stages(int TN, bool fuse, int kk) {
+    int st = (int)(((size_t)192 * 1024) / skinny_stage_bytes(TN, fuse, kk));
+    return st < 2 ? 2 : (st > 6 ? 6 : st);
+}
+
+// K slices per stage: the most (<= 4) for which two stages fit in 192 KB.
+// The 3-D views that load several slices at once need d_in % 64 == 0.
+int skinny_kk(int TN, bool fuse, int K) {
+    if (K % 64 != 0) return 1;
+    for (int kk = 4; kk > 1; kk /= 2)
+        if (kk <= K / 64 && 2 * skinny_stage_bytes(TN, fuse, kk) <= (size_t)192 * 1024) return kk;
+    return 1;
+}
+
+// Launch shape of the skinny kernel. The K split depends only on (T, d_in,
+// d_out) - a base-only call, a call with the shrink kernel ahead and one with
+// the shrink fused in split K identically, so their partial sums agree. The
+// kernel holds tensor memory, so it runs one CTA per SM, and a CTA of the next
+// GEMM cannot share an SM with it: the split is the largest (<= 8) whose CTAs
+// fit in half of the SMs, so that consecutive GEMMs stream their weights side
+// by side. `mode`: 0 base only, 1 U from the shrink kernel, 2 shrink fused in.
+SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max) {
     SkinnyConfig c;
     const int Tt = T < kSkinnyMaxT ? T : kSkinnyMaxT;
     c.TN = ((Tt + 15) / 16) * 16;
     if (c.TN < 16) c.TN = 16;
-    const size_t stage = (size_t)128 * 64 * 2 + (size_t)c.TN * 64 * 2;
-    const size_t budget = 200 * 1024;
-    c.can_stage_u = skinny_epi_bytes(c.TN, kStageURank, true) + 2048 <= budget ? 1 : 0;
-    // 2 CTAs per SM when 4 stages fit in half the shared memory, else 1 with
-    // as many stages as fit.
-    if (skinny_smem_bytes(c.TN, 4, kStageURank, c.can_stage_u) <= 113 * 1024) {
-        c.stages = 4;
-    } else {
-        c.stages = (int)(budget / stage);
-        if (c.stages > 6) c.stages = 6;
-        if (c.stages < 2) c.stages = 2;
-    }
-    c.smem = skinny_smem_bytes(c.TN, c.stages, kStageURank, c.can_stage_u);
+    const int canon_stages = skinny_stages(c.TN, false, 1);
+    const size_t canon_smem = skinny_smem_bytes(c.TN, canon_stages, 8, false, false, true, 1);
     const int units = ((N + 127) / 128) * ((T + c.TN - 1) / c.TN);
     const int kb = (K + 63) / 64;
-    // Largest split (<= 8) whose clusters all fit in one wave; every split must
-    // own at least one K block.
     c.ks = 1;
     for (int ks = 8; ks >= 2; ks /= 2) {
         if (kb < ks) continue;
         const int per = (kb + ks - 1) / ks;
         if ((ks - 1) * per >= kb) continue;
-        if (units <= max_clusters_cached(c.TN, c.stages, c.smem, ks)) {
+        if (units * ks > num_sms() / 2) continue;
+        if (units <= max_clusters_cached(c.TN, canon_stages, canon_smem, ks)) {
             c.ks = ks;
             break;
         }
     }
+    const bool fuse = mode == 2;
+    c.kk = skinny_kk(c.TN, fuse, K);
+    c.stages = skinny_stages(c.TN, fuse, c.kk);
+    c.stage_u = (mode == 1 && R_max <= kStageURank &&
+                 skinny_epi_bytes(c.TN, R_max, true, false, false) + 2048 <= (size_t)200 * 1024) ? 1 : 0;
+    c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, mode == 0, c.kk);
     return c;
 }
 
@@ -457,7 +469,16 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
               !overlaps(prev, pool->B, (size_t)pool->S * d_out * pool->R_max * 2) &&
               !overlaps(prev, pool->rank, (size_t)pool->S * 4) && !overlaps(prev, pool->scale, (size_t)pool->S * 4);
 
-    if (plan) {
+    // Decode batches of one token tile, with a pool whose adapter slots' A rows
+    // (slots 1..S-1) fit one 128-row tile, compute U inside the GEMM (tensor
+    // cores, that A tile against each K slice of x): no shrink kernel, and
+    // everything but the stores of y comes before the GEMM's wait. The tokens'
+    // slots are read during the K loop, so the ids must not come from the
+    // kernel ahead.
+    const bool ids_early = !plan || !overlaps(prev, plan->ids, (size_t)T * 4);
+    const bool fuse = plan && path == 0 && T <= 64 && ids_early && pool->S >= 2 &&
+                      (pool->S - 1) * pool->R_max <= 128 && ((T + 15) / 16 * 16) * pool->R_max <= 2048;
+    if (plan && !fuse) {
         ShrinkArgs sa;
         sa.x = static_cast<const __nv_bfloat16*>(x);
         sa.ids = plan->ids;
@@ -490,16 +511,47 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     ex.U = plan ? plan->U : nullptr;
     ex.B = plan ? static_cast<const __nv_bfloat16*>(pool->B) : nullptr;
     ex.rank = plan ? pool->rank : nullptr;
-    ex.R_max = plan ? pool->R_max : 0;
+    ex.scale = plan ? pool->scale : nullptr;
+    ex.R_max = plan ? pool->R_max : 8;
     ex.S = plan ? pool->S : 0;
 
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_start, st) != cudaSuccess) return LORA_ECUDA;
     if (path == 0) {
-        const SkinnyConfig c = skinny_config(T, d_in, d_out);
-        CUtensorMap tmW, tmX;
-        if (!make_tmap(&tmW, W, (uint64_t)d_in, (uint64_t)d_out, 64, 128) ||
-            !make_tmap(&tmX, x, (uint64_t)d_in, (uint64_t)T, 64, (uint32_t)c.TN))
-            return LORA_ECUDA;
+        const int mode = !plan ? 0 : (fuse ? 2 : 1);
+        const SkinnyConfig c = skinny_config(T, d_in, d_out, mode, plan ? pool->R_max : 8);
+        CUtensorMap tmW, tmX, tmA;
+        const uint64_t ksl = (uint64_t)d_in / 64;           // 64-column slices (kk > 1: d_in % 64 == 0)
+        if (c.kk == 1) {
+            if (!make_tmap(&tmW, W, (uint64_t)d_in, (uint64_t)d_out, 64, 128) ||
+                !make_tmap(&tmX, x, (uint64_t)d_in, (uint64_t)T, 64, (uint32_t)c.TN))
+                return LORA_ECUDA;
+        } else {
+            // [rows][d_in] seen as {64 columns, rows, slices}: a box of kk
+            // slices lands as kk consecutive 128-byte swizzled tiles
+            const uint64_t dw[3] = {64, (uint64_t)d_out, ksl}, dx[3] = {64, (uint64_t)T, ksl};
+            const uint64_t pr[2] = {(uint64_t)d_in * 2, 128};
+            const uint32_t bw[3] = {64, 128, (uint32_t)c.kk}, bx[3] = {64, (uint32_t)c.TN, (uint32_t)c.kk};
+            if (!make_tmap_nd(&tmW, W, 3, dw, pr, bw, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !make_tmap_nd(&tmX, x, 3, dx, pr, bx, CU_TENSOR_MAP_SWIZZLE_128B))
+                return LORA_ECUDA;
+        }
+        if (fuse) {
+            // A pool [S][R_max][d_in]: slots 1..S-1, R_max rows x 64 columns each
+            // (x kk slices), per copy
+            if (c.kk == 1) {
+                const uint64_t da[3] = {(uint64_t)d_in, (uint64_t)pool->R_max, (uint64_t)pool->S};
+                const uint64_t pa[2] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2};
+                const uint32_t ba[3] = {64, (uint32_t)pool->R_max, (uint32_t)(pool->S - 1)};
+                if (!make_tmap_nd(&tmA, pool->A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+            } else {
+                const uint64_t da[4] = {64, (uint64_t)pool->R_max, (uint64_t)pool->S, ksl};
+                const uint64_t pa[3] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2, 128};
+                const uint32_t ba[4] = {64, (uint32_t)pool->R_max, (uint32_t)(pool->S - 1), (uint32_t)c.kk};
+                if (!make_tmap_nd(&tmA, pool->A, 4, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+            }
+        } else {
+            tmA = tmX;                 // unused
+        }
         SkinnyArgs a;
         a.y = static_cast<__nv_bfloat16*>(y);
         a.ex = ex;
@@ -510,11 +562,14 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.kb_total = (d_in + 63) / 64;
         a.ks = c.ks;
         a.stages = c.stages;
-        a.stage_u = (plan && c.can_stage_u && pool->R_max <= kStageURank) ? 1 : 0;
+        a.stage_u = c.stage_u;
+        a.fuse = fuse ? 1 : 0;
+        a.a_rows = fuse ? (pool->S - 1) * pool->R_max : 0;
+        a.kk = c.kk;
         a.smem = c.smem;
         a.x_early = x_early ? 1 : 0;
-        a.ids_early = (!plan || !overlaps(prev, plan->ids, (size_t)T * 4)) ? 1 : 0;
-        if (launch_skinny(tmW, tmX, a, pdl, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
+        a.ids_early = ids_early ? 1 : 0;
+        if (launch_skinny(tmW, tmX, tmA, a, pdl, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;
         CUtensorMap tmA, tmB, tmU, tmBs;

@@ -36,24 +36,36 @@ constexpr int kSkThreads = 256;             // 8 warps: TMA, MMA, then six that 
 constexpr int kBK = 64;                     // K elements per stage (128 bytes of bf16)
 constexpr int kWRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kWTileBytes = kWRows * kBK * 2;
-
-// Epilogue scratch after the K loop, in the pipeline's buffers: the received
-// partials [ks][TN][128/ks] (128 x TN floats) and (when staged) U rows
-// [TN][R_max].
-size_t skinny_epi_bytes(int TN, int R_max, bool stage_u) {
-    return (size_t)kWRows * TN * 4 + (stage_u ? (size_t)TN * R_max * 4 : 0);
-}
+constexpr int kMaxAct = kWRows / 8;        // adapter slots of an A tile (R_max >= 8 rows each)
 
 // The tile's tokens grouped by slot (kept apart from the pipeline's buffers,
-// since it is built during the K loop): per token its slot and rank rounded up
-// to 8, the tokens in slot order, and per group its slot, rank and first
-// position, plus the group count.
-size_t skinny_grp_bytes(int TN) { return ((size_t)6 * TN + 4) * 4; }
+// since it is built during the K loop), and the A tile's slot list.
+__host__ __device__ size_t skinny_grp_bytes(int TN) { return ((size_t)8 * TN + kMaxAct + 8) * 4; }
 
-size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u) {
-    const size_t stage = (size_t)kWTileBytes + (size_t)TN * kBK * 2;
-    const size_t pipe = stage * stages;
-    const size_t epi = skinny_epi_bytes(TN, R_max, stage_u);
+// Epilogue scratch after the K loop, in the pipeline's buffers: the received
+// partials [ks][TN][128/ks] (128 x TN floats), then per mode
+//   late U (shrink kernel ahead):  U rows [TN][R_max] when staged;
+//   fused shrink:  U [TN][R_max], U partials [ks <= 8][TN][R_max], y staging;
+//   base only:     y staging [TN][<= 128] bf16.
+__host__ __device__ size_t skinny_epi_bytes(int TN, int R_max, bool stage_u, bool fuse, bool base_only) {
+    const size_t red = (size_t)kWRows * TN * 4;
+    const size_t ystage = (size_t)TN * kWRows * 2;
+    if (fuse) return red + (size_t)9 * TN * R_max * 4 + ystage;
+    if (base_only) return red + ystage;
+    return red + (stage_u ? (size_t)TN * R_max * 4 : 0);
+}
+
+// One pipeline stage holds `kk` consecutive 64-column K slices of the weight
+// tile, of x and (fused) of the A tile, each slice in its own 128-byte
+// swizzled block.
+__host__ __device__ size_t skinny_stage_bytes(int TN, bool fuse, int kk) {
+    return (size_t)kk * ((size_t)kWTileBytes + (size_t)TN * kBK * 2 + (fuse ? (size_t)kWTileBytes : 0));
+}
+
+__host__ __device__ size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u, bool fuse, bool base_only,
+                                             int kk) {
+    const size_t pipe = skinny_stage_bytes(TN, fuse, kk) * stages;
+    const size_t epi = skinny_epi_bytes(TN, R_max, stage_u, fuse, base_only);
     const size_t body = pipe > epi ? pipe : epi;
     return 1024 /*alignment slack*/ + body + 256 /*barriers*/ + skinny_grp_bytes(TN);
 }
@@ -80,6 +92,7 @@ __device__ __forceinline__ float expand_dot_from(const float* __restrict__ u, co
     return d;
 }
 
+
 struct TileGroups {
     int* tslot;   // [TN] slot of each token (0: no correction)
     int* tr8;     // [TN] its rank rounded up to 8 (0 with slot 0)
@@ -88,7 +101,11 @@ struct TileGroups {
     int* gr8;     // [TN] rank of each group, rounded up to 8
     int* gbeg;    // [TN + 1] first position of each group in `order`, then n_tok
     int* n_groups;
+    // with the shrink fused in:
+    int* tact;    // [TN] the token's slot - 1 (its A-tile rows start at tact * R_max), or -1
+    float* tsc;   // [TN] alpha / r of the token's slot
 };
+
 
 __device__ __forceinline__ void grp_barrier(int nthr) {
     asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
@@ -97,7 +114,9 @@ __device__ __forceinline__ void grp_barrier(int nthr) {
 // Group the tile's tokens by adapter slot, with the `nthr` threads (whole
 // warps) numbered i0 = 0.. that run it, and send this CTA's rows of B for
 // every group to L2. Invalid ids, slot 0 and rank-0 slots all map to slot 0:
-// those tokens get the base output only. Reads the ids, the pool's ranks and B.
+// those tokens get the base output only. Reads the ids, the pool's ranks and
+// scales, and B. With the shrink fused in, also notes each token's rows of the
+// A tile and its slot's alpha / r.
 __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, int n_tok, int i0, int nthr,
                              int n_lo, int n_rows, int n_rows_per) {
     const bool with_ex = a.ex.ids != nullptr;
@@ -160,6 +179,13 @@ __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, 
             *gp.n_groups = G;
         }
     }
+    if (a.fuse) {                      // the A tile holds slots 1..S-1 in order
+        for (int t = i0; t < n_tok; t += nthr) {
+            const int s = gp.tslot[t];
+            gp.tact[t] = s - 1;
+            gp.tsc[t] = s > 0 ? a.ex.scale[s] : 0.f;
+        }
+    }
     grp_barrier(nthr);
     if (with_ex && n_rows > 0) {       // rows [n_lo, n_lo + n_rows) of B_s are contiguous
         const int G = *gp.n_groups;
@@ -172,27 +198,48 @@ __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, 
 
 __global__ void __launch_bounds__(kSkThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   SkinnyArgs a) {
+                   const __grid_constant__ CUtensorMap tmA, SkinnyArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, derived by offsetting the shared array itself so
     // the compiler keeps every pointer below in the shared address space.
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int TN = a.TN;
     const int stages = a.stages;
+    const bool fuse = a.fuse != 0;
+    const int R = a.ex.R_max;
+    const int KK = a.kk;                                          // K slices per stage
     const uint32_t x_tile_bytes = (uint32_t)TN * kBK * 2;
-    const uint32_t stage_bytes = kWTileBytes + x_tile_bytes;
+    const uint32_t w_off = 0, x_off = (uint32_t)KK * kWTileBytes;  // within a stage
+    const uint32_t a_off = x_off + (uint32_t)KK * x_tile_bytes;
+    const uint32_t a_slice = (uint32_t)a.a_rows * kBK * 2;        // one slice of the A tile
+    const uint32_t stage_bytes = (uint32_t)skinny_stage_bytes(TN, fuse, KK);
     const size_t pipe = (size_t)stage_bytes * stages;
-    const size_t epi_bytes = (size_t)kWRows * TN * 4 + (a.stage_u ? (size_t)TN * a.ex.R_max * 4 : 0);
+    const size_t epi_bytes = skinny_epi_bytes(TN, R, a.stage_u != 0, fuse, a.ex.ids == nullptr);
     uint8_t* tail = base + (pipe > epi_bytes ? pipe : epi_bytes);
     uint64_t* full = reinterpret_cast<uint64_t*>(tail);          // [stages]
     uint64_t* empty = full + stages;                              // [stages]
     uint64_t* accf = empty + stages;                              // [1]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
-    float* red = reinterpret_cast<float*>(base);                  // received partials, after the K loop
-    float* sU = red + (size_t)kWRows * TN;                        // staged U rows, after the K loop
+    // After the K loop, in the pipeline's buffers: the received partials of
+    // the weight rows this CTA finishes, [ks][TN][rows_per] floats, then
+    //  - late U (the shrink ran as its own kernel): the tile's U rows [TN][R];
+    //  - fused shrink: every CTA's partial U of each token's own slot
+    //    [ks][TN][R], the reduced and scaled U [TN][R], and y [TN][rows_per]
+    //    in bf16, stored after the wait; without a plan only the latter.
+    float* red = reinterpret_cast<float*>(base);
+    float* sU = red + (size_t)kWRows * TN;
+    float* upart = sU + (fuse ? (size_t)TN * R : 0);              // fused: [ks][TN][R]
+    __nv_bfloat16* ystage = reinterpret_cast<__nv_bfloat16*>(upart + (fuse ? (size_t)a.ks * TN * R : 0));
     int* gmem = reinterpret_cast<int*>(tail + 256);
-    const TileGroups gp{gmem, gmem + TN, gmem + 2 * TN, gmem + 3 * TN, gmem + 4 * TN, gmem + 5 * TN,
-                        gmem + 6 * TN + 1};
+    const TileGroups gp{gmem,
+                        gmem + TN,
+                        gmem + 2 * TN,
+                        gmem + 3 * TN,
+                        gmem + 4 * TN,
+                        gmem + 5 * TN,
+                        gmem + 6 * TN + 1,
+                        gmem + 6 * TN + 2,
+                        reinterpret_cast<float*>(gmem + 7 * TN + 2)};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x;
@@ -207,11 +254,16 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int n_lo = n0 + kz * rows_per;
     const int n_rows = max(0, min(rows_per, a.N - n_lo));
     const int n_tok = min(TN, a.T - t0);
-    const uint32_t tmem_cols = TN <= 32 ? 32u : (TN <= 64 ? 64u : (TN <= 128 ? 128u : 256u));
+    const uint32_t acc_cols = (uint32_t)TN * (fuse ? 2u : 1u);   // weight accumulator, then U's
+    const uint32_t tmem_cols = acc_cols <= 32 ? 32u : (acc_cols <= 64 ? 64u : (acc_cols <= 128 ? 128u : 256u));
+    // The epilogue stores y only after the wait, from shared memory, unless U
+    // comes from the shrink kernel ahead of this one.
+    const bool late_u = a.ex.ids != nullptr && !fuse;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
+        if (fuse) tma_prefetch_desc(&tmA);
         for (int i = 0; i < stages; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
             mbar_init(smem_u32(&empty[i]), 1);
@@ -233,35 +285,54 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     bool ok = true;
     if (warp == 0 && lane == 0) {
-        // TMA producer. Weights are never written by the kernels this one waits
-        // for, so the first `stages` weight tiles go to shared memory and the next
-        // `stages` to L2 before the wait. x is loaded before
-        // the wait too unless the host saw that the previous kernel writes it.
-        const int pre = min(nkb, stages);
+        // TMA producer, one copy per operand per stage (a stage is KK slices of
+        // 64 columns: a TMA copy has a fixed cost, so fewer, larger copies
+        // stream faster). Weights are never written by the kernels this one
+        // waits for, so the first `stages` stages of weights are requested
+        // before the wait; x too unless the host saw that the previous kernel
+        // writes it. With the shrink fused in, each stage also holds the A rows
+        // of every adapter slot of the pool (slots 1..S-1, R_max rows each) for
+        // the same slices: the A tile.
+        const int nst = (nkb + KK - 1) / KK;                      // stages of this CTA's K range
+        const int pre = min(nst, stages);
+        const uint32_t tx = (uint32_t)KK * (kWTileBytes + x_tile_bytes + (fuse ? a_slice : 0u));
+        // slice index of stage i: kb_lo + i KK (with kk > 1 the tensor maps
+        // are 3-D / 4-D views whose last coordinate counts 64-column slices)
+        auto load_w = [&](uint32_t dst, uint32_t fb, int i) {
+            if (KK == 1) tma_load_2d(dst, &tmW, fb, (kb_lo + i) * kBK, n0);
+            else tma_load_3d(dst, &tmW, fb, 0, n0, kb_lo + i * KK);
+        };
+        auto load_x = [&](uint32_t dst, uint32_t fb, int i) {
+            if (KK == 1) tma_load_2d(dst, &tmX, fb, (kb_lo + i) * kBK, t0);
+            else tma_load_3d(dst, &tmX, fb, 0, t0, kb_lo + i * KK);
+        };
+        auto load_a = [&](uint32_t dst, uint32_t fb, int i) {
+            if (KK == 1) tma_load_3d(dst, &tmA, fb, (kb_lo + i) * kBK, 0, 1);
+            else tma_load_4d(dst, &tmA, fb, 0, 0, 1, kb_lo + i * KK);
+        };
         for (int i = 0; i < pre; ++i) {
             const uint32_t fb = smem_u32(&full[i]);
-            const uint32_t sW = smem_u32(base + (size_t)i * stage_bytes);
-            mbar_arrive_expect_tx(fb, stage_bytes);
-            tma_load_2d(sW, &tmW, fb, (kb_lo + i) * kBK, n0);
-            if (a.x_early) tma_load_2d(sW + kWTileBytes, &tmX, fb, (kb_lo + i) * kBK, t0);
+            const uint32_t sb = smem_u32(base + (size_t)i * stage_bytes);
+            mbar_arrive_expect_tx(fb, tx);
+            load_w(sb + w_off, fb, i);
+            if (fuse) load_a(sb + a_off, fb, i);
+            if (a.x_early) load_x(sb + x_off, fb, i);
         }
-        // One more ring's worth to L2: enough bytes in flight to cover the wait,
-        // without queueing this CTA's whole range ahead of other kernels' loads.
-        for (int i = pre; i < min(nkb, 2 * stages); ++i) tma_prefetch_l2_2d(&tmW, (kb_lo + i) * kBK, n0);
         if (!a.x_early) pdl_wait();
         int issued = 0;
-        for (int i = 0; i < nkb && ok; ++i) {
+        for (int i = 0; i < nst && ok; ++i) {
             const int st = i % stages;
             const uint32_t ph = (uint32_t)(i / stages) & 1u;
-            const uint32_t sW = smem_u32(base + (size_t)st * stage_bytes);
+            const uint32_t sb = smem_u32(base + (size_t)st * stage_bytes);
             const uint32_t fb = smem_u32(&full[st]);
             if (i >= pre) {
                 if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
-                mbar_arrive_expect_tx(fb, stage_bytes);
-                tma_load_2d(sW, &tmW, fb, (kb_lo + i) * kBK, n0);
-                tma_load_2d(sW + kWTileBytes, &tmX, fb, (kb_lo + i) * kBK, t0);
+                mbar_arrive_expect_tx(fb, tx);
+                load_w(sb + w_off, fb, i);
+                load_x(sb + x_off, fb, i);
+                if (fuse) load_a(sb + a_off, fb, i);
             } else if (!a.x_early) {
-                tma_load_2d(sW + kWTileBytes, &tmX, fb, (kb_lo + i) * kBK, t0);
+                load_x(sb + x_off, fb, i);
             }
             ++issued;
         }
@@ -269,19 +340,34 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         for (int i = max(0, max(issued, pre) - stages); i < max(issued, pre); ++i)
             mbar_wait(smem_u32(&full[i % stages]), (uint32_t)(i / stages) & 1u, kErrFullWait);
     } else if (warp == 1 && lane == 0) {
-        // MMA issuer.
+        // MMA issuer: the weight tile into columns [0, TN) and, fused, the A
+        // tile into [TN, 2 TN), both against the same x tile. A stage's slices
+        // past this CTA's K range (loaded with the last stage) are skipped.
         const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)TN);
-        for (int i = 0; i < nkb && ok; ++i) {
+        const int nst = (nkb + KK - 1) / KK;
+        for (int i = 0; i < nst && ok; ++i) {
             const int st = i % stages;
             const uint32_t ph = (uint32_t)(i / stages) & 1u;
             if (!mbar_wait(smem_u32(&full[st]), ph, kErrFullWait)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sW = smem_u32(base + (size_t)st * stage_bytes);
-            const uint32_t sX = sW + kWTileBytes;
+            const uint32_t sb = smem_u32(base + (size_t)st * stage_bytes);
+            const int n_sl = min(KK, nkb - i * KK);
+            for (int q = 0; q < n_sl; ++q) {
+                const uint32_t sW = sb + w_off + (uint32_t)q * kWTileBytes;
+                const uint32_t sX = sb + x_off + (uint32_t)q * x_tile_bytes;
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                tc_mma_bf16(tmem, sdesc_sw128(sW + kk * 32), sdesc_sw128(sX + kk * 32), idesc,
-                            (i > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    tc_mma_bf16(tmem, sdesc_sw128(sW + kk * 32), sdesc_sw128(sX + kk * 32), idesc,
+                                (i > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (fuse) {
+                    const uint32_t sA = sb + a_off + (uint32_t)q * a_slice;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        tc_mma_bf16(tmem + (uint32_t)TN, sdesc_sw128(sA + kk * 32), sdesc_sw128(sX + kk * 32), idesc,
+                                    (i > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
             }
             tc_commit(smem_u32(&empty[st]));
         }
@@ -323,31 +409,71 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int i = 0; i < 16; ++i)
                 st_cluster_f32(dst0 + (uint32_t)((((kz * TN) + c + i) * rows_per + ln) * 4), v[i]);
         }
+        if (fuse) {
+            // U: row `row` of the A tile is rank j of adapter slot ai + 1 (row =
+            // ai R + j). Token t needs it when t is on that slot; its partial
+            // goes to upart[kz][t][j] of every CTA of the cluster.
+            const int ai = row / R, j = row - ai * R;
+            const uint32_t up = smem_u32(upart);
+            for (int c = 16 * (warp >> 2); c < TN; c += 32) {
+                float v[16];
+                if (have) {
+                    tc_ld16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(TN + c), v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = c + i;
+                    if (t < n_tok && gp.tact[t] == ai) {
+                        const uint32_t off = (uint32_t)((((kz * TN) + t) * R + j) * 4);
+                        for (int q = 0; q < a.ks; ++q)
+                            st_cluster_f32((a.ks > 1 ? mapa_shared(up, (uint32_t)q) : up) + off, v[i]);
+                    }
+                }
+            }
+        }
     }
     tc_fence_before();
 
-    // U comes from the kernels before this one, and so do the ids when the
-    // host could not rule that out: only from here on does the epilogue depend
-    // on them.
-    pdl_wait();
     const bool with_ex = a.ex.ids != nullptr;
-    if (!a.ids_early) group_tokens(a, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
-    const int R = a.ex.R_max;
-    if (with_ex && a.stage_u) {
-        const int R4 = R >> 2;
-        for (int q = threadIdx.x; q < n_tok * R4; q += kSkThreads) {
-            const int tl = q / R4, j4 = q - tl * R4;
-            if (gp.tr8[tl] > j4 * 4)
-                reinterpret_cast<float4*>(sU)[q] =
-                    __ldg(reinterpret_cast<const float4*>(a.ex.U + (size_t)(t0 + tl) * R) + j4);
+    if (late_u) {
+        // U comes from the kernels before this one, and so do the ids when the
+        // host could not rule that out: only from here on does the epilogue
+        // depend on them.
+        pdl_wait();
+        if (!a.ids_early)
+            group_tokens(a, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
+        if (a.stage_u) {
+            const int R4 = R >> 2;
+            for (int q = threadIdx.x; q < n_tok * R4; q += kSkThreads) {
+                const int tl = q / R4, j4 = q - tl * R4;
+                if (gp.tr8[tl] > j4 * 4)
+                    reinterpret_cast<float4*>(sU)[q] =
+                        __ldg(reinterpret_cast<const float4*>(a.ex.U + (size_t)(t0 + tl) * R) + j4);
+            }
         }
     }
     if (a.ks > 1) cluster.sync();      // every push into this CTA has landed
     else __syncthreads();
+    if (fuse) {
+        // U[t, j] = (alpha / r) * sum over cluster ranks (in rank order) of the
+        // partials, for j below the token's rank rounded up to 8
+        for (int q = threadIdx.x; q < n_tok * R; q += kSkThreads) {
+            const int t = q / R, j = q - t * R;
+            if (gp.tact[t] >= 0 && j < gp.tr8[t]) {
+                float u = upart[(size_t)t * R + j];
+                for (int z = 1; z < a.ks; ++z) u += upart[((size_t)z * TN + t) * R + j];
+                sU[(size_t)t * R + j] = gp.tsc[t] * u;
+            }
+        }
+        __syncthreads();
+    }
 
-    // Work items are (weight row, slot group) pairs: an item loads its row of
-    // B_s once (the next item's is requested while this one is computed) and
-    // finishes every token of the group:
+    // Work items are (weight row, slot-group piece) pairs: an item loads its
+    // row of B_s once (the next item's is requested while this one is
+    // computed) and finishes every token of the piece:
     //   y[t, n] = bf16( sum_z partial_z[t, n] + sum_j U[t, j] B[s, n, j] ),
     // z in rank order, j ascending; slot-0 groups only sum the partials.
     const int lg = __ffs(rows_per) - 1;               // rows_per = 128 / ks is a power of two
@@ -355,6 +481,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int ks = a.ks;
     __nv_bfloat16* __restrict__ yp = a.y;
     const __nv_bfloat16* __restrict__ Bp = a.ex.B;
+    const bool u_smem = fuse || a.stage_u;
     auto load_b = [&](int item, uint4 (&b)[8]) {
         const int g = item >> lg, ln = item & (rows_per - 1);
         const int r8 = gp.gr8[g];
@@ -370,7 +497,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int g = item >> lg, ln = item & (rows_per - 1);
         if (ln < n_rows) {
             const int n = n_lo + ln;
-            const int r8 = gp.gr8[g];
+            const int r8 = with_ex ? gp.gr8[g] : 0;
             const int pe = gp.gbeg[g + 1];
             // two tokens at a time: independent chains, each B element
             // unpacked once for both
@@ -392,8 +519,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     vb = (z < ks) ? vb + pb[z] : vb;
                 }
                 if (r8 > 0) {
-                    const float* ua = a.stage_u ? sU + (size_t)ta * R : a.ex.U + (size_t)(t0 + ta) * R;
-                    const float* ub = a.stage_u ? sU + (size_t)tb * R : a.ex.U + (size_t)(t0 + tb) * R;
+                    const float* ua = u_smem ? sU + (size_t)ta * R : a.ex.U + (size_t)(t0 + ta) * R;
+                    const float* ub = u_smem ? sU + (size_t)tb * R : a.ex.U + (size_t)(t0 + tb) * R;
                     float da = 0.f, db = 0.f;
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -422,12 +549,30 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                     va += da;
                     vb += db;
                 }
-                yp[(size_t)(t0 + ta) * a.N + n] = __float2bfloat16_rn(va);
-                if (two) yp[(size_t)(t0 + tb) * a.N + n] = __float2bfloat16_rn(vb);
+                if (late_u) {
+                    yp[(size_t)(t0 + ta) * a.N + n] = __float2bfloat16_rn(va);
+                    if (two) yp[(size_t)(t0 + tb) * a.N + n] = __float2bfloat16_rn(vb);
+                } else {
+                    ystage[(size_t)ta * rows_per + ln] = __float2bfloat16_rn(va);
+                    if (two) ystage[(size_t)tb * rows_per + ln] = __float2bfloat16_rn(vb);
+                }
             }
         }
 #pragma unroll
         for (int c = 0; c < 8; ++c) bc[c] = bn[c];
+    }
+    if (!late_u) {
+        // Everything above needed only this kernel's inputs; y may still be
+        // read or written by the kernels ahead of it, so it is stored after the
+        // wait: 16-byte runs of n_rows consecutive outputs per token.
+        __syncthreads();
+        pdl_wait();
+        const int v8 = n_rows >> 3;                   // n_rows is a multiple of 8
+        for (int q = threadIdx.x; q < n_tok * v8; q += kSkThreads) {
+            const int t = q / v8, c = q - t * v8;
+            *reinterpret_cast<uint4*>(yp + (size_t)(t0 + t) * a.N + n_lo + c * 8) =
+                *reinterpret_cast<const uint4*>(ystage + (size_t)t * rows_per + c * 8);
+        }
     }
 
     if (warp == 1) {
@@ -436,8 +581,8 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     }
 }
 
-cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyArgs& a,
-                          bool pdl, int num_sms, cudaStream_t stream) {
+cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmA,
+                          const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream) {
     (void)num_sms;
     const size_t smem = a.smem;
     cudaError_t e = ensure_smem_attr((const void*)gemm_skinny_kernel, 1, smem);
@@ -461,7 +606,7 @@ cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel, tmW, tmX, a);
+    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel, tmW, tmX, tmA, a);
 }
 
 // How many clusters of `ks` CTAs of this configuration can be resident at once.

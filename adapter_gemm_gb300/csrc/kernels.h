@@ -51,9 +51,10 @@ struct ShrinkArgs {
 // (no correction anywhere).
 struct ExpandArgs {
     const int32_t* ids;            // [T] the step's raw slot ids (invalid ones mean slot 0)
-    const float* U;                // [T, R_max] by token
+    const float* U;                // [T, R_max] by token (shrink kernel ahead)
     const __nv_bfloat16* B;        // [S, N, R_max]
     const int32_t* rank;           // [S]
+    const float* scale;            // [S] alpha / r (fused shrink)
     int R_max;
     int S;
 };
@@ -69,6 +70,9 @@ struct SkinnyArgs {
     int stage_u;       // copy the tile's U rows into shared memory for the epilogue
     int x_early;       // x may be loaded before the wait for the previous kernel
     int ids_early;     // the ids may be read before that wait
+    int fuse;          // compute U in this kernel (an A tile per K slice) instead of reading it
+    int a_rows;        // rows of the A tile: (S - 1) * R_max, at most 128
+    int kk;            // 64-column K slices per pipeline stage (> 1: 3-D / 4-D tensor maps)
     size_t smem;       // dynamic shared memory of the launch
 };
 
@@ -85,8 +89,8 @@ struct WideArgs {
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream);
-cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const SkinnyArgs& a,
-                          bool pdl, int num_sms, cudaStream_t stream);
+cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmA,
+                          const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream);
 cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
                         const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
 cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);
@@ -100,8 +104,10 @@ cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
 
 // Shared-memory bytes the skinny kernel needs for a token tile of TN columns
 // and `stages` pipeline stages.
-size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u);
-size_t skinny_epi_bytes(int TN, int R_max, bool stage_u);
+__host__ __device__ size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u, bool fuse,
+                                             bool base_only, int kk);
+__host__ __device__ size_t skinny_epi_bytes(int TN, int R_max, bool stage_u, bool fuse, bool base_only);
+__host__ __device__ size_t skinny_stage_bytes(int TN, bool fuse, int kk);
 int skinny_max_active_clusters(int TN, size_t smem, int ks);
 
 }  // namespace lora
