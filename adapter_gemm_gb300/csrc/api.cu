@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <atomic>
 #include <mutex>
 #include <tuple>
 #include <cuda.h>
@@ -214,6 +215,13 @@ SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max) {
 }
 
 cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+std::atomic<uint64_t> g_launches{0};
+
+// Count a launch that succeeded.
+cudaError_t counted(cudaError_t e) {
+    if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+    return e;
+}
 
 // The kernels of a lora_linear call start (programmatic dependent launch)
 // before the kernel ahead of them on the stream has finished, and read their
@@ -263,6 +271,8 @@ int shrink_splits(int max_tiles, int K) {
 extern "C" {
 
 int lora_version(void) { return 1; }
+
+uint64_t lora_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* lora_strerror(lora_status s) {
     switch (s) {
@@ -369,8 +379,10 @@ lora_status lora_pool_install(lora_pool* pool, int slot, const void* A, const vo
     const int K = pool->d_in, N = pool->d_out, R = pool->R_max;
     // Validate before writing: count non-finite values of both factors.
     if (cudaMemsetAsync(pool->work, 0, 4, st) != cudaSuccess) return LORA_ECUDA;
-    if (launch_count_nonfinite(static_cast<const __nv_bfloat16*>(A), (size_t)rank * K, pool->work, st) != cudaSuccess ||
-        launch_count_nonfinite(static_cast<const __nv_bfloat16*>(B), (size_t)N * rank, pool->work, st) != cudaSuccess)
+    if (counted(launch_count_nonfinite(static_cast<const __nv_bfloat16*>(A), (size_t)rank * K, pool->work, st)) !=
+            cudaSuccess ||
+        counted(launch_count_nonfinite(static_cast<const __nv_bfloat16*>(B), (size_t)N * rank, pool->work, st)) !=
+            cudaSuccess)
         return LORA_ECUDA;
     int32_t bad = 0;
     if (cudaMemcpyAsync(&bad, pool->work, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
@@ -417,7 +429,7 @@ lora_status lora_plan(const int32_t* ids, int T, lora_plan_t* plan, void* stream
     // The plan kernel reads the ids before it waits for the kernels ahead of it,
     // unless they alias the output of the previous lora_linear on this stream.
     const bool pdl = !overlaps(last_out(st), ids, (size_t)T * 4);
-    if (launch_plan(ids, T, p, pdl, st) != cudaSuccess) return LORA_ECUDA;
+    if (counted(launch_plan(ids, T, p, pdl, st)) != cudaSuccess) return LORA_ECUDA;
     return LORA_OK;
 }
 
@@ -502,7 +514,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         const bool by_slot = path == 0 && T <= kBySlotMaxT;
         const int grid_x = by_slot ? pool->S - 1 : plan->max_tiles;
         sa.ks = by_slot ? slot_splits(grid_x, d_in) : shrink_splits(plan->max_tiles, d_in);
-        if (launch_shrink(sa, grid_x, by_slot, pdl, st) != cudaSuccess) return LORA_ECUDA;
+        if (grid_x > 0 && counted(launch_shrink(sa, grid_x, by_slot, pdl, st)) != cudaSuccess) return LORA_ECUDA;
         pdl = true;                    // the GEMM follows the shrink, which waited
     }
 
@@ -569,7 +581,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.smem = c.smem;
         a.x_early = x_early ? 1 : 0;
         a.ids_early = ids_early ? 1 : 0;
-        if (launch_skinny(tmW, tmX, tmA, a, pdl, num_sms(), st) != cudaSuccess) return LORA_ECUDA;
+        if (counted(launch_skinny(tmW, tmX, tmA, a, pdl, num_sms(), st)) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;
         CUtensorMap tmA, tmB, tmU, tmBs;
@@ -607,7 +619,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.kb_total = (d_in + 63) / 64;
         int grid = a.m_tiles * a.n_tiles;
         if (grid > num_sms()) grid = num_sms();
-        if (launch_wide(tmA, tmB, tmU, tmBs, a, pdl, grid, st) != cudaSuccess) return LORA_ECUDA;
+        if (counted(launch_wide(tmA, tmB, tmU, tmBs, a, pdl, grid, st)) != cudaSuccess) return LORA_ECUDA;
     }
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;
     set_last_out(st, y, (size_t)T * d_out * 2);

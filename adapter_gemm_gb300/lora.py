@@ -71,6 +71,7 @@ _SIGS = {
     "lora_last_device_error": (_c_int, [ctypes.POINTER(_c_int32)]),
     "lora_strerror": (ctypes.c_char_p, [_c_int]),
     "lora_version": (_c_int, []),
+    "lora_launch_count": (ctypes.c_uint64, []),
 }
 
 
@@ -120,6 +121,11 @@ def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return _c_void_p(t.data_ptr())
+
+
+def launch_count() -> int:
+    """Kernels the library has launched (or captured) so far in this process."""
+    return int(_lib().lora_launch_count())
 
 
 def version() -> int:

@@ -263,13 +263,16 @@ def main():
         for j, (W, pool) in enumerate(copies[c]):
             L.linear(x_of[j], W, pool, plans[c], ys[j])
 
-    launches_per_step = 1 + 2 * len(w.targets)
 
     # ---- warmup (eager), then CUDA graphs: one holding a run of G steps (the
     # copies in rotation), plus one single-step graph per copy for the rest,
     # so the host launches one graph per G steps and never starves the GPU
     for i in range(max(args.warmup, 3)):
         step(i)
+    torch.cuda.synchronize()
+    n0 = L.launch_count()
+    step(0)
+    launches_per_step = L.launch_count() - n0       # the library's own kernels in one step
     torch.cuda.synchronize()
     use_graph = not args.no_graph
     G = n_copies * max(1, -(-16 // n_copies))

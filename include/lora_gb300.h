@@ -213,6 +213,12 @@ const char* lora_strerror(lora_status status);
 /* Library version, for diagnostics. */
 int lora_version(void);
 
+/* Number of kernels this library has launched in this process (or recorded
+ * into a stream capture), counted on the host at each successful launch. A
+ * diagnostic: the difference over one call sequence is the number of kernels
+ * that sequence runs. Thread-safe; never synchronises. */
+uint64_t lora_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif
