@@ -118,7 +118,7 @@ bool valid_sizes(int S, int R_max, int d_in) {
 
 int max_tiles_for(int T, int S) { return (T + kTileRows - 1) / kTileRows + S; }
 
-bool plan_needs_xsorted(int T) { return T > kSkinnyMaxT; }
+bool plan_needs_xsorted(int T) { return T > kSkinnyPathMaxT; }
 
 // Sub-buffer sizes of the plan workspace, in carve order.
 constexpr int kPlanParts = 14;
@@ -182,9 +182,10 @@ int skinny_kk(int TN, bool fuse, int K) {
 // d_out) - a base-only call, a call with the shrink kernel ahead and one with
 // the shrink fused in split K identically, so their partial sums agree. The
 // kernel holds tensor memory, so it runs one CTA per SM, and a CTA of the next
-// GEMM cannot share an SM with it: the split is the largest (<= 8) whose CTAs
-// fit in half of the SMs, so that consecutive GEMMs stream their weights side
-// by side. `mode`: 0 base only, 1 U from the shrink kernel, 2 shrink fused in.
+// GEMM cannot share an SM with it: for decode-sized token tiles the split is
+// the largest (<= 8) whose CTAs fit in half of the SMs, so that consecutive
+// GEMMs stream their weights side by side; wider tiles may use every SM.
+// `mode`: 0 base only, 1 U from the shrink kernel, 2 shrink fused in.
 SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max) {
     SkinnyConfig c;
     const int Tt = T < kSkinnyMaxT ? T : kSkinnyMaxT;
@@ -194,12 +195,15 @@ SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max) {
     const size_t canon_smem = skinny_smem_bytes(c.TN, canon_stages, 8, false, false, true, 1);
     const int units = ((N + 127) / 128) * ((T + c.TN - 1) / c.TN);
     const int kb = (K + 63) / 64;
+    // Decode-sized token tiles are latency-bound: half the SMs, so that the
+    // next GEMM streams beside this one. Wider tiles are compute-heavy: all.
+    const int cap = c.TN <= 64 ? num_sms() / 2 : num_sms();
     c.ks = 1;
     for (int ks = 8; ks >= 2; ks /= 2) {
         if (kb < ks) continue;
         const int per = (kb + ks - 1) / ks;
         if ((ks - 1) * per >= kb) continue;
-        if (units * ks > num_sms() / 2) continue;
+        if (units * ks > cap) continue;
         if (units <= max_clusters_cached(c.TN, canon_stages, canon_smem, ks)) {
             c.ks = ks;
             break;
@@ -447,7 +451,7 @@ lora_status lora_plan_check(const lora_plan_t* plan, void* stream, int32_t* n_in
 int lora_linear_path(int T, int d_in, int d_out) {
     (void)d_in;
     (void)d_out;
-    return T <= kSkinnyMaxT ? 0 : 1;
+    return T <= kSkinnyPathMaxT ? 0 : 1;
 }
 
 lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out, const lora_pool* pool,
@@ -584,10 +588,31 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         if (counted(launch_skinny(tmW, tmX, tmA, a, pdl, num_sms(), st)) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;
+        // 128 x 256 output tiles, or 128 x 128 for mid-sized grids (fewer
+        // than two waves of wide tiles) when the narrow tiles finish in fewer
+        // wide-tile times: waves x width. Depends on the shape only.
+        const int m_tiles = (T + 127) / 128;
+        const int sms = num_sms();
+        const int t256 = m_tiles * ((d_out + 255) / 256), t128 = m_tiles * ((d_out + 127) / 128);
+        const int cost256 = 2 * ((t256 + sms - 1) / sms), cost128 = (t128 + sms - 1) / sms;
+        const int bn = (t256 < 2 * sms && cost128 < cost256) ? 128 : 256;
+        // narrow tiles take two K slices per stage (3-D views; x and the
+        // plan-ordered copy of x are [T][d_in], W is [d_out][d_in]), so that a
+        // stage's copies are as large as a wide tile's
+        const int kk = (bn == 128 && d_in % 64 == 0 && d_in >= 128) ? 2 : 1;
         CUtensorMap tmA, tmB, tmU, tmBs;
-        if (!make_tmap(&tmA, A, (uint64_t)d_in, (uint64_t)T, 64, 128) ||
-            !make_tmap(&tmB, W, (uint64_t)d_in, (uint64_t)d_out, 64, 256))
-            return LORA_ECUDA;
+        if (kk == 1) {
+            if (!make_tmap(&tmA, A, (uint64_t)d_in, (uint64_t)T, 64, 128) ||
+                !make_tmap(&tmB, W, (uint64_t)d_in, (uint64_t)d_out, 64, (uint32_t)bn))
+                return LORA_ECUDA;
+        } else {
+            const uint64_t da[3] = {64, (uint64_t)T, (uint64_t)d_in / 64}, pa[2] = {(uint64_t)d_in * 2, 128};
+            const uint64_t db[3] = {64, (uint64_t)d_out, (uint64_t)d_in / 64}, pb[2] = {(uint64_t)d_in * 2, 128};
+            const uint32_t ba[3] = {64, 128, 2}, bbx[3] = {64, (uint32_t)bn, 2};
+            if (!make_tmap_nd(&tmA, A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !make_tmap_nd(&tmB, W, 3, db, pb, bbx, CU_TENSOR_MAP_SWIZZLE_128B))
+                return LORA_ECUDA;
+        }
         const int R16 = plan ? (pool->R_max + 15) / 16 * 16 : 16;
         if (plan) {
             // expand operands: U hi|lo [T][2*R16] in plan order, B_pool [S][N][R_max]
@@ -595,7 +620,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
             const uint32_t bu[2] = {16, 128};
             const uint64_t db[3] = {(uint64_t)pool->R_max, (uint64_t)d_out, (uint64_t)pool->S};
             const uint64_t pb[2] = {(uint64_t)pool->R_max * 2, (uint64_t)d_out * pool->R_max * 2};
-            const uint32_t bb[3] = {16, 256, 1};
+            const uint32_t bb[3] = {16, (uint32_t)bn, 1};
             if (!make_tmap_nd(&tmU, plan->U_hl, 2, du, pu, bu, CU_TENSOR_MAP_SWIZZLE_32B) ||
                 !make_tmap_nd(&tmBs, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B))
                 return LORA_ECUDA;
@@ -614,8 +639,10 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.T = T;
         a.K = d_in;
         a.N = d_out;
-        a.m_tiles = (T + 127) / 128;
-        a.n_tiles = (d_out + 255) / 256;
+        a.m_tiles = m_tiles;
+        a.n_tiles = (d_out + bn - 1) / bn;
+        a.bn = bn;
+        a.kk = kk;
         a.kb_total = (d_in + 63) / 64;
         int grid = a.m_tiles * a.n_tiles;
         if (grid > num_sms()) grid = num_sms();

@@ -1,5 +1,6 @@
 // The layer for prefill-sized batches: a persistent tcgen05 GEMM over 128x256
-// output tiles, with the expand half of SGMV done on the tensor cores too.
+// output tiles (128x128 when 256-wide tiles would leave SMs idle), with the
+// expand half of SGMV done on the tensor cores too.
 //
 //   acc[i, n]  = sum_k xs[i, k] W[n, k]                          (K loop)
 //   acc[i, n] += sum_j U[i, j] B[s, n, j]   for rows i of slot s  (expand steps)
@@ -30,21 +31,44 @@
 namespace lora {
 
 constexpr int kWdThreads = 256;
-constexpr int kWdBM = 128, kWdBN = 256, kWdBK = 64;
-constexpr int kWdStages = 4;
+constexpr int kWdBM = 128, kWdBK = 64;
 constexpr uint32_t kWdABytes = kWdBM * kWdBK * 2;     // 16 KB
-constexpr uint32_t kWdBBytes = kWdBN * kWdBK * 2;     // 32 KB
-constexpr uint32_t kWdStageBytes = kWdABytes + kWdBBytes;
 constexpr uint32_t kXuBytes = kWdBM * 16 * 2;         // expand step: U tile, 4 KB (hi or lo)
-constexpr uint32_t kXbBytes = kWdBN * 16 * 2;         // expand step: B_s tile, 8 KB
 constexpr int kMaxSegs = kWdBM;                       // segments crossing one 128-row tile
-// ring | barriers (256 B) | two expand lists of kMaxSegs int4 + counts
-constexpr size_t kWdSmem = 1024 + (size_t)kWdStageBytes * kWdStages + 256 + 2 * (size_t)kMaxSegs * 16 + 16;
 
+// Output tiles are 128 x BN: BN = 256, or 128 when 256-wide tiles would be too
+// few to occupy every SM (mid-sized batches).
+// A stage holds KK consecutive 64-column K slices of both operand tiles, each
+// slice its own 128-byte swizzled block, filled by one TMA copy per operand
+// (3-D views when KK > 1): a TMA copy has a fixed cost, so fewer, larger
+// copies keep the tensor cores fed. An expand step takes one stage.
+template <int BN, int KK>
+struct WideCfg {
+    static constexpr uint32_t kBBytes = BN * kWdBK * 2;            // weight slice, 32 / 16 KB
+    static constexpr uint32_t kSliceBytes = kWdABytes + kBBytes;
+    static constexpr uint32_t kStageBytes = KK * kSliceBytes;
+    static constexpr int kStages = (int)((192u * 1024u) / kStageBytes) > 6 ? 6 : (int)((192u * 1024u) / kStageBytes);
+    static constexpr uint32_t kXbBytes = BN * 16 * 2;              // expand step: B_s tile
+    // B_s tiles per expand stage, next to the U tiles (hi, lo)
+    static constexpr int kXPer = (int)((kStageBytes - 2 * kXuBytes) / kXbBytes) > 16
+                                     ? 16 : (int)((kStageBytes - 2 * kXuBytes) / kXbBytes);
+    static constexpr uint32_t kTmemCols = 2 * BN;                  // two accumulators
+    // ring | barriers (256 B) | two expand lists of kMaxSegs int4 + counts
+    static constexpr size_t kSmem = 1024 + (size_t)kStageBytes * kStages + 256 + 2 * (size_t)kMaxSegs * 16 + 16;
+};
+
+template <int BN, int KK>
 __global__ void __launch_bounds__(kWdThreads, 1)
 gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmBs,
                  WideArgs a) {
+    using C = WideCfg<BN, KK>;
+    constexpr int kWdBN = BN;
+    constexpr int kWdStages = C::kStages;
+    constexpr uint32_t kWdStageBytes = C::kStageBytes;
+    constexpr uint32_t kXbBytes = C::kXbBytes;
+    constexpr int kXPer = C::kXPer;
+    const int n_kst = (a.kb_total + KK - 1) / KK;      // K stages per tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)kWdStageBytes * kWdStages);
@@ -81,7 +105,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         fence_mbar_init();
     }
     if (warp == 2) {
-        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -101,15 +125,20 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int mt = tile % a.m_tiles;
                 const int m0 = mt * kWdBM;
                 const int n0 = (tile / a.m_tiles) * kWdBN;
-                for (int kb = 0; kb < a.kb_total; ++kb, ++it) {
+                for (int ksi = 0; ksi < n_kst; ++ksi, ++it) {
                     const int st = it % kWdStages;
                     const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                     if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
                     const uint32_t sA = smem_u32(base + (size_t)st * kWdStageBytes);
                     const uint32_t fb = smem_u32(&full[st]);
                     mbar_arrive_expect_tx(fb, kWdStageBytes);
-                    tma_load_2d(sA, &tmA, fb, kb * kWdBK, m0);
-                    tma_load_2d(sA + kWdABytes, &tmB, fb, kb * kWdBK, n0);
+                    if (KK == 1) {
+                        tma_load_2d(sA, &tmA, fb, ksi * kWdBK, m0);
+                        tma_load_2d(sA + kWdABytes, &tmB, fb, ksi * kWdBK, n0);
+                    } else {           // KK slices of A, then KK slices of B
+                        tma_load_3d(sA, &tmA, fb, 0, m0, ksi * KK);
+                        tma_load_3d(sA + KK * kWdABytes, &tmB, fb, 0, n0, ksi * KK);
+                    }
                     ++issued;
                 }
                 if (!expand || !ok) continue;
@@ -127,19 +156,31 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 }
                 xcount[as] = ns;
                 mbar_arrive(smem_u32(&lfull[as]));
-                for (int q = 0; q < ns && ok; ++q) {
-                    const int4 sg = xlist[as * kMaxSegs + q];
-                    for (int ks = 0; ks < sg.w; ++ks, ++it) {
+                // Expand stages: per 16-rank step, the tile's U rows (hi and
+                // lo, shared by every segment) and the B_s tiles of up to
+                // kXPer segments that reach that step.
+                int maxw = 0;
+                for (int q = 0; q < ns; ++q) maxw = max(maxw, xlist[as * kMaxSegs + q].w);
+                for (int ks = 0; ks < maxw && ok; ++ks) {
+                    for (int q0 = 0; q0 < ns && ok;) {
+                        int sel[kXPer], n_sel = 0, q = q0;
+                        for (; q < ns && n_sel < kXPer; ++q)
+                            if (xlist[as * kMaxSegs + q].w > ks) sel[n_sel++] = q;
+                        q0 = q;
+                        if (n_sel == 0) continue;
                         const int st = it % kWdStages;
                         const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                         if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
                         const uint32_t sU = smem_u32(base + (size_t)st * kWdStageBytes);
                         const uint32_t fb = smem_u32(&full[st]);
-                        mbar_arrive_expect_tx(fb, 2 * kXuBytes + kXbBytes);
+                        mbar_arrive_expect_tx(fb, 2 * kXuBytes + (uint32_t)n_sel * kXbBytes);
                         tma_load_2d(sU, &tmU, fb, ks * 16, m0);                       // U hi
                         tma_load_2d(sU + kXuBytes, &tmU, fb, a.R16 + ks * 16, m0);    // U lo
-                        tma_load_3d(sU + 2 * kXuBytes, &tmBs, fb, ks * 16, n0, sg.x);  // B_s
+                        for (int j = 0; j < n_sel; ++j)                                // B_s
+                            tma_load_3d(sU + 2 * kXuBytes + (uint32_t)j * kXbBytes, &tmBs, fb, ks * 16, n0,
+                                        xlist[as * kMaxSegs + sel[j]].x);
                         ++issued;
+                        ++it;
                     }
                 }
             }
@@ -160,44 +201,61 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (!mbar_wait(smem_u32(&tempty[as]), (use & 1u) ^ 1u, kErrAccFreeWait)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d = tmem + (uint32_t)(as * kWdBN);
-                for (int kb = 0; kb < a.kb_total; ++kb, ++it) {
+                for (int ksi = 0; ksi < n_kst; ++ksi, ++it) {
                     const int st = it % kWdStages;
                     const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                     if (!mbar_wait(smem_u32(&full[st]), ph, kErrFullWait)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t sA = smem_u32(base + (size_t)st * kWdStageBytes);
-                    const uint32_t sB = sA + kWdABytes;
+                    const uint32_t sA0 = smem_u32(base + (size_t)st * kWdStageBytes);
+                    // slices past d_in (the last stage) are zero-filled by TMA
+                    const int n_sl = min(KK, a.kb_total - ksi * KK);
+                    for (int q = 0; q < n_sl; ++q) {
+                        const uint32_t sA = KK == 1 ? sA0 : sA0 + (uint32_t)q * kWdABytes;
+                        const uint32_t sB = KK == 1 ? sA0 + kWdABytes : sA0 + KK * kWdABytes + (uint32_t)q * C::kBBytes;
 #pragma unroll
-                    for (int kk = 0; kk < kWdBK / 16; ++kk)
-                        tc_mma_bf16(d, sdesc_sw128(sA + kk * 32), sdesc_sw128(sB + kk * 32), idesc,
-                                    (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kWdBK / 16; ++kk)
+                            tc_mma_bf16(d, sdesc_sw128(sA + kk * 32), sdesc_sw128(sB + kk * 32), idesc,
+                                        (ksi > 0 || q > 0 || kk > 0) ? 1u : 0u);
+                    }
                     tc_commit(smem_u32(&empty[st]));
                 }
                 if (expand && ok) {
                     if (!mbar_wait(smem_u32(&lfull[as]), use & 1u, kErrFullWait)) { ok = false; break; }
                     const int ns = xcount[as];
-                    for (int q = 0; q < ns && ok; ++q) {
-                        const int4 sg = xlist[as * kMaxSegs + q];
-                        // lanes (rows) outside [sg.y, sg.z) keep their value
-                        uint32_t dis[4];
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int lo = max(sg.y, 32 * w), hi = min(sg.z, 32 * w + 32);
-                            const uint32_t on = (hi <= lo) ? 0u
-                                               : (hi - lo == 32 ? 0xFFFFFFFFu
-                                                                : (((1u << (hi - lo)) - 1u) << (lo - 32 * w)));
-                            dis[w] = ~on;
-                        }
-                        for (int ks = 0; ks < sg.w; ++ks, ++it) {
+                    int maxw = 0;
+                    for (int q = 0; q < ns; ++q) maxw = max(maxw, xlist[as * kMaxSegs + q].w);
+                    // the same stages as the producer: per rank step, groups
+                    // of up to kXPer segments that reach it
+                    for (int ks = 0; ks < maxw && ok; ++ks) {
+                        for (int q0 = 0; q0 < ns && ok;) {
+                            int sel[kXPer], n_sel = 0, q = q0;
+                            for (; q < ns && n_sel < kXPer; ++q)
+                                if (xlist[as * kMaxSegs + q].w > ks) sel[n_sel++] = q;
+                            q0 = q;
+                            if (n_sel == 0) continue;
                             const int st = it % kWdStages;
                             const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                             if (!mbar_wait(smem_u32(&full[st]), ph, kErrFullWait)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t sU = smem_u32(base + (size_t)st * kWdStageBytes);
-                            const uint64_t bdesc = sdesc_sw32(sU + 2 * kXuBytes);
-                            tc_mma_bf16_masked(d, sdesc_sw32(sU), bdesc, idesc, dis);
-                            tc_mma_bf16_masked(d, sdesc_sw32(sU + kXuBytes), bdesc, idesc, dis);
+                            for (int j = 0; j < n_sel; ++j) {
+                                const int4 sg = xlist[as * kMaxSegs + sel[j]];
+                                // lanes (rows) outside [sg.y, sg.z) keep their value
+                                uint32_t dis[4];
+#pragma unroll
+                                for (int w = 0; w < 4; ++w) {
+                                    const int lo = max(sg.y, 32 * w), hi = min(sg.z, 32 * w + 32);
+                                    const uint32_t on = (hi <= lo) ? 0u
+                                                       : (hi - lo == 32 ? 0xFFFFFFFFu
+                                                                        : (((1u << (hi - lo)) - 1u) << (lo - 32 * w)));
+                                    dis[w] = ~on;
+                                }
+                                const uint64_t bdesc = sdesc_sw32(sU + 2 * kXuBytes + (uint32_t)j * kXbBytes);
+                                tc_mma_bf16_masked(d, sdesc_sw32(sU), bdesc, idesc, dis);
+                                tc_mma_bf16_masked(d, sdesc_sw32(sU + kXuBytes), bdesc, idesc, dis);
+                            }
                             tc_commit(smem_u32(&empty[st]));
+                            ++it;
                         }
                     }
                     mbar_arrive(smem_u32(&lempty[as]));
@@ -250,18 +308,22 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __syncthreads();
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, C::kTmemCols);
     }
 }
 
-cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
-                        const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
-    cudaError_t e = ensure_smem_attr((const void*)gemm_wide_kernel, 2, kWdSmem);
+template <int BN, int KK>
+static cudaError_t launch_wide_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
+                                  const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid,
+                                  cudaStream_t stream) {
+    const size_t smem = WideCfg<BN, KK>::kSmem;
+    cudaError_t e = ensure_smem_attr((const void*)gemm_wide_kernel<BN, KK>, (BN == 256 ? 2 : 3) + (KK == 1 ? 0 : 2),
+                                     smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kWdThreads, 1, 1);
-    cfg.dynamicSmemBytes = kWdSmem;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     int na = 0;
@@ -272,7 +334,16 @@ cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CU
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_wide_kernel, tmA, tmB, tmU, tmBs, a);
+    return cudaLaunchKernelEx(&cfg, gemm_wide_kernel<BN, KK>, tmA, tmB, tmU, tmBs, a);
+}
+
+cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
+                        const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
+    if (a.kk == 2)
+        return a.bn == 128 ? launch_wide_bn<128, 2>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream)
+                           : launch_wide_bn<256, 2>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream);
+    return a.bn == 128 ? launch_wide_bn<128, 1>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream)
+                       : launch_wide_bn<256, 1>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream);
 }
 
 cudaError_t wide_take_error(int* code) {

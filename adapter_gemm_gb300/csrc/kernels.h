@@ -11,6 +11,7 @@ constexpr int kTileRows = 16;       // plan work tiles, rows (== LORA_TILE_ROWS)
 constexpr int kMaxSlots = 1024;     // one plan thread per slot in the scans
 constexpr int kMaxRank = 128;       // R_max cap: shrink keeps R_max/8 MMA column tiles
 constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 256)
+constexpr int kSkinnyPathMaxT = 256; // batches up to this many rows take the swap-AB kernel
 constexpr int kStageURank = 64;     // the skinny epilogue stages U rows of rank <= 64
 constexpr int kBySlotMaxT = 64;     // up to this many rows the shrink groups rows by slot itself
 
@@ -85,6 +86,8 @@ struct WideArgs {
     int R_max, R16;
     int T, K, N;
     int m_tiles, n_tiles, kb_total;
+    int bn;                         // output tile width: 256 or 128
+    int kk;                         // 64-column K slices per stage: 1 or 2 (3-D tensor maps)
 };
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream);

@@ -148,4 +148,5 @@ def test_path_choice_depends_on_shape_only(lib):
     assert lib.lora_linear_path(1, 4096, 4096) == 0
     assert lib.lora_linear_path(256, 14336, 4096) == 0
     assert lib.lora_linear_path(257, 4096, 4096) == 1
+    assert lib.lora_linear_path(512, 14336, 4096) == 1
     assert lib.lora_linear_path(4096, 4096, 14336) == 1

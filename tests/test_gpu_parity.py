@@ -159,6 +159,8 @@ RAGGED = [
     (256, 520, 1032, 33, 128),
     (257, 200, 264, 4, 16),
     (300, 1000, 520, 7, 24),
+    (480, 4160, 264, 5, 16),
+    (512, 1024, 392, 12, 32),
     (700, 4104, 1288, 40, 64),
     (1500, 2048, 776, 17, 128),
 ]
