@@ -291,3 +291,73 @@ def test_row_offsets_beyond_int32():
     assert_parity(y[torch.as_tensor(rows, device=DEV)], ref, "int64 offsets")
     del x, y, plan
     torch.cuda.empty_cache()
+
+
+# --------------------------------------------- back-to-back calls, no sync ----
+# The kernels start before the kernel ahead of them has finished and read their
+# inputs early when the host can tell those are not that kernel's output. These
+# tests chain calls on one stream with no synchronisation in between: each
+# step's input is the previous step's output, and the same plan object (its
+# arrays and U) is rebuilt for every step.
+
+def _chained_steps(T, K, S, R, n_steps, base_only=False, seed=3):
+    w = WL.random_case(seed=seed, T=T, K=K, N=K, S=S, R_max=R)
+    t = w.targets[0]
+    W = t.W.to(DEV)
+    pool = L.Pool(S, R, K, K, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    rng = np.random.default_rng(seed + 1)
+    ids_np = [rng.integers(0, S, size=T).astype(np.int32) for _ in range(n_steps)]
+    ids = [torch.from_numpy(v).to(DEV) for v in ids_np]
+    plan = L.Plan(T, S, R, K, device=DEV)
+    xs = [w.x.to(DEV)]
+    torch.cuda.synchronize()
+    for k in range(n_steps):                 # no synchronisation inside the loop
+        if base_only:
+            xs.append(L.linear(xs[-1], W))
+        else:
+            plan.build(ids[k])
+            xs.append(L.linear(xs[-1], W, pool, plan))
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    for k in range(n_steps):
+        x_in = f64(xs[k])
+        step_ids = np.zeros(T, np.int32) if base_only else ids_np[k]
+        ref = O.lora_linear(x_in, f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, step_ids)
+        assert_parity(xs[k + 1], ref, f"step {k}")
+
+
+def test_chained_decode_steps_fused_shrink():
+    _chained_steps(T=64, K=1024, S=9, R=16, n_steps=4)        # (S-1) R = 128: shrink fused in
+
+
+def test_chained_decode_steps_shrink_kernel():
+    _chained_steps(T=48, K=1024, S=20, R=16, n_steps=4)       # shrink kernel ahead of the GEMM
+
+
+def test_chained_decode_steps_base_only():
+    _chained_steps(T=64, K=1024, S=9, R=16, n_steps=4, base_only=True)
+
+
+def test_chained_prefill_steps():
+    _chained_steps(T=300, K=512, S=12, R=16, n_steps=3)       # the wide kernel
+
+
+def test_one_plan_many_targets_without_sync():
+    """Several layers of one step share the plan (and its U), back to back."""
+    T, K, S, R = 64, 512, 20, 16
+    ws = [WL.random_case(seed=40 + i, T=T, K=K, N=K, S=S, R_max=R) for i in range(3)]
+    ids_np = ws[0].ids
+    ids = torch.from_numpy(ids_np.astype(np.int32)).to(DEV)
+    plan = L.Plan(T, S, R, K, device=DEV).build(ids)
+    x = ws[0].x.to(DEV)
+    outs = []
+    for w in ws:
+        t = w.targets[0]
+        pool = L.Pool(S, R, K, K, device=DEV)
+        pool.load_padded(t.A, t.B, t.rank, t.alpha)
+        outs.append((t, L.linear(x, t.W.to(DEV), pool, plan)))
+    torch.cuda.synchronize()
+    for t, y in outs:
+        ref = O.lora_linear(f64(x), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, ids_np)
+        assert_parity(y, ref, "shared plan")
