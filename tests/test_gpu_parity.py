@@ -361,3 +361,33 @@ def test_one_plan_many_targets_without_sync():
     for t, y in outs:
         ref = O.lora_linear(f64(x), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, ids_np)
         assert_parity(y, ref, "shared plan")
+
+
+# ------------------------------------------------ decode path selection ----
+
+def test_fused_shrink_invalid_ids_and_mixed_ranks():
+    """A pool whose adapters' A rows fit one 128-row tile computes U inside the
+    GEMM: ids outside [0, S) give base rows, ranks below R_max (zero padding)
+    and a rank-0 slot add nothing beyond their true rank."""
+    w = WL.random_case(seed=21, T=48, K=512, N=384, S=5, R_max=32, ranks=[0, 8, 32, 17, 0])
+    w.ids[[0, 5, 9]] = [-3, 5, 77]
+    w.ids[[1, 2]] = 4                                    # the rank-0 slot
+    dw = DeviceWorkload(w, DEV)
+    assert dw.plan.check() == 3
+    n0 = L.launch_count()
+    y = dw.run(0)
+    assert L.launch_count() - n0 == 1                    # one kernel: the shrink is fused in
+    assert_parity(y, dw.oracle(0), "fused shrink")
+    yb = dw.run(0, base_only=True)
+    for r in (0, 1, 2, 5, 9):
+        assert torch.equal(y[r].view(torch.int16), yb[r].view(torch.int16))
+
+
+def test_shrink_kernel_when_pool_exceeds_one_tile():
+    """(S - 1) * R_max > 128: U comes from the shrink kernel ahead of the GEMM."""
+    w = WL.random_case(seed=22, T=48, K=512, N=384, S=10, R_max=16)
+    dw = DeviceWorkload(w, DEV)
+    n0 = L.launch_count()
+    y = dw.run(0)
+    assert L.launch_count() - n0 == 2
+    assert_parity(y, dw.oracle(0), "shrink kernel")
