@@ -438,6 +438,57 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     tc_fence_before();
 
     const bool with_ex = a.ex.ids != nullptr;
+    if (a.ks > 1) cluster.sync();      // every push into this CTA has landed
+    else __syncthreads();
+    const int lg = __ffs(rows_per) - 1;               // rows_per = 128 / ks is a power of two
+    if (a.ks > 1) {
+        // the split-K partials of each output, summed in rank order into the
+        // rank-0 slot (each element by one thread)
+        for (int q = threadIdx.x; q < n_tok * rows_per; q += kSkThreads) {
+            const int t = q >> lg, ln = q & (rows_per - 1);
+            float v = red[(size_t)t * rows_per + ln];
+            for (int z = 1; z < a.ks; ++z) v += red[((size_t)z * TN + t) * rows_per + ln];
+            red[(size_t)t * rows_per + ln] = v;
+        }
+    }
+    if (fuse) {
+        // U[t, j] = (alpha / r) * sum over cluster ranks (in rank order) of the
+        // partials, for j below the token's rank rounded up to 8
+        for (int q = threadIdx.x; q < n_tok * R; q += kSkThreads) {
+            const int t = q / R, j = q - t * R;
+            if (gp.tact[t] >= 0 && j < gp.tr8[t]) {
+                float u = upart[(size_t)t * R + j];
+                for (int z = 1; z < a.ks; ++z) u += upart[((size_t)z * TN + t) * R + j];
+                sU[(size_t)t * R + j] = gp.tsc[t] * u;
+            }
+        }
+    }
+    __syncthreads();
+
+    // Work items are (weight row, slot-group piece) pairs: an item loads its
+    // row of B_s once (the next item's is requested while this one is
+    // computed) and finishes every token of the piece:
+    //   y[t, n] = bf16( sum_z partial_z[t, n] + sum_j U[t, j] B[s, n, j] ),
+    // z in rank order, j ascending; slot-0 groups only sum the partials.
+    __nv_bfloat16* __restrict__ yp = a.y;
+    const __nv_bfloat16* __restrict__ Bp = a.ex.B;
+    const bool u_smem = fuse || a.stage_u;
+    auto load_b = [&](int item, uint4 (&b)[8]) {
+        const int g = item >> lg, ln = item & (rows_per - 1);
+        const int r8 = gp.gr8[g];
+        const uint4* brow = reinterpret_cast<const uint4*>(Bp + ((size_t)gp.gslot[g] * a.N + (n_lo + ln)) * R);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            b[c] = (c * 8 < r8 && ln < n_rows) ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
+    };
+    uint4 bc[8], bn[8];
+    // B is a weight: the first item's row is requested before the wait when
+    // the groups are already known
+    bool b_loaded = false;
+    if (a.ids_early && (int)threadIdx.x < (*gp.n_groups << lg)) {
+        load_b(threadIdx.x, bc);
+        b_loaded = true;
+    }
     if (late_u) {
         // U comes from the kernels before this one, and so do the ids when the
         // host could not rule that out: only from here on does the epilogue
@@ -454,44 +505,10 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         __ldg(reinterpret_cast<const float4*>(a.ex.U + (size_t)(t0 + tl) * R) + j4);
             }
         }
-    }
-    if (a.ks > 1) cluster.sync();      // every push into this CTA has landed
-    else __syncthreads();
-    if (fuse) {
-        // U[t, j] = (alpha / r) * sum over cluster ranks (in rank order) of the
-        // partials, for j below the token's rank rounded up to 8
-        for (int q = threadIdx.x; q < n_tok * R; q += kSkThreads) {
-            const int t = q / R, j = q - t * R;
-            if (gp.tact[t] >= 0 && j < gp.tr8[t]) {
-                float u = upart[(size_t)t * R + j];
-                for (int z = 1; z < a.ks; ++z) u += upart[((size_t)z * TN + t) * R + j];
-                sU[(size_t)t * R + j] = gp.tsc[t] * u;
-            }
-        }
         __syncthreads();
     }
-
-    // Work items are (weight row, slot-group piece) pairs: an item loads its
-    // row of B_s once (the next item's is requested while this one is
-    // computed) and finishes every token of the piece:
-    //   y[t, n] = bf16( sum_z partial_z[t, n] + sum_j U[t, j] B[s, n, j] ),
-    // z in rank order, j ascending; slot-0 groups only sum the partials.
-    const int lg = __ffs(rows_per) - 1;               // rows_per = 128 / ks is a power of two
     const int n_items = *gp.n_groups << lg;
-    const int ks = a.ks;
-    __nv_bfloat16* __restrict__ yp = a.y;
-    const __nv_bfloat16* __restrict__ Bp = a.ex.B;
-    const bool u_smem = fuse || a.stage_u;
-    auto load_b = [&](int item, uint4 (&b)[8]) {
-        const int g = item >> lg, ln = item & (rows_per - 1);
-        const int r8 = gp.gr8[g];
-        const uint4* brow = reinterpret_cast<const uint4*>(Bp + ((size_t)gp.gslot[g] * a.N + (n_lo + ln)) * R);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-            b[c] = (c * 8 < r8 && ln < n_rows) ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
-    };
-    uint4 bc[8], bn[8];
-    if ((int)threadIdx.x < n_items) load_b(threadIdx.x, bc);
+    if (!b_loaded && (int)threadIdx.x < n_items) load_b(threadIdx.x, bc);
     for (int item = threadIdx.x; item < n_items; item += kSkThreads) {
         if (item + kSkThreads < n_items) load_b(item + kSkThreads, bn);
         const int g = item >> lg, ln = item & (rows_per - 1);
@@ -504,20 +521,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int p = gp.gbeg[g]; p < pe; p += 2) {
                 const bool two = p + 1 < pe;
                 const int ta = gp.order[p], tb = two ? gp.order[p + 1] : ta;
-                // unconditional loads (rank index clamped), so all of them are
-                // in flight together; ranks past ks are then left out of the sum
-                float pa[8], pb[8];
-#pragma unroll
-                for (int z = 0; z < 8; ++z) {
-                    pa[z] = red[(min(z, ks - 1) * TN + ta) * rows_per + ln];
-                    pb[z] = red[(min(z, ks - 1) * TN + tb) * rows_per + ln];
-                }
-                float va = pa[0], vb = pb[0];
-#pragma unroll
-                for (int z = 1; z < 8; ++z) {
-                    va = (z < ks) ? va + pa[z] : va;
-                    vb = (z < ks) ? vb + pb[z] : vb;
-                }
+                float va = red[ta * rows_per + ln], vb = red[tb * rows_per + ln];   // summed partials
                 if (r8 > 0) {
                     const float* ua = u_smem ? sU + (size_t)ta * R : a.ex.U + (size_t)(t0 + ta) * R;
                     const float* ub = u_smem ? sU + (size_t)tb * R : a.ex.U + (size_t)(t0 + tb) * R;
