@@ -17,11 +17,11 @@ namespace lora {
 // Dynamic shared memory limits already raised, per device and kernel slot.
 cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes) {
     static std::mutex mu;
-    static size_t done[64][4] = {};
+    static size_t done[64][kSmemSlots] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || slot < 0 || slot >= 4)
+    if (dev < 0 || dev >= 64 || slot < 0 || slot >= kSmemSlots)
         return cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev][slot] >= bytes) return cudaSuccess;

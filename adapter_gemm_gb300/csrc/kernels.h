@@ -103,6 +103,9 @@ cudaError_t skinny_take_error(int* code);
 cudaError_t wide_take_error(int* code);
 
 // Raise a kernel's dynamic shared memory limit once per device.
+// One slot per kernel (instantiation) whose dynamic shared memory limit is
+// raised: 0 plan, 1 swap-AB decode, 2..5 wide (tile width x K slices).
+constexpr int kSmemSlots = 8;
 cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
 
 // Shared-memory bytes the skinny kernel needs for a token tile of TN columns
