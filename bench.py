@@ -155,6 +155,27 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The largest of the ranks' times (a whole job ends with its slowest
+    replica); the value itself on a single process. `device` is where the
+    process group's backend keeps tensors (a CUDA device for NCCL, None for
+    gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, steps: int, world: int, ms: float) -> float:
+    """Units all replicas processed per second: every rank runs the same
+    per-GPU workload (weak scaling), and the job takes the slowest rank's
+    time `ms` for `steps` steps."""
+    return units_per_rank * steps * world / (ms / 1e3)
+
+
 # --------------------------------------------------------------- oracle leg --
 
 def oracle_tokens_per_s(w, seconds: float):
@@ -329,13 +350,9 @@ def main():
     if world > 1:
         dist.barrier()
     clocks.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        tmax = torch.tensor([ms], device=dev)
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        ms = float(tmax.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), dev)
     ms_per_step = ms / args.steps
-    value = T * args.steps * world / (ms / 1e3)
+    value = job_throughput(T, args.steps, world, ms)
 
     # ---- dominant kernel: each GEMM launch between a pair of events that the
     # library records on the launch stream right around it. The launches are
@@ -413,50 +430,53 @@ def main():
     # ---- end to end through the public API with host buffers: every step
     # copies x and the ids in from pinned host memory and y back out, captured
     # with the step in the same graphs as above
-    e2e = None
-    if rank == 0 or world > 1:
-        hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
-        hids = torch.from_numpy(w.ids).pin_memory()
-        hy = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
-        dx = {k: torch.empty_like(v) for k, v in xs.items()}
-        dids = torch.empty_like(ids)
-        keys = [id(WL.input_for(w, t)) for t in w.targets]
+    hx = {k: v.cpu().pin_memory() for k, v in xs.items()}
+    hids = torch.from_numpy(w.ids).pin_memory()
+    hy = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
+    dx = {k: torch.empty_like(v) for k, v in xs.items()}
+    dids = torch.empty_like(ids)
+    keys = [id(WL.input_for(w, t)) for t in w.targets]
 
-        def e2e_step(i):
-            c = i % n_copies
-            for k in hx:
-                dx[k].copy_(hx[k], non_blocking=True)
-            dids.copy_(hids, non_blocking=True)
-            plans[c].build(dids)
-            for j, (W, pool) in enumerate(copies[c]):
-                L.linear(dx[keys[j]], W, pool, plans[c], ys[j])
-                hy[j].copy_(ys[j], non_blocking=True)
+    def e2e_step(i):
+        c = i % n_copies
+        for k in hx:
+            dx[k].copy_(hx[k], non_blocking=True)
+        dids.copy_(hids, non_blocking=True)
+        plans[c].build(dids)
+        for j, (W, pool) in enumerate(copies[c]):
+            L.linear(dx[keys[j]], W, pool, plans[c], ys[j])
+            hy[j].copy_(ys[j], non_blocking=True)
 
-        for i in range(3):
-            e2e_step(i)
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    esteps = G * max(1, min(args.steps, 512) // G)
+    if use_graph:
+        ebig = capture(lambda: [e2e_step(i) for i in range(G)])
+        ebig.replay()
         torch.cuda.synchronize()
-        esteps = G * max(1, min(args.steps, 512) // G)
-        if use_graph:
-            ebig = capture(lambda: [e2e_step(i) for i in range(G)])
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    f0.record()
+    if use_graph:
+        for _ in range(esteps // G):
             ebig.replay()
-            torch.cuda.synchronize()
-        f0 = torch.cuda.Event(enable_timing=True)
-        f1 = torch.cuda.Event(enable_timing=True)
-        f0.record()
-        if use_graph:
-            for _ in range(esteps // G):
-                ebig.replay()
-        else:
-            for i in range(esteps):
-                e2e_step(i)
-        f1.record()
-        torch.cuda.synchronize()
-        ems = f0.elapsed_time(f1)
-        bi = sum(v.numel() * v.element_size() for v in hx.values()) + hids.numel() * 4
-        bo = sum(v.numel() * v.element_size() for v in hy)
-        e2e = {"value": round(T * esteps * world / (ems / 1e3), 1), "unit": "tokens/s",
-               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "steps": esteps,
-               "ms_per_step": round(ems / esteps, 6)}
+    else:
+        for i in range(esteps):
+            e2e_step(i)
+    f1.record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ems = max_over_ranks(f0.elapsed_time(f1), dev)
+    bi = sum(v.numel() * v.element_size() for v in hx.values()) + hids.numel() * 4
+    bo = sum(v.numel() * v.element_size() for v in hy)
+    e2e = {"value": round(job_throughput(T, esteps, world, ems), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo), "steps": esteps,
+           "ms_per_step": round(ems / esteps, 6)}
 
     assert L.last_device_error() == 0, "a kernel gave up a bounded wait"
 
