@@ -164,17 +164,26 @@ int max_clusters_cached(int TN, int stages, size_t smem, int ks) {
     return n;
 }
 
-int skinny_stages(int TN, bool fuse, int kk) {
-    int st = (int)(((size_t)192 * 1024) / skinny_stage_bytes(TN, fuse, kk));
+// Shared memory the pipeline may use: 192 KB, less what a tensor-core expand
+// keeps beside it, within the per-CTA limit.
+size_t skinny_pipe_budget(int TN, bool tce) {
+    const size_t fixed = 1024 + 256 + skinny_grp_bytes(TN) + (tce ? skinny_xtab_bytes(TN) : 0);
+    const size_t room = kSkinnyMaxSmem - fixed;
+    return room < (size_t)192 * 1024 ? room : (size_t)192 * 1024;
+}
+
+int skinny_stages(int TN, bool fuse, bool tce, int kk) {
+    int st = (int)(skinny_pipe_budget(TN, tce) / skinny_stage_bytes(TN, fuse, kk));
     return st < 2 ? 2 : (st > 6 ? 6 : st);
 }
 
-// K slices per stage: the most (<= 4) for which two stages fit in 192 KB.
-// The 3-D views that load several slices at once need d_in % 64 == 0.
-int skinny_kk(int TN, bool fuse, int K) {
-    if (K % 64 != 0) return 1;
+// K slices per stage: the most (<= 4) for which two stages fit the budget.
+// The 3-D / 4-D views that load several slices at once need d_in % 64 == 0,
+// and (fused) A slices whose packed rows keep each slice 1024-byte aligned.
+int skinny_kk(int TN, bool fuse, bool tce, int a_rows, int K) {
+    if (K % 64 != 0 || (fuse && a_rows % 8 != 0)) return 1;
     for (int kk = 4; kk > 1; kk /= 2)
-        if (kk <= K / 64 && 2 * skinny_stage_bytes(TN, fuse, kk) <= (size_t)192 * 1024) return kk;
+        if (kk <= K / 64 && 2 * skinny_stage_bytes(TN, fuse, kk) <= skinny_pipe_budget(TN, tce)) return kk;
     return 1;
 }
 
@@ -185,14 +194,16 @@ int skinny_kk(int TN, bool fuse, int K) {
 // GEMM cannot share an SM with it: for decode-sized token tiles the split is
 // the largest (<= 8) whose CTAs fit in half of the SMs, so that consecutive
 // GEMMs stream their weights side by side; wider tiles may use every SM.
-// `mode`: 0 base only, 1 U from the shrink kernel, 2 shrink fused in.
-SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max) {
+// `mode`: 0 base only, 1 U from the shrink kernel (expand on the CUDA cores),
+// 2 shrink fused in, 3 U from the shrink kernel with the expand on the tensor
+// cores.
+SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S) {
     SkinnyConfig c;
     const int Tt = T < kSkinnyMaxT ? T : kSkinnyMaxT;
     c.TN = ((Tt + 15) / 16) * 16;
     if (c.TN < 16) c.TN = 16;
-    const int canon_stages = skinny_stages(c.TN, false, 1);
-    const size_t canon_smem = skinny_smem_bytes(c.TN, canon_stages, 8, false, false, true, 1);
+    const int canon_stages = skinny_stages(c.TN, false, false, 1);
+    const size_t canon_smem = skinny_smem_bytes(c.TN, canon_stages, 8, false, false, false, true, 1);
     const int units = ((N + 127) / 128) * ((T + c.TN - 1) / c.TN);
     const int kb = (K + 63) / 64;
     // Decode-sized token tiles are latency-bound: half the SMs, so that the
@@ -209,12 +220,17 @@ SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max) {
             break;
         }
     }
-    const bool fuse = mode == 2;
-    c.kk = skinny_kk(c.TN, fuse, K);
-    c.stages = skinny_stages(c.TN, fuse, c.kk);
+    const bool fuse = mode == 2, tce = mode >= 2;
+    const int a_rows = fuse ? (S - 1) * R_max : 0;
+    c.kk = skinny_kk(c.TN, fuse, tce, a_rows, K);
+    c.stages = skinny_stages(c.TN, fuse, tce, c.kk);
     c.stage_u = (mode == 1 && R_max <= kStageURank &&
                  skinny_epi_bytes(c.TN, R_max, true, false, false) + 2048 <= (size_t)200 * 1024) ? 1 : 0;
-    c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, mode == 0, c.kk);
+    c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, tce, mode == 0, c.kk);
+    while (c.stages > 2 && c.smem > kSkinnyMaxSmem) {
+        --c.stages;
+        c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, tce, mode == 0, c.kk);
+    }
     return c;
 }
 
@@ -485,15 +501,19 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
               !overlaps(prev, pool->B, (size_t)pool->S * d_out * pool->R_max * 2) &&
               !overlaps(prev, pool->rank, (size_t)pool->S * 4) && !overlaps(prev, pool->scale, (size_t)pool->S * 4);
 
-    // Decode batches of one token tile, with a pool whose adapter slots' A rows
-    // (slots 1..S-1) fit one 128-row tile, compute U inside the GEMM (tensor
-    // cores, that A tile against each K slice of x): no shrink kernel, and
+    // Decode batches of one token tile, with a pool whose adapter slots
+    // (1..S-1, R_max ranks each, rounded up to 16) fit one 128-row tile,
+    // compute U and the expand inside the GEMM (tensor cores: that A tile
+    // against each K slice of x, then Bcat against U): no shrink kernel, and
     // everything but the stores of y comes before the GEMM's wait. The tokens'
     // slots are read during the K loop, so the ids must not come from the
     // kernel ahead.
     const bool ids_early = !plan || !overlaps(prev, plan->ids, (size_t)T * 4);
-    const bool fuse = plan && path == 0 && T <= 64 && ids_early && pool->S >= 2 &&
-                      (pool->S - 1) * pool->R_max <= 128 && ((T + 15) / 16 * 16) * pool->R_max <= 2048;
+    const int r16 = plan ? (pool->R_max + 15) / 16 * 16 : 0;
+    // The expand runs on the tensor cores (Bcat against U) when every adapter
+    // slot's ranks (rounded up to 16) fit 128 pairs; else on the CUDA cores.
+    const bool tc_expand = plan && path == 0 && T <= 64 && pool->S >= 2 && (pool->S - 1) * r16 <= 128;
+    const bool fuse = tc_expand && ids_early;
     if (plan && !fuse) {
         ShrinkArgs sa;
         sa.x = static_cast<const __nv_bfloat16*>(x);
@@ -533,8 +553,8 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
 
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_start, st) != cudaSuccess) return LORA_ECUDA;
     if (path == 0) {
-        const int mode = !plan ? 0 : (fuse ? 2 : 1);
-        const SkinnyConfig c = skinny_config(T, d_in, d_out, mode, plan ? pool->R_max : 8);
+        const int mode = !plan ? 0 : (fuse ? 2 : (tc_expand ? 3 : 1));
+        const SkinnyConfig c = skinny_config(T, d_in, d_out, mode, plan ? pool->R_max : 8, plan ? pool->S : 1);
         CUtensorMap tmW, tmX, tmA;
         const uint64_t ksl = (uint64_t)d_in / 64;           // 64-column slices (kk > 1: d_in % 64 == 0)
         if (c.kk == 1) {
@@ -581,6 +601,8 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.stage_u = c.stage_u;
         a.fuse = fuse ? 1 : 0;
         a.a_rows = fuse ? (pool->S - 1) * pool->R_max : 0;
+        a.a_chunks = tc_expand ? (pool->S - 1) * r16 / 16 : 0;
+        a.tcx = (tc_expand && !fuse) ? 1 : 0;
         a.kk = c.kk;
         a.smem = c.smem;
         a.x_early = x_early ? 1 : 0;

@@ -14,15 +14,28 @@
 // TMEM and pushes each owner's rows into that owner's shared memory
 // (distributed shared memory stores, one slot per sender); the owner then sums
 // the ks partials in rank order (a fixed order, so results do not depend on
-// timing), adds the row's low-rank
-// correction (the expand half of SGMV: U[t, :r] . B[s, n, :r], fp32, j
-// ascending) unless the token is on slot 0 or a rank-0 slot, rounds to bf16
-// and writes y once. No fp32 atomics, no extra pass over y.
+// timing), rounds to bf16 and writes y once. No fp32 atomics, no extra pass
+// over y.
+//
+// The low-rank correction (SGMV's expand) is added in one of two ways:
+//  - shrink fused in (one token tile, every adapter's A rows in one 128-row
+//    tile): each CTA computes its K slice's share of U for every slot on the
+//    tensor cores (the A tile against the same x slices), and adds that
+//    share's expand to its own partial tile with more MMAs before the push:
+//        partial[n, t] += sum_k Bcat[n, k] Ucat[t, k],
+//    k running over (slot, rank) pairs, Bcat[n, (s, j)] = B[s, n, j] and
+//    Ucat[t, (s, j)] = (alpha_s / r_s) U_part[t, j] when s is the token's slot
+//    and j < r_s, else 0. U_part is split into bf16 high and low halves, two
+//    MMAs per 16 pairs. The expand is linear in U, so the owner's sum over
+//    ranks is the full correction;
+//  - U from the shrink kernel ahead: the owner adds U[t, :r] . B[s, n, :r]
+//    (fp32, j ascending) to the summed partials on the CUDA cores.
+// Tokens on slot 0, on a rank-0 slot or with an invalid id get no correction.
 //
 // Roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warp 1 owns the
-// TMEM allocation; warps 2..7 group the tile's tokens by slot during the K
-// loop; all eight warps drain the accumulator (warp w reads TMEM lanes
-// 32 (w % 4).. and half of the token columns) and do the reduction and expand.
+// TMEM allocation; warps 2..7 read the tokens' slots (and, fused, stage Bcat)
+// during the K loop; all eight warps drain the accumulator (warp w reads TMEM
+// lanes 32 (w % 4).. and half of the token columns) and do the reduction.
 #include <cstdint>
 #include <cooperative_groups.h>
 #include "ptx.cuh"
@@ -37,37 +50,58 @@ constexpr int kBK = 64;                     // K elements per stage (128 bytes o
 constexpr int kWRows = 128;                 // weight rows per tile (MMA M)
 constexpr int kWTileBytes = kWRows * kBK * 2;
 constexpr int kMaxAct = kWRows / 8;        // adapter slots of an A tile (R_max >= 8 rows each)
+constexpr int kMaxChunks = 8;              // tensor-core expand: (slot, rank) pairs in 16-wide chunks, <= 128 pairs
+constexpr int kChunkRowBytes = 32;         // one row of a 16-wide bf16 chunk (32-byte swizzle)
+constexpr int kBcatBytes = kMaxChunks * kWRows * kChunkRowBytes;
+constexpr int kMaxASlots = 8;              // adapter slots of the expand (R16 >= 16 pairs each)
+
+// Tensor-core expand: Bcat, then the token tables: msc[a][t] (alpha / r where
+// token t is on slot a + 1, else 0), each token's slot - 1 (or -1) and the
+// slots' ranks.
+__host__ __device__ size_t skinny_xtab_bytes(int TN) {
+    return (size_t)kBcatBytes + ((size_t)kMaxASlots * TN + TN + kMaxASlots) * 4;
+}
 
 // The tile's tokens grouped by slot (kept apart from the pipeline's buffers,
-// since it is built during the K loop), and the A tile's slot list.
+// since it is built during the K loop).
 __host__ __device__ size_t skinny_grp_bytes(int TN) { return ((size_t)8 * TN + kMaxAct + 8) * 4; }
 
 // Epilogue scratch after the K loop, in the pipeline's buffers: the received
 // partials [ks][TN][128/ks] (128 x TN floats), then per mode
-//   late U (shrink kernel ahead):  U rows [TN][R_max] when staged;
-//   fused shrink:  U [TN][R_max], U partials [ks <= 8][TN][R_max], y staging;
-//   base only:     y staging [TN][<= 128] bf16.
-__host__ __device__ size_t skinny_epi_bytes(int TN, int R_max, bool stage_u, bool fuse, bool base_only) {
+//   late U on the CUDA cores:  U rows [TN][R_max] when staged;
+//   tensor-core expand:        Ucat high and low halves [chunk][2][TN][16] bf16, y staging;
+//   base only:                 y staging [TN][<= 128] bf16.
+__host__ __device__ size_t skinny_epi_bytes(int TN, int R_max, bool stage_u, bool tc_expand, bool base_only) {
     const size_t red = (size_t)kWRows * TN * 4;
     const size_t ystage = (size_t)TN * kWRows * 2;
-    if (fuse) return red + (size_t)9 * TN * R_max * 4 + ystage;
+    if (tc_expand) return red + (size_t)kMaxChunks * 2 * TN * kChunkRowBytes + ystage;
     if (base_only) return red + ystage;
     return red + (stage_u ? (size_t)TN * R_max * 4 : 0);
 }
 
 // One pipeline stage holds `kk` consecutive 64-column K slices of the weight
-// tile, of x and (fused) of the A tile, each slice in its own 128-byte
-// swizzled block.
+// tile, of x and (shrink fused in) of the A tile, each slice in its own
+// 128-byte swizzled block.
 __host__ __device__ size_t skinny_stage_bytes(int TN, bool fuse, int kk) {
     return (size_t)kk * ((size_t)kWTileBytes + (size_t)TN * kBK * 2 + (fuse ? (size_t)kWTileBytes : 0));
 }
 
-__host__ __device__ size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u, bool fuse, bool base_only,
-                                             int kk) {
+// With a tensor-core expand, Bcat and the token tables sit after the pipeline /
+// epilogue region, since they are staged during the K loop.
+__host__ __device__ size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u, bool fuse, bool tc_expand,
+                                             bool base_only, int kk) {
     const size_t pipe = skinny_stage_bytes(TN, fuse, kk) * stages;
-    const size_t epi = skinny_epi_bytes(TN, R_max, stage_u, fuse, base_only);
+    const size_t epi = skinny_epi_bytes(TN, R_max, stage_u, tc_expand, base_only);
     const size_t body = pipe > epi ? pipe : epi;
-    return 1024 /*alignment slack*/ + body + 256 /*barriers*/ + skinny_grp_bytes(TN);
+    return 1024 /*alignment slack*/ + body + (tc_expand ? skinny_xtab_bytes(TN) : 0) + 256 /*barriers*/ +
+           skinny_grp_bytes(TN);
+}
+
+// Byte offset of element j (< 16) of row r in a 16-wide bf16 chunk stored with
+// the 32-byte swizzle (the 16-byte halves of a row swap on every fourth row
+// pair), the layout the MMA's shared-memory descriptor describes.
+__device__ __forceinline__ uint32_t sw32_offset(int r, int j) {
+    return (uint32_t)r * kChunkRowBytes + ((uint32_t)(((j >> 3) ^ (r >> 2)) & 1) << 4) + (uint32_t)(j & 7) * 2u;
 }
 
 // d + u[0..7] . b[0..7] (b = 8 packed bf16), j ascending.
@@ -101,9 +135,6 @@ struct TileGroups {
     int* gr8;     // [TN] rank of each group, rounded up to 8
     int* gbeg;    // [TN + 1] first position of each group in `order`, then n_tok
     int* n_groups;
-    // with the shrink fused in:
-    int* tact;    // [TN] the token's slot - 1 (its A-tile rows start at tact * R_max), or -1
-    float* tsc;   // [TN] alpha / r of the token's slot
 };
 
 
@@ -114,9 +145,7 @@ __device__ __forceinline__ void grp_barrier(int nthr) {
 // Group the tile's tokens by adapter slot, with the `nthr` threads (whole
 // warps) numbered i0 = 0.. that run it, and send this CTA's rows of B for
 // every group to L2. Invalid ids, slot 0 and rank-0 slots all map to slot 0:
-// those tokens get the base output only. Reads the ids, the pool's ranks and
-// scales, and B. With the shrink fused in, also notes each token's rows of the
-// A tile and its slot's alpha / r.
+// those tokens get the base output only. Reads the ids, the pool's ranks and B.
 __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, int n_tok, int i0, int nthr,
                              int n_lo, int n_rows, int n_rows_per) {
     const bool with_ex = a.ex.ids != nullptr;
@@ -179,13 +208,6 @@ __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, 
             *gp.n_groups = G;
         }
     }
-    if (a.fuse) {                      // the A tile holds slots 1..S-1 in order
-        for (int t = i0; t < n_tok; t += nthr) {
-            const int s = gp.tslot[t];
-            gp.tact[t] = s - 1;
-            gp.tsc[t] = s > 0 ? a.ex.scale[s] : 0.f;
-        }
-    }
     grp_barrier(nthr);
     if (with_ex && n_rows > 0) {       // rows [n_lo, n_lo + n_rows) of B_s are contiguous
         const int G = *gp.n_groups;
@@ -194,6 +216,73 @@ __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, 
                 prefetch_l2_bulk(a.ex.B + ((size_t)gp.gslot[g] * a.N + n_lo) * a.ex.R_max,
                                  (uint32_t)n_rows * (uint32_t)a.ex.R_max * 2u);
     }
+}
+
+// Tensor-core expand tables, run by the `nthr` threads numbered i0 = 0..:
+// msc[a][t] = alpha / r of slot a + 1 when token t is on that slot (a valid id
+// of a slot of nonzero rank), else 0; tact[t] = that a, or -1; srank[a] = the
+// rank of slot a + 1. Reads the ids and the pool's ranks and scales.
+__device__ void expand_tables(const SkinnyArgs& a, float* msc, int* tact, int* srank, int t0, int n_tok, int i0,
+                              int nthr) {
+    const int TN = a.TN, n_act = a.ex.S - 1;
+    for (int t = i0; t < TN; t += nthr) {
+        int act = -1;
+        float sc = 0.f;
+        if (t < n_tok) {
+            const int id = a.ex.ids[t0 + t];
+            if (id >= 1 && id < a.ex.S && a.ex.rank[id] > 0) {
+                act = id - 1;
+                sc = a.ex.scale[id];
+            }
+        }
+        tact[t] = act;
+        for (int ai = 0; ai < n_act; ++ai) msc[ai * TN + t] = (act == ai) ? sc : 0.f;
+    }
+    for (int ai = i0; ai < n_act; ai += nthr) srank[ai] = min(a.ex.rank[ai + 1], a.ex.R_max);
+}
+
+// This tile's Bcat in shared memory, by the `nthr` threads numbered i0 = 0..:
+// chunk c = a * cps + h (cps = R16 / 16 chunks per slot) holds
+// B[a + 1, n0 + n, 16 h + 0..15] for the tile's 128 weight rows n, zero past
+// R_max and past d_out. Reads only B (a weight), so it may run before the wait.
+// Each thread has four 16-byte loads in flight at a time.
+__device__ void stage_bcat(const SkinnyArgs& a, uint8_t* bcat, int n0, int i0, int nthr) {
+    const int R = a.ex.R_max, cps = (R + 15) >> 4;
+    const int n_items = a.a_chunks * kWRows * 2;      // (chunk, row, 16-byte half)
+    const __nv_bfloat16* __restrict__ Bp = a.ex.B;
+    auto fetch = [&](int e) -> uint4 {
+        const int h = e & 1, n = (e >> 1) & (kWRows - 1), c = e >> 8;
+        const int ai = c / cps, j0 = (c - ai * cps) * 16 + h * 8;
+        const int row = n0 + n;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (e < n_items && row < a.N && j0 < R) {
+            const __nv_bfloat16* src = Bp + ((size_t)(ai + 1) * a.N + row) * R + j0;
+            if ((R & 7) == 0) {
+                v = __ldg(reinterpret_cast<const uint4*>(src));
+            } else {
+                uint16_t q[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    q[i] = (j0 + i < R) ? __ldg(reinterpret_cast<const unsigned short*>(src) + i) : (uint16_t)0;
+                v = make_uint4(q[0] | ((uint32_t)q[1] << 16), q[2] | ((uint32_t)q[3] << 16),
+                               q[4] | ((uint32_t)q[5] << 16), q[6] | ((uint32_t)q[7] << 16));
+            }
+        }
+        return v;
+    };
+    auto put = [&](int e, uint4 v) {
+        if (e >= n_items) return;
+        const int h = e & 1, n = (e >> 1) & (kWRows - 1), c = e >> 8;
+        *reinterpret_cast<uint4*>(bcat + (size_t)c * kWRows * kChunkRowBytes + sw32_offset(n, h * 8)) = v;
+    };
+    for (int e = i0; e < n_items; e += 4 * nthr) {
+        const uint4 v0 = fetch(e), v1 = fetch(e + nthr), v2 = fetch(e + 2 * nthr), v3 = fetch(e + 3 * nthr);
+        put(e, v0);
+        put(e + nthr, v1);
+        put(e + 2 * nthr, v2);
+        put(e + 3 * nthr, v3);
+    }
+    fence_proxy_async_smem();          // read by the expand MMAs after the K loop
 }
 
 __global__ void __launch_bounds__(kSkThreads, 1)
@@ -205,8 +294,11 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int TN = a.TN;
     const int stages = a.stages;
-    const bool fuse = a.fuse != 0;
+    const bool fuse = a.fuse != 0;                // U computed here
+    const bool tcx = a.tcx != 0;                  // U from the kernel ahead, expand on the tensor cores
+    const bool tce = fuse || tcx;                 // tensor-core expand
     const int R = a.ex.R_max;
+    const int R16 = (R + 15) & ~15;
     const int KK = a.kk;                                          // K slices per stage
     const uint32_t x_tile_bytes = (uint32_t)TN * kBK * 2;
     const uint32_t w_off = 0, x_off = (uint32_t)KK * kWTileBytes;  // within a stage
@@ -214,22 +306,27 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const uint32_t a_slice = (uint32_t)a.a_rows * kBK * 2;        // one slice of the A tile
     const uint32_t stage_bytes = (uint32_t)skinny_stage_bytes(TN, fuse, KK);
     const size_t pipe = (size_t)stage_bytes * stages;
-    const size_t epi_bytes = skinny_epi_bytes(TN, R, a.stage_u != 0, fuse, a.ex.ids == nullptr);
-    uint8_t* tail = base + (pipe > epi_bytes ? pipe : epi_bytes);
+    const size_t epi_bytes = skinny_epi_bytes(TN, R, a.stage_u != 0, tce, a.ex.ids == nullptr);
+    uint8_t* bcat = base + (pipe > epi_bytes ? pipe : epi_bytes); // tensor-core expand: [chunk][128][16] bf16
+    float* msc = reinterpret_cast<float*>(bcat + kBcatBytes);    // [S - 1][TN]
+    int* tact = reinterpret_cast<int*>(msc + kMaxASlots * TN);    // [TN]
+    int* srank = tact + TN;                                       // [S - 1]
+    uint8_t* tail = bcat + (tce ? skinny_xtab_bytes(TN) : 0);
     uint64_t* full = reinterpret_cast<uint64_t*>(tail);          // [stages]
     uint64_t* empty = full + stages;                              // [stages]
-    uint64_t* accf = empty + stages;                              // [1]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+    uint64_t* accf = empty + stages;                              // [1] K loop done
+    uint64_t* accx = accf + 1;                                    // [1] expand MMAs done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accx + 1);
     // After the K loop, in the pipeline's buffers: the received partials of
     // the weight rows this CTA finishes, [ks][TN][rows_per] floats, then
-    //  - late U (the shrink ran as its own kernel): the tile's U rows [TN][R];
-    //  - fused shrink: every CTA's partial U of each token's own slot
-    //    [ks][TN][R], the reduced and scaled U [TN][R], and y [TN][rows_per]
-    //    in bf16, stored after the wait; without a plan only the latter.
+    //  - late U on the CUDA cores: the tile's U rows [TN][R] when staged;
+    //  - tensor-core expand: Ucat [chunk][high, low][TN][16] bf16, then y
+    //    [TN][rows_per] bf16, stored after the wait; without a plan only y.
     float* red = reinterpret_cast<float*>(base);
     float* sU = red + (size_t)kWRows * TN;
-    float* upart = sU + (fuse ? (size_t)TN * R : 0);              // fused: [ks][TN][R]
-    __nv_bfloat16* ystage = reinterpret_cast<__nv_bfloat16*>(upart + (fuse ? (size_t)a.ks * TN * R : 0));
+    uint8_t* ucat = reinterpret_cast<uint8_t*>(sU);
+    __nv_bfloat16* ystage = reinterpret_cast<__nv_bfloat16*>(
+        ucat + (tce ? (size_t)kMaxChunks * 2 * TN * kChunkRowBytes : 0));
     int* gmem = reinterpret_cast<int*>(tail + 256);
     const TileGroups gp{gmem,
                         gmem + TN,
@@ -237,9 +334,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                         gmem + 3 * TN,
                         gmem + 4 * TN,
                         gmem + 5 * TN,
-                        gmem + 6 * TN + 1,
-                        gmem + 6 * TN + 2,
-                        reinterpret_cast<float*>(gmem + 7 * TN + 2)};
+                        gmem + 6 * TN + 1};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x;
@@ -256,9 +351,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     const int n_tok = min(TN, a.T - t0);
     const uint32_t acc_cols = (uint32_t)TN * (fuse ? 2u : 1u);   // weight accumulator, then U's
     const uint32_t tmem_cols = acc_cols <= 32 ? 32u : (acc_cols <= 64 ? 64u : (acc_cols <= 128 ? 128u : 256u));
-    // The epilogue stores y only after the wait, from shared memory, unless U
-    // comes from the shrink kernel ahead of this one.
-    const bool late_u = a.ex.ids != nullptr && !fuse;
+    // Expand on the CUDA cores, after U from the kernel ahead: y is stored
+    // straight from the items.
+    const bool late_u = a.ex.ids != nullptr && !tce;
+    // The CTA that adds the expand to its partial tile: every one when it
+    // holds its own share of U (fused), else rank 0, which holds all of U.
+    const bool adds_x = fuse || (tcx && kz == 0);
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmW);
@@ -269,6 +367,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             mbar_init(smem_u32(&empty[i]), 1);
         }
         mbar_init(smem_u32(accf), 1);
+        mbar_init(smem_u32(accx), 1);
         fence_mbar_init();
     }
     if (warp == 1) {
@@ -284,6 +383,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     pdl_trigger();
 
     bool ok = true;
+    const int nst = (nkb + KK - 1) / KK;                          // stages of this CTA's K range
     if (warp == 0 && lane == 0) {
         // TMA producer, one copy per operand per stage (a stage is KK slices of
         // 64 columns: a TMA copy has a fixed cost, so fewer, larger copies
@@ -293,7 +393,6 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // writes it. With the shrink fused in, each stage also holds the A rows
         // of every adapter slot of the pool (slots 1..S-1, R_max rows each) for
         // the same slices: the A tile.
-        const int nst = (nkb + KK - 1) / KK;                      // stages of this CTA's K range
         const int pre = min(nst, stages);
         const uint32_t tx = (uint32_t)KK * (kWTileBytes + x_tile_bytes + (fuse ? a_slice : 0u));
         // slice index of stage i: kb_lo + i KK (with kk > 1 the tensor maps
@@ -344,7 +443,6 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // tile into [TN, 2 TN), both against the same x tile. A stage's slices
         // past this CTA's K range (loaded with the last stage) are skipped.
         const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)TN);
-        const int nst = (nkb + KK - 1) / KK;
         for (int i = 0; i < nst && ok; ++i) {
             const int st = i % stages;
             const uint32_t ph = (uint32_t)(i / stages) & 1u;
@@ -372,25 +470,146 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             tc_commit(smem_u32(&empty[st]));
         }
         tc_commit(smem_u32(accf));     // fires once every MMA above has completed
-    } else if (warp >= 2 && a.ids_early) {
+    } else if (warp >= 2 && tce) {
+        // Idle during the K loop: Bcat, and the token tables when the ids may
+        // be read before the wait.
+        stage_bcat(a, bcat, n0, (int)threadIdx.x - 64, kSkThreads - 64);
+        if (a.ids_early) expand_tables(a, msc, tact, srank, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64);
+    } else if (warp >= 2 && late_u && a.ids_early) {
         // Idle during the K loop: group the tokens and fetch B's rows to L2.
         group_tokens(a, gp, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64, n_lo, n_rows, rows_per);
     }
     __syncwarp();
-    // Split-K reduction. CTA rank c owns weight rows [c*rows_per, (c+1)*rows_per)
-    // of the tile. Once every CTA of the cluster is past its K loop, each one
-    // pushes its partial rows straight from TMEM into the owner's shared memory
-    // (recv[src rank][token][row], plain stores into the peer), then each owner
-    // sums what it received in rank order: a fixed order, and no remote loads.
-    const int row = (warp & 3) * 32 + lane;         // the accumulator row (weight row) this thread moves
+    const int row = (warp & 3) * 32 + lane;         // the accumulator row (TMEM lane) this thread reads
     // One thread waits for the K loop (sleeping between tries); the others
     // park on the block barrier and take no issue slots meanwhile.
     int got = 1;
     if (threadIdx.x == 0 && nkb > 0) got = mbar_wait_sleep(smem_u32(accf), 0, kErrAccWait) ? 1 : 0;
-    const bool have = nkb > 0 && __syncthreads_and(got);   // also: this CTA's stage buffers are free
+    bool have = nkb > 0 && __syncthreads_and(got);   // also: this CTA's stage buffers are free
     tc_fence_after();
     cg::cluster_group cluster = cg::this_cluster();
-    if (a.ks > 1) cluster.sync();      // ... and every peer's
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    if (tce) {
+        // This CTA's stage buffers are free for its peers' pushes (their last
+        // users, the TMA copies and the MMAs, have completed); the wait for
+        // the peers' comes after the expand.
+        if (a.ks > 1) cluster_arrive_relaxed();
+        // Ucat: only a token on slot a + 1 (ranks below its rank) has values,
+        // at the positions of that slot; every other entry, the pad positions
+        // R..R16 - 1 of a slot and the columns past the tile's tokens stay 0.
+        // So the chunks are zeroed first (16-byte stores).
+        if (adds_x) {
+            uint4* z = reinterpret_cast<uint4*>(ucat);
+            const int n16 = a.a_chunks * 2 * TN * kChunkRowBytes / 16;
+            for (int q = threadIdx.x; q < n16; q += kSkThreads) z[q] = make_uint4(0, 0, 0, 0);
+        }
+        if (tcx) {
+            // U (and, when the host could not rule out that the kernel ahead
+            // writes them, the ids) come from the kernels before this one.
+            pdl_wait();
+            if (!a.ids_early) expand_tables(a, msc, tact, srank, t0, n_tok, (int)threadIdx.x, kSkThreads);
+        }
+        __syncthreads();
+        const size_t lo_off = (size_t)TN * kChunkRowBytes;
+        if (fuse) {
+            // From this CTA's share of U: TMEM row `row` of the U accumulator is
+            // rank j of A-tile slot ai (row = ai R + j), pair (ai, j) of the
+            // expand at position R16 ai + j of Ucat's rows; a token on slot
+            // ai + 1 with rank > j gets (alpha / r) U there.
+            const int ai = row / R, j = row - ai * R;
+            const bool jv = row < a.a_rows && j < srank[row < a.a_rows ? ai : 0];
+            const int pos = ai * R16 + j;
+            uint8_t* uhi = ucat + (size_t)(pos >> 4) * 2 * TN * kChunkRowBytes;
+            for (int c = 16 * (warp >> 2); c < TN; c += 32) {
+                float v[16];
+                if (have) {
+                    tc_ld16(tmem + lane_base + (uint32_t)(TN + c), v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                }
+                if (jv) {
+                    float m[16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 m4 = *reinterpret_cast<const float4*>(msc + (size_t)ai * TN + c + 4 * q);
+                        m[4 * q] = m4.x;
+                        m[4 * q + 1] = m4.y;
+                        m[4 * q + 2] = m4.z;
+                        m[4 * q + 3] = m4.w;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (m[i] != 0.f) {
+                            const float u = m[i] * v[i];
+                            const __nv_bfloat16 h = __float2bfloat16_rn(u);
+                            const __nv_bfloat16 l = __float2bfloat16_rn(u - __bfloat162float(h));
+                            const uint32_t o = sw32_offset(c + i, pos & 15);
+                            *reinterpret_cast<__nv_bfloat16*>(uhi + o) = h;
+                            *reinterpret_cast<__nv_bfloat16*>(uhi + lo_off + o) = l;
+                        }
+                    }
+                }
+            }
+        } else if (adds_x) {
+            // From U of the kernel ahead ([T][R_max] fp32, alpha / r applied),
+            // eight ranks of one token per item.
+            const int g8 = R16 >> 3;
+            for (int q = threadIdx.x; q < n_tok * g8; q += kSkThreads) {
+                const int t = q / g8, j0 = (q - t * g8) * 8;
+                const int act = tact[t];
+                if (act < 0) continue;
+                const int rk = srank[act];
+                if (j0 >= rk) continue;
+                const float* up = a.ex.U + (size_t)(t0 + t) * R + j0;
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float x0 = (j0 + e < rk) ? up[e] : 0.f;
+                    const float x1 = (j0 + e + 1 < rk) ? up[e + 1] : 0.f;
+                    const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                    const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                    hi[e >> 1] = pack_bf16x2(x0, x1);
+                    lo[e >> 1] = pack_bf16x2(x0 - h0, x1 - h1);
+                }
+                uint8_t* dst = ucat + (size_t)(act * (R16 >> 4) + (j0 >> 4)) * 2 * TN * kChunkRowBytes +
+                               sw32_offset(t, j0 & 15);
+                *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                *reinterpret_cast<uint4*>(dst + lo_off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            }
+        }
+        if (adds_x) {
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (warp == 1 && lane == 0 && have) {
+                // partial[n, t] += sum over pairs of Bcat[n, k] (Ucat_high + Ucat_low)[t, k]
+                const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)TN);
+                const uint32_t sb = smem_u32(bcat), su = smem_u32(ucat);
+                for (int c = 0; c < a.a_chunks; ++c) {
+                    const uint64_t da = sdesc_sw32(sb + (uint32_t)(c * kWRows * kChunkRowBytes));
+                    const uint32_t uc = su + (uint32_t)(c * 2 * TN * kChunkRowBytes);
+                    tc_mma_bf16(tmem, da, sdesc_sw32(uc), idesc, 1u);
+                    tc_mma_bf16(tmem, da, sdesc_sw32(uc + (uint32_t)(TN * kChunkRowBytes)), idesc, 1u);
+                }
+                tc_commit(smem_u32(accx));
+            }
+            got = 1;
+            if (threadIdx.x == 0 && have) got = mbar_wait(smem_u32(accx), 0, kErrAccWait) ? 1 : 0;
+            have = __syncthreads_and(got) && have;
+            tc_fence_after();
+        }
+        __syncwarp();
+        if (a.ks > 1) cluster_wait_acquire();    // every peer's buffers are free
+    } else if (a.ks > 1) {
+        cluster.sync();                // every peer's stage buffers are free
+    }
+    // Split-K reduction. CTA rank c owns weight rows [c*rows_per, (c+1)*rows_per)
+    // of the tile. Each CTA pushes its partial rows straight from TMEM into the
+    // owner's shared memory (recv[src rank][token][row], plain stores into the
+    // peer), then each owner sums what it received in rank order: a fixed
+    // order, and no remote loads.
     const uint32_t recv = smem_u32(red);
     {
         // warp w reads TMEM lanes 32 (w % 4) .. (the lanes its quadrant may
@@ -400,7 +619,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         for (int c = 16 * (warp >> 2); c < TN; c += 32) {
             float v[16];
             if (have) {
-                tc_ld16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)c, v);
+                tc_ld16(tmem + lane_base + (uint32_t)c, v);
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) v[i] = 0.f;
@@ -409,90 +628,81 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             for (int i = 0; i < 16; ++i)
                 st_cluster_f32(dst0 + (uint32_t)((((kz * TN) + c + i) * rows_per + ln) * 4), v[i]);
         }
-        if (fuse) {
-            // U: row `row` of the A tile is rank j of adapter slot ai + 1 (row =
-            // ai R + j). Token t needs it when t is on that slot; its partial
-            // goes to upart[kz][t][j] of every CTA of the cluster.
-            const int ai = row / R, j = row - ai * R;
-            const uint32_t up = smem_u32(upart);
-            for (int c = 16 * (warp >> 2); c < TN; c += 32) {
-                float v[16];
-                if (have) {
-                    tc_ld16(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(TN + c), v);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = c + i;
-                    if (t < n_tok && gp.tact[t] == ai) {
-                        const uint32_t off = (uint32_t)((((kz * TN) + t) * R + j) * 4);
-                        for (int q = 0; q < a.ks; ++q)
-                            st_cluster_f32((a.ks > 1 ? mapa_shared(up, (uint32_t)q) : up) + off, v[i]);
-                    }
-                }
-            }
-        }
     }
     tc_fence_before();
 
     const bool with_ex = a.ex.ids != nullptr;
     if (a.ks > 1) cluster.sync();      // every push into this CTA has landed
     else __syncthreads();
-    const int lg = __ffs(rows_per) - 1;               // rows_per = 128 / ks is a power of two
-    if (a.ks > 1) {
-        // the split-K partials of each output, summed in rank order into the
-        // rank-0 slot (each element by one thread)
-        for (int q = threadIdx.x; q < n_tok * rows_per; q += kSkThreads) {
-            const int t = q >> lg, ln = q & (rows_per - 1);
-            float v = red[(size_t)t * rows_per + ln];
-            for (int z = 1; z < a.ks; ++z) v += red[((size_t)z * TN + t) * rows_per + ln];
-            red[(size_t)t * rows_per + ln] = v;
+    __nv_bfloat16* __restrict__ yp = a.y;
+    if (!late_u) {
+        // y = bf16(sum of the partials in rank order), eight weight rows of one
+        // token per item, staged for 16-byte stores after the wait: everything
+        // up to here needed only this kernel's inputs, but y may still be read
+        // or written by the kernels ahead of this one.
+        const int g8 = rows_per >> 3;
+        for (int q = threadIdx.x; q < n_tok * g8; q += kSkThreads) {
+            const int t = q / g8, ln = (q - t * g8) * 8;
+            const float4* p0 = reinterpret_cast<const float4*>(red + (size_t)t * rows_per + ln);
+            float4 s0 = p0[0], s1 = p0[1];
+            for (int z = 1; z < a.ks; ++z) {
+                const float4* pz = reinterpret_cast<const float4*>(red + ((size_t)z * TN + t) * rows_per + ln);
+                const float4 u0 = pz[0], u1 = pz[1];
+                s0.x += u0.x; s0.y += u0.y; s0.z += u0.z; s0.w += u0.w;
+                s1.x += u1.x; s1.y += u1.y; s1.z += u1.z; s1.w += u1.w;
+            }
+            *reinterpret_cast<uint4*>(ystage + (size_t)t * rows_per + ln) =
+                make_uint4(pack_bf16x2(s0.x, s0.y), pack_bf16x2(s0.z, s0.w), pack_bf16x2(s1.x, s1.y),
+                           pack_bf16x2(s1.z, s1.w));
         }
-    }
-    if (fuse) {
-        // U[t, j] = (alpha / r) * sum over cluster ranks (in rank order) of the
-        // partials, for j below the token's rank rounded up to 8
-        for (int q = threadIdx.x; q < n_tok * R; q += kSkThreads) {
-            const int t = q / R, j = q - t * R;
-            if (gp.tact[t] >= 0 && j < gp.tr8[t]) {
-                float u = upart[(size_t)t * R + j];
-                for (int z = 1; z < a.ks; ++z) u += upart[((size_t)z * TN + t) * R + j];
-                sU[(size_t)t * R + j] = gp.tsc[t] * u;
+        __syncthreads();
+        pdl_wait();
+        const int v8 = n_rows >> 3;                   // n_rows is a multiple of 8
+        for (int q = threadIdx.x; q < n_tok * v8; q += kSkThreads) {
+            const int t = q / v8, c = q - t * v8;
+            *reinterpret_cast<uint4*>(yp + (size_t)(t0 + t) * a.N + n_lo + c * 8) =
+                *reinterpret_cast<const uint4*>(ystage + (size_t)t * rows_per + c * 8);
+        }
+    } else {
+        const int lg = __ffs(rows_per) - 1;           // rows_per = 128 / ks is a power of two
+        if (a.ks > 1) {
+            // the split-K partials of each output, summed in rank order into
+            // the rank-0 slot (each element by one thread)
+            for (int q = threadIdx.x; q < n_tok * rows_per; q += kSkThreads) {
+                const int t = q >> lg, ln = q & (rows_per - 1);
+                float v = red[(size_t)t * rows_per + ln];
+                for (int z = 1; z < a.ks; ++z) v += red[((size_t)z * TN + t) * rows_per + ln];
+                red[(size_t)t * rows_per + ln] = v;
             }
         }
-    }
-    __syncthreads();
+        __syncthreads();
 
-    // Work items are (weight row, slot-group piece) pairs: an item loads its
-    // row of B_s once (the next item's is requested while this one is
-    // computed) and finishes every token of the piece:
-    //   y[t, n] = bf16( sum_z partial_z[t, n] + sum_j U[t, j] B[s, n, j] ),
-    // z in rank order, j ascending; slot-0 groups only sum the partials.
-    __nv_bfloat16* __restrict__ yp = a.y;
-    const __nv_bfloat16* __restrict__ Bp = a.ex.B;
-    const bool u_smem = fuse || a.stage_u;
-    auto load_b = [&](int item, uint4 (&b)[8]) {
-        const int g = item >> lg, ln = item & (rows_per - 1);
-        const int r8 = gp.gr8[g];
-        const uint4* brow = reinterpret_cast<const uint4*>(Bp + ((size_t)gp.gslot[g] * a.N + (n_lo + ln)) * R);
+        // Work items are (weight row, slot-group piece) pairs: an item loads
+        // its row of B_s once (the next item's is requested while this one is
+        // computed) and finishes every token of the piece:
+        //   y[t, n] = bf16( sum_z partial_z[t, n] + sum_j U[t, j] B[s, n, j] ),
+        // z in rank order, j ascending; slot-0 groups only sum the partials.
+        const __nv_bfloat16* __restrict__ Bp = a.ex.B;
+        const bool u_smem = a.stage_u != 0;
+        auto load_b = [&](int item, uint4 (&b)[8]) {
+            const int g = item >> lg, ln = item & (rows_per - 1);
+            const int r8 = gp.gr8[g];
+            const uint4* brow = reinterpret_cast<const uint4*>(Bp + ((size_t)gp.gslot[g] * a.N + (n_lo + ln)) * R);
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-            b[c] = (c * 8 < r8 && ln < n_rows) ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
-    };
-    uint4 bc[8], bn[8];
-    // B is a weight: the first item's row is requested before the wait when
-    // the groups are already known
-    bool b_loaded = false;
-    if (a.ids_early && (int)threadIdx.x < (*gp.n_groups << lg)) {
-        load_b(threadIdx.x, bc);
-        b_loaded = true;
-    }
-    if (late_u) {
-        // U comes from the kernels before this one, and so do the ids when the
-        // host could not rule that out: only from here on does the epilogue
-        // depend on them.
+            for (int c = 0; c < 8; ++c)
+                b[c] = (c * 8 < r8 && ln < n_rows) ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
+        };
+        uint4 bc[8], bn[8];
+        // B is a weight: the first item's row is requested before the wait
+        // when the groups are already known
+        bool b_loaded = false;
+        if (a.ids_early && (int)threadIdx.x < (*gp.n_groups << lg)) {
+            load_b(threadIdx.x, bc);
+            b_loaded = true;
+        }
+        // U comes from the kernels before this one, and so do the ids when
+        // the host could not rule that out: only from here on does the
+        // epilogue depend on them.
         pdl_wait();
         if (!a.ids_early)
             group_tokens(a, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
@@ -506,76 +716,58 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             }
         }
         __syncthreads();
-    }
-    const int n_items = *gp.n_groups << lg;
-    if (!b_loaded && (int)threadIdx.x < n_items) load_b(threadIdx.x, bc);
-    for (int item = threadIdx.x; item < n_items; item += kSkThreads) {
-        if (item + kSkThreads < n_items) load_b(item + kSkThreads, bn);
-        const int g = item >> lg, ln = item & (rows_per - 1);
-        if (ln < n_rows) {
-            const int n = n_lo + ln;
-            const int r8 = with_ex ? gp.gr8[g] : 0;
-            const int pe = gp.gbeg[g + 1];
-            // two tokens at a time: independent chains, each B element
-            // unpacked once for both
-            for (int p = gp.gbeg[g]; p < pe; p += 2) {
-                const bool two = p + 1 < pe;
-                const int ta = gp.order[p], tb = two ? gp.order[p + 1] : ta;
-                float va = red[ta * rows_per + ln], vb = red[tb * rows_per + ln];   // summed partials
-                if (r8 > 0) {
-                    const float* ua = u_smem ? sU + (size_t)ta * R : a.ex.U + (size_t)(t0 + ta) * R;
-                    const float* ub = u_smem ? sU + (size_t)tb * R : a.ex.U + (size_t)(t0 + tb) * R;
-                    float da = 0.f, db = 0.f;
+        const int n_items = *gp.n_groups << lg;
+        if (!b_loaded && (int)threadIdx.x < n_items) load_b(threadIdx.x, bc);
+        for (int item = threadIdx.x; item < n_items; item += kSkThreads) {
+            if (item + kSkThreads < n_items) load_b(item + kSkThreads, bn);
+            const int g = item >> lg, ln = item & (rows_per - 1);
+            if (ln < n_rows) {
+                const int n = n_lo + ln;
+                const int r8 = with_ex ? gp.gr8[g] : 0;
+                const int pe = gp.gbeg[g + 1];
+                // two tokens at a time: independent chains, each B element
+                // unpacked once for both
+                for (int p = gp.gbeg[g]; p < pe; p += 2) {
+                    const bool two = p + 1 < pe;
+                    const int ta = gp.order[p], tb = two ? gp.order[p + 1] : ta;
+                    float va = red[ta * rows_per + ln], vb = red[tb * rows_per + ln];   // summed partials
+                    if (r8 > 0) {
+                        const float* ua = u_smem ? sU + (size_t)ta * R : a.ex.U + (size_t)(t0 + ta) * R;
+                        const float* ub = u_smem ? sU + (size_t)tb * R : a.ex.U + (size_t)(t0 + tb) * R;
+                        float da = 0.f, db = 0.f;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        if (c * 8 < r8) {
-                            const float4 a0 = *reinterpret_cast<const float4*>(ua + c * 8);
-                            const float4 a1 = *reinterpret_cast<const float4*>(ua + c * 8 + 4);
-                            const float4 b0 = *reinterpret_cast<const float4*>(ub + c * 8);
-                            const float4 b1 = *reinterpret_cast<const float4*>(ub + c * 8 + 4);
-                            const uint4 w = bc[c];
-                            float e;
-                            e = bf16lo(w.x); da = fmaf(a0.x, e, da); db = fmaf(b0.x, e, db);
-                            e = bf16hi(w.x); da = fmaf(a0.y, e, da); db = fmaf(b0.y, e, db);
-                            e = bf16lo(w.y); da = fmaf(a0.z, e, da); db = fmaf(b0.z, e, db);
-                            e = bf16hi(w.y); da = fmaf(a0.w, e, da); db = fmaf(b0.w, e, db);
-                            e = bf16lo(w.z); da = fmaf(a1.x, e, da); db = fmaf(b1.x, e, db);
-                            e = bf16hi(w.z); da = fmaf(a1.y, e, da); db = fmaf(b1.y, e, db);
-                            e = bf16lo(w.w); da = fmaf(a1.z, e, da); db = fmaf(b1.z, e, db);
-                            e = bf16hi(w.w); da = fmaf(a1.w, e, da); db = fmaf(b1.w, e, db);
+                        for (int c = 0; c < 8; ++c) {
+                            if (c * 8 < r8) {
+                                const float4 a0 = *reinterpret_cast<const float4*>(ua + c * 8);
+                                const float4 a1 = *reinterpret_cast<const float4*>(ua + c * 8 + 4);
+                                const float4 b0 = *reinterpret_cast<const float4*>(ub + c * 8);
+                                const float4 b1 = *reinterpret_cast<const float4*>(ub + c * 8 + 4);
+                                const uint4 w = bc[c];
+                                float e;
+                                e = bf16lo(w.x); da = fmaf(a0.x, e, da); db = fmaf(b0.x, e, db);
+                                e = bf16hi(w.x); da = fmaf(a0.y, e, da); db = fmaf(b0.y, e, db);
+                                e = bf16lo(w.y); da = fmaf(a0.z, e, da); db = fmaf(b0.z, e, db);
+                                e = bf16hi(w.y); da = fmaf(a0.w, e, da); db = fmaf(b0.w, e, db);
+                                e = bf16lo(w.z); da = fmaf(a1.x, e, da); db = fmaf(b1.x, e, db);
+                                e = bf16hi(w.z); da = fmaf(a1.y, e, da); db = fmaf(b1.y, e, db);
+                                e = bf16lo(w.w); da = fmaf(a1.z, e, da); db = fmaf(b1.z, e, db);
+                                e = bf16hi(w.w); da = fmaf(a1.w, e, da); db = fmaf(b1.w, e, db);
+                            }
                         }
+                        if (r8 > 64) {
+                            const __nv_bfloat16* brow = Bp + ((size_t)gp.gslot[g] * a.N + n) * R;
+                            da = expand_dot_from(ua, brow, 64, r8, da);
+                            db = expand_dot_from(ub, brow, 64, r8, db);
+                        }
+                        va += da;
+                        vb += db;
                     }
-                    if (r8 > 64) {
-                        const __nv_bfloat16* brow = Bp + ((size_t)gp.gslot[g] * a.N + n) * R;
-                        da = expand_dot_from(ua, brow, 64, r8, da);
-                        db = expand_dot_from(ub, brow, 64, r8, db);
-                    }
-                    va += da;
-                    vb += db;
-                }
-                if (late_u) {
                     yp[(size_t)(t0 + ta) * a.N + n] = __float2bfloat16_rn(va);
                     if (two) yp[(size_t)(t0 + tb) * a.N + n] = __float2bfloat16_rn(vb);
-                } else {
-                    ystage[(size_t)ta * rows_per + ln] = __float2bfloat16_rn(va);
-                    if (two) ystage[(size_t)tb * rows_per + ln] = __float2bfloat16_rn(vb);
                 }
             }
-        }
 #pragma unroll
-        for (int c = 0; c < 8; ++c) bc[c] = bn[c];
-    }
-    if (!late_u) {
-        // Everything above needed only this kernel's inputs; y may still be
-        // read or written by the kernels ahead of it, so it is stored after the
-        // wait: 16-byte runs of n_rows consecutive outputs per token.
-        __syncthreads();
-        pdl_wait();
-        const int v8 = n_rows >> 3;                   // n_rows is a multiple of 8
-        for (int q = threadIdx.x; q < n_tok * v8; q += kSkThreads) {
-            const int t = q / v8, c = q - t * v8;
-            *reinterpret_cast<uint4*>(yp + (size_t)(t0 + t) * a.N + n_lo + c * 8) =
-                *reinterpret_cast<const uint4*>(ystage + (size_t)t * rows_per + c * 8);
+            for (int c = 0; c < 8; ++c) bc[c] = bn[c];
         }
     }
 

@@ -14,6 +14,7 @@ constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 25
 constexpr int kSkinnyPathMaxT = 256; // batches up to this many rows take the swap-AB kernel
 constexpr int kStageURank = 64;     // the skinny epilogue stages U rows of rank <= 64
 constexpr int kBySlotMaxT = 64;     // up to this many rows the shrink groups rows by slot itself
+constexpr size_t kSkinnyMaxSmem = (size_t)227 * 1024;   // dynamic shared memory a CTA may have
 
 struct PlanArgs {
     int32_t* slot_of_token;
@@ -73,6 +74,8 @@ struct SkinnyArgs {
     int ids_early;     // the ids may be read before that wait
     int fuse;          // compute U in this kernel (an A tile per K slice) instead of reading it
     int a_rows;        // rows of the A tile: (S - 1) * R_max, at most 128
+    int a_chunks;      // tensor-core expand: (S - 1) * R16 / 16 chunks of 16 (slot, rank) pairs, at most 8
+    int tcx;           // U from the shrink kernel ahead, expand on the tensor cores (rank 0 of the cluster)
     int kk;            // 64-column K slices per pipeline stage (> 1: 3-D / 4-D tensor maps)
     size_t smem;       // dynamic shared memory of the launch
 };
@@ -110,10 +113,12 @@ cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
 
 // Shared-memory bytes the skinny kernel needs for a token tile of TN columns
 // and `stages` pipeline stages.
-__host__ __device__ size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u, bool fuse,
+__host__ __device__ size_t skinny_smem_bytes(int TN, int stages, int R_max, bool stage_u, bool fuse, bool tc_expand,
                                              bool base_only, int kk);
-__host__ __device__ size_t skinny_epi_bytes(int TN, int R_max, bool stage_u, bool fuse, bool base_only);
+__host__ __device__ size_t skinny_epi_bytes(int TN, int R_max, bool stage_u, bool tc_expand, bool base_only);
 __host__ __device__ size_t skinny_stage_bytes(int TN, bool fuse, int kk);
+__host__ __device__ size_t skinny_grp_bytes(int TN);
+__host__ __device__ size_t skinny_xtab_bytes(int TN);
 int skinny_max_active_clusters(int TN, size_t smem, int ks);
 
 }  // namespace lora

@@ -168,6 +168,37 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
 }
 
+// 16-byte store into (possibly another CTA's) shared memory of the cluster.
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Arrive half of a cluster barrier that releases this thread's earlier memory
+// accesses to the peers that wait on it.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// The two halves of a cluster barrier, so that work can run between them:
+// every thread of every CTA of the cluster arrives, and a wait returns once
+// all have arrived. The relaxed arrive orders none of the thread's earlier
+// memory accesses: use it only where the peers' next accesses touch memory
+// that the arriving CTA last used through an already completed asynchronous
+// operation (a TMA copy, an MMA whose commit has been waited for).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Make this thread's ordinary shared-memory writes visible to the tensor
+// cores' (async proxy) reads that follow a barrier.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- PDL -------
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");

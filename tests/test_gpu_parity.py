@@ -383,6 +383,35 @@ def test_fused_shrink_invalid_ids_and_mixed_ranks():
         assert torch.equal(y[r].view(torch.int16), yb[r].view(torch.int16))
 
 
+def test_tensor_core_expand_with_ids_from_previous_output():
+    """The step's ids lie in the previous call's output on the same stream, so
+    the GEMM may not read them before its wait: U comes from the shrink kernel
+    ahead (two kernels) and the expand still runs on the tensor cores."""
+    T, K, N = 40, 512, 256
+    w = WL.random_case(seed=23, T=T, K=K, N=N, S=6, R_max=16, ranks=[0, 16, 5, 12, 16, 9])
+    t = w.targets[0]
+    W = t.W.to(DEV)
+    pool = L.Pool(w.S, w.R_max, K, N, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    x = w.x.to(DEV)
+    ids_dev = torch.from_numpy(w.ids.astype(np.int32)).to(DEV)
+    plan = L.Plan(T, w.S, w.R_max, K, device=DEV).build(ids_dev)
+    buf = torch.empty(T, N, dtype=torch.bfloat16, device=DEV)
+    L.linear(x, W, pool, plan, buf)
+    first = buf.clone()                                  # ordered after the GEMM on this stream
+    ids_in_y = buf.view(torch.int32).reshape(-1)[:T]     # overwrite part of that output with the ids
+    ids_in_y.copy_(ids_dev)
+    plan.build(ids_in_y)
+    n0 = L.launch_count()
+    y = L.linear(x, W, pool, plan)
+    assert L.launch_count() - n0 == 2                    # shrink kernel + GEMM
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    ref = O.lora_linear(f64(x), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, w.ids)
+    assert_parity(first, ref, "fused shrink")
+    assert_parity(y, ref, "shrink kernel, tensor-core expand")
+
+
 def test_shrink_kernel_when_pool_exceeds_one_tile():
     """(S - 1) * R_max > 128: U comes from the shrink kernel ahead of the GEMM."""
     w = WL.random_case(seed=22, T=48, K=512, N=384, S=10, R_max=16)
