@@ -470,24 +470,41 @@ int lora_linear_path(int T, int d_in, int d_out) {
     return T <= kSkinnyPathMaxT ? 0 : 1;
 }
 
-lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out, const lora_pool* pool,
-                        const lora_plan_t* plan, void* y, void* stream) {
-    if (T < 0 || d_in < 8 || d_out < 8) return LORA_EINVAL;
-    if ((d_in % 8) != 0 || (d_out % 8) != 0) return LORA_ESHAPE;
-    if (T == 0) return LORA_OK;
-    if (!x || !W || !y) return LORA_EINVAL;
-    if (!aligned16(x) || !aligned16(W) || !aligned16(y)) return LORA_EINVAL;
-    if (plan) {
-        if (!pool || !pool->A || !pool->B || !pool->rank || !pool->scale) return LORA_EINVAL;
-        if (!aligned16(pool->A) || !aligned16(pool->B)) return LORA_EINVAL;
-        if (plan->T != T || plan->S != pool->S || plan->R_max != pool->R_max || pool->d_in != d_in ||
-            pool->d_out != d_out || d_in > plan->d_in_cap)
-            return LORA_ESHAPE;
-    }
+static_assert(kMaxSlices == LORA_MAX_SLICES, "slice limit of the C ABI and the kernels");
+
+namespace {
+
+// Projections that share x, as one decode GEMM (lora_linear_sliced).
+struct SliceSet {
+    int n;
+    const lora_pool* pools[kMaxSlices];
+    int d_out[kMaxSlices];
+};
+
+bool pool_valid(const lora_pool* pool, const lora_plan_t* plan, int T, int d_in, int d_out) {
+    if (!pool || !pool->A || !pool->B || !pool->rank || !pool->scale) return false;
+    if (!aligned16(pool->A) || !aligned16(pool->B)) return false;
+    return plan->T == T && plan->S == pool->S && plan->R_max == pool->R_max && pool->d_in == d_in &&
+           pool->d_out == d_out && d_in <= plan->d_in_cap;
+}
+
+bool pool_overlaps(const Range& prev, const lora_pool* pool, int d_in, int d_out) {
+    return overlaps(prev, pool->A, (size_t)pool->S * pool->R_max * d_in * 2) ||
+           overlaps(prev, pool->B, (size_t)pool->S * d_out * pool->R_max * 2) ||
+           overlaps(prev, pool->rank, (size_t)pool->S * 4) || overlaps(prev, pool->scale, (size_t)pool->S * 4);
+}
+
+// The layer on y rows of pitch ldy (>= d_out). With `slices`, W, y and d_out
+// cover every slice and `pool` is the first slice's; only the decode GEMM
+// with the shrink fused in takes several slices.
+lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out, const lora_pool* pool,
+                        const lora_plan_t* plan, void* y, int ldy, const SliceSet* slices, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int path = lora_linear_path(T, d_in, d_out);
     if (plan && path == 1 && !plan->x_sorted) return LORA_ESHAPE;
     if (plan && path == 0 && !plan->ids) return LORA_EINVAL;     // lora_plan was never run
+    const int n_sl = slices ? slices->n : 1;
+    const size_t y_bytes = ((size_t)(T - 1) * ldy + d_out) * 2;
 
     // Inputs written by the previous lora_linear on this stream are read only
     // after the wait; weights or pool aliasing it (never expected) turn the
@@ -497,9 +514,8 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
                          !(plan && overlaps(prev, plan->ids, (size_t)T * 4));
     bool pdl = !overlaps(prev, W, (size_t)d_out * d_in * 2);
     if (plan)
-        pdl = pdl && !overlaps(prev, pool->A, (size_t)pool->S * pool->R_max * d_in * 2) &&
-              !overlaps(prev, pool->B, (size_t)pool->S * d_out * pool->R_max * 2) &&
-              !overlaps(prev, pool->rank, (size_t)pool->S * 4) && !overlaps(prev, pool->scale, (size_t)pool->S * 4);
+        for (int q = 0; q < n_sl; ++q)
+            pdl = pdl && !pool_overlaps(prev, slices ? slices->pools[q] : pool, d_in, slices ? slices->d_out[q] : d_out);
 
     // Decode batches of one token tile, with a pool whose adapter slots
     // (1..S-1, R_max ranks each, rounded up to 16) fit one 128-row tile,
@@ -514,6 +530,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     // slot's ranks (rounded up to 16) fit 128 pairs; else on the CUDA cores.
     const bool tc_expand = plan && path == 0 && T <= 64 && pool->S >= 2 && (pool->S - 1) * r16 <= 128;
     const bool fuse = tc_expand && ids_early;
+    if (slices && !fuse) return LORA_EINVAL;                   // callers check this first
     if (plan && !fuse) {
         ShrinkArgs sa;
         sa.x = static_cast<const __nv_bfloat16*>(x);
@@ -545,9 +562,6 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     ExpandArgs ex;
     ex.ids = plan ? plan->ids : nullptr;
     ex.U = plan ? plan->U : nullptr;
-    ex.B = plan ? static_cast<const __nv_bfloat16*>(pool->B) : nullptr;
-    ex.rank = plan ? pool->rank : nullptr;
-    ex.scale = plan ? pool->scale : nullptr;
     ex.R_max = plan ? pool->R_max : 8;
     ex.S = plan ? pool->S : 0;
 
@@ -555,7 +569,9 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     if (path == 0) {
         const int mode = !plan ? 0 : (fuse ? 2 : (tc_expand ? 3 : 1));
         const SkinnyConfig c = skinny_config(T, d_in, d_out, mode, plan ? pool->R_max : 8, plan ? pool->S : 1);
-        CUtensorMap tmW, tmX, tmA;
+        SkinnyMaps maps;
+        CUtensorMap& tmW = maps.w;
+        CUtensorMap& tmX = maps.x;
         const uint64_t ksl = (uint64_t)d_in / 64;           // 64-column slices (kk > 1: d_in % 64 == 0)
         if (c.kk == 1) {
             if (!make_tmap(&tmW, W, (uint64_t)d_in, (uint64_t)d_out, 64, 128) ||
@@ -571,25 +587,39 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
                 !make_tmap_nd(&tmX, x, 3, dx, pr, bx, CU_TENSOR_MAP_SWIZZLE_128B))
                 return LORA_ECUDA;
         }
-        if (fuse) {
-            // A pool [S][R_max][d_in]: slots 1..S-1, R_max rows x 64 columns each
-            // (x kk slices), per copy
-            if (c.kk == 1) {
-                const uint64_t da[3] = {(uint64_t)d_in, (uint64_t)pool->R_max, (uint64_t)pool->S};
-                const uint64_t pa[2] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2};
-                const uint32_t ba[3] = {64, (uint32_t)pool->R_max, (uint32_t)(pool->S - 1)};
-                if (!make_tmap_nd(&tmA, pool->A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
-            } else {
-                const uint64_t da[4] = {64, (uint64_t)pool->R_max, (uint64_t)pool->S, ksl};
-                const uint64_t pa[3] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2, 128};
-                const uint32_t ba[4] = {64, (uint32_t)pool->R_max, (uint32_t)(pool->S - 1), (uint32_t)c.kk};
-                if (!make_tmap_nd(&tmA, pool->A, 4, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
-            }
-        } else {
-            tmA = tmX;                 // unused
-        }
         SkinnyArgs a;
+        a.n_slices = n_sl;
+        int noff = 0;
+        for (int q = 0; q < kMaxSlices; ++q) {
+            const lora_pool* p = q < n_sl ? (slices ? slices->pools[q] : pool) : nullptr;
+            const int nb = q < n_sl ? (slices ? slices->d_out[q] : d_out) : 0;
+            SliceExpand& e = a.sl[q];
+            e.B = (plan && p) ? static_cast<const __nv_bfloat16*>(p->B) : nullptr;
+            e.rank = (plan && p) ? p->rank : nullptr;
+            e.scale = (plan && p) ? p->scale : nullptr;
+            e.nb = nb;
+            e.noff = noff;
+            noff += nb;
+            e.tile_end = (noff + 127) / 128;
+            maps.a[q] = tmX;           // unused unless fused
+            if (fuse && p) {
+                // A pool [S][R_max][d_in]: slots 1..S-1, R_max rows x 64
+                // columns each (x kk slices), per copy
+                if (c.kk == 1) {
+                    const uint64_t da[3] = {(uint64_t)d_in, (uint64_t)p->R_max, (uint64_t)p->S};
+                    const uint64_t pa[2] = {(uint64_t)d_in * 2, (uint64_t)p->R_max * d_in * 2};
+                    const uint32_t ba[3] = {64, (uint32_t)p->R_max, (uint32_t)(p->S - 1)};
+                    if (!make_tmap_nd(&maps.a[q], p->A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+                } else {
+                    const uint64_t da[4] = {64, (uint64_t)p->R_max, (uint64_t)p->S, ksl};
+                    const uint64_t pa[3] = {(uint64_t)d_in * 2, (uint64_t)p->R_max * d_in * 2, 128};
+                    const uint32_t ba[4] = {64, (uint32_t)p->R_max, (uint32_t)(p->S - 1), (uint32_t)c.kk};
+                    if (!make_tmap_nd(&maps.a[q], p->A, 4, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+                }
+            }
+        }
         a.y = static_cast<__nv_bfloat16*>(y);
+        a.ldy = ldy;
         a.ex = ex;
         a.T = T;
         a.K = d_in;
@@ -607,7 +637,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         a.smem = c.smem;
         a.x_early = x_early ? 1 : 0;
         a.ids_early = ids_early ? 1 : 0;
-        if (counted(launch_skinny(tmW, tmX, tmA, a, pdl, num_sms(), st)) != cudaSuccess) return LORA_ECUDA;
+        if (counted(launch_skinny(maps, a, pdl, num_sms(), st)) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;
         // 128 x 256 output tiles, or 128 x 128 for mid-sized grids (fewer
@@ -652,6 +682,7 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         }
         WideArgs a;
         a.y = static_cast<__nv_bfloat16*>(y);
+        a.ldy = ldy;
         a.token_order = plan ? plan->token_order : nullptr;
         a.mt_ptr = plan ? plan->mt_ptr : nullptr;
         a.mt_seg = plan ? reinterpret_cast<const int4*>(plan->mt_seg) : nullptr;
@@ -671,7 +702,78 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
         if (counted(launch_wide(tmA, tmB, tmU, tmBs, a, pdl, grid, st)) != cudaSuccess) return LORA_ECUDA;
     }
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;
-    set_last_out(st, y, (size_t)T * d_out * 2);
+    set_last_out(st, y, y_bytes);
+    return LORA_OK;
+}
+
+}  // namespace
+
+lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out, const lora_pool* pool,
+                        const lora_plan_t* plan, void* y, void* stream) {
+    if (T < 0 || d_in < 8 || d_out < 8) return LORA_EINVAL;
+    if ((d_in % 8) != 0 || (d_out % 8) != 0) return LORA_ESHAPE;
+    if (T == 0) return LORA_OK;
+    if (!x || !W || !y) return LORA_EINVAL;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y)) return LORA_EINVAL;
+    if (plan) {
+        if (!pool || !pool->A || !pool->B || !pool->rank || !pool->scale) return LORA_EINVAL;
+        if (!pool_valid(pool, plan, T, d_in, d_out)) return (!aligned16(pool->A) || !aligned16(pool->B)) ? LORA_EINVAL
+                                                                                                         : LORA_ESHAPE;
+    }
+    return linear_impl(x, W, T, d_in, d_out, pool, plan, y, d_out, nullptr, stream);
+}
+
+lora_status lora_linear_sliced(const void* x, const void* W, int T, int d_in, int n_slices, const int32_t* d_outs,
+                               const lora_pool* const* pools, const lora_plan_t* plan, void* y, void* stream) {
+    if (T < 0 || d_in < 8 || n_slices < 1 || n_slices > LORA_MAX_SLICES || !d_outs) return LORA_EINVAL;
+    if (d_in % 8 != 0) return LORA_ESHAPE;
+    int N = 0;
+    for (int q = 0; q < n_slices; ++q) {
+        if (d_outs[q] < 8) return LORA_EINVAL;
+        if (d_outs[q] % 8 != 0) return LORA_ESHAPE;
+        N += d_outs[q];
+    }
+    if (T == 0) return LORA_OK;
+    if (!x || !W || !y) return LORA_EINVAL;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y)) return LORA_EINVAL;
+    if (plan) {
+        if (!pools) return LORA_EINVAL;
+        for (int q = 0; q < n_slices; ++q) {
+            const lora_pool* p = pools[q];
+            if (!p || !p->A || !p->B || !p->rank || !p->scale || !aligned16(p->A) || !aligned16(p->B))
+                return LORA_EINVAL;
+            if (!pool_valid(p, plan, T, d_in, d_outs[q])) return LORA_ESHAPE;
+        }
+    } else {
+        // base only: the slices are one projection of N outputs
+        return linear_impl(x, W, T, d_in, N, nullptr, nullptr, y, N, nullptr, stream);
+    }
+    // One decode GEMM for every slice when each computes U itself (the
+    // shrink fused in) and no weight tile straddles two slices; else one
+    // call per slice, each writing its columns of y.
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Range prev = last_out(st);
+    const bool ids_early = !overlaps(prev, plan->ids, (size_t)T * 4);
+    bool one = lora_linear_path(T, d_in, N) == 0 && T <= 64 && ids_early && plan->S >= 2 &&
+               (plan->S - 1) * ((plan->R_max + 15) / 16 * 16) <= 128;
+    for (int q = 0; q + 1 < n_slices; ++q) one = one && d_outs[q] % 128 == 0;
+    if (one) {
+        SliceSet set;
+        set.n = n_slices;
+        for (int q = 0; q < n_slices; ++q) {
+            set.pools[q] = pools[q];
+            set.d_out[q] = d_outs[q];
+        }
+        return linear_impl(x, W, T, d_in, N, pools[0], plan, y, N, &set, stream);
+    }
+    int off = 0;
+    for (int q = 0; q < n_slices; ++q) {
+        const lora_status r = linear_impl(x, static_cast<const __nv_bfloat16*>(W) + (size_t)off * d_in, T, d_in,
+                                          d_outs[q], pools[q], plan, static_cast<__nv_bfloat16*>(y) + off, N,
+                                          nullptr, stream);
+        if (r != LORA_OK) return r;
+        off += d_outs[q];
+    }
     return LORA_OK;
 }
 

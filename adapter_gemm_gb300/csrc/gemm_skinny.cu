@@ -146,8 +146,8 @@ __device__ __forceinline__ void grp_barrier(int nthr) {
 // warps) numbered i0 = 0.. that run it, and send this CTA's rows of B for
 // every group to L2. Invalid ids, slot 0 and rank-0 slots all map to slot 0:
 // those tokens get the base output only. Reads the ids, the pool's ranks and B.
-__device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, int n_tok, int i0, int nthr,
-                             int n_lo, int n_rows, int n_rows_per) {
+__device__ void group_tokens(const SkinnyArgs& a, const SliceExpand& sv, const TileGroups& gp, int t0, int n_tok,
+                             int i0, int nthr, int n_lo, int n_rows, int n_rows_per) {
     const bool with_ex = a.ex.ids != nullptr;
     const int lane = threadIdx.x & 31;
     for (int t = i0; t < n_tok; t += nthr) {
@@ -155,7 +155,7 @@ __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, 
         if (with_ex) {
             const int id = a.ex.ids[t0 + t];
             if (id >= 1 && id < a.ex.S) {
-                const int r = min(a.ex.rank[id], a.ex.R_max);
+                const int r = min(sv.rank[id], a.ex.R_max);
                 if (r > 0) {
                     s = id;
                     r8 = (r + 7) & ~7;
@@ -213,7 +213,7 @@ __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, 
         const int G = *gp.n_groups;
         for (int g = i0; g < G; g += nthr)
             if (gp.gr8[g] > 0)
-                prefetch_l2_bulk(a.ex.B + ((size_t)gp.gslot[g] * a.N + n_lo) * a.ex.R_max,
+                prefetch_l2_bulk(sv.B + ((size_t)gp.gslot[g] * sv.nb + (n_lo - sv.noff)) * a.ex.R_max,
                                  (uint32_t)n_rows * (uint32_t)a.ex.R_max * 2u);
     }
 }
@@ -222,23 +222,23 @@ __device__ void group_tokens(const SkinnyArgs& a, const TileGroups& gp, int t0, 
 // msc[a][t] = alpha / r of slot a + 1 when token t is on that slot (a valid id
 // of a slot of nonzero rank), else 0; tact[t] = that a, or -1; srank[a] = the
 // rank of slot a + 1. Reads the ids and the pool's ranks and scales.
-__device__ void expand_tables(const SkinnyArgs& a, float* msc, int* tact, int* srank, int t0, int n_tok, int i0,
-                              int nthr) {
+__device__ void expand_tables(const SkinnyArgs& a, const SliceExpand& sv, float* msc, int* tact, int* srank, int t0,
+                              int n_tok, int i0, int nthr) {
     const int TN = a.TN, n_act = a.ex.S - 1;
     for (int t = i0; t < TN; t += nthr) {
         int act = -1;
         float sc = 0.f;
         if (t < n_tok) {
             const int id = a.ex.ids[t0 + t];
-            if (id >= 1 && id < a.ex.S && a.ex.rank[id] > 0) {
+            if (id >= 1 && id < a.ex.S && sv.rank[id] > 0) {
                 act = id - 1;
-                sc = a.ex.scale[id];
+                sc = sv.scale[id];
             }
         }
         tact[t] = act;
         for (int ai = 0; ai < n_act; ++ai) msc[ai * TN + t] = (act == ai) ? sc : 0.f;
     }
-    for (int ai = i0; ai < n_act; ai += nthr) srank[ai] = min(a.ex.rank[ai + 1], a.ex.R_max);
+    for (int ai = i0; ai < n_act; ai += nthr) srank[ai] = min(sv.rank[ai + 1], a.ex.R_max);
 }
 
 // This tile's Bcat in shared memory, by the `nthr` threads numbered i0 = 0..:
@@ -246,17 +246,17 @@ __device__ void expand_tables(const SkinnyArgs& a, float* msc, int* tact, int* s
 // B[a + 1, n0 + n, 16 h + 0..15] for the tile's 128 weight rows n, zero past
 // R_max and past d_out. Reads only B (a weight), so it may run before the wait.
 // Each thread has four 16-byte loads in flight at a time.
-__device__ void stage_bcat(const SkinnyArgs& a, uint8_t* bcat, int n0, int i0, int nthr) {
+__device__ void stage_bcat(const SkinnyArgs& a, const SliceExpand& sv, uint8_t* bcat, int n0, int i0, int nthr) {
     const int R = a.ex.R_max, cps = (R + 15) >> 4;
     const int n_items = a.a_chunks * kWRows * 2;      // (chunk, row, 16-byte half)
-    const __nv_bfloat16* __restrict__ Bp = a.ex.B;
+    const __nv_bfloat16* __restrict__ Bp = sv.B;
     auto fetch = [&](int e) -> uint4 {
         const int h = e & 1, n = (e >> 1) & (kWRows - 1), c = e >> 8;
         const int ai = c / cps, j0 = (c - ai * cps) * 16 + h * 8;
-        const int row = n0 + n;
+        const int row = n0 - sv.noff + n;              // row of the slice's B
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (e < n_items && row < a.N && j0 < R) {
-            const __nv_bfloat16* src = Bp + ((size_t)(ai + 1) * a.N + row) * R + j0;
+        if (e < n_items && row < sv.nb && j0 < R) {
+            const __nv_bfloat16* src = Bp + ((size_t)(ai + 1) * sv.nb + row) * R + j0;
             if ((R & 7) == 0) {
                 v = __ldg(reinterpret_cast<const uint4*>(src));
             } else {
@@ -286,8 +286,7 @@ __device__ void stage_bcat(const SkinnyArgs& a, uint8_t* bcat, int n0, int i0, i
 }
 
 __global__ void __launch_bounds__(kSkThreads, 1)
-gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   const __grid_constant__ CUtensorMap tmA, SkinnyArgs a) {
+gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constant__ SkinnyArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte aligned base, derived by offsetting the shared array itself so
     // the compiler keeps every pointer below in the shared address space.
@@ -338,6 +337,13 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x;
+    // the slice this weight tile belongs to (tiles never straddle slices)
+    int sl = 0;
+    while (sl + 1 < a.n_slices && n_tile >= a.sl[sl].tile_end) ++sl;
+    const SliceExpand& sv = a.sl[sl];
+    const CUtensorMap& tmW = maps.w;
+    const CUtensorMap& tmX = maps.x;
+    const CUtensorMap& tmA = maps.a[sl];
     const int kz = (a.ks > 1) ? (int)blockIdx.y : 0;
     const int t_tile = blockIdx.z;
     const int n0 = n_tile * kWRows, t0 = t_tile * TN;
@@ -473,11 +479,11 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     } else if (warp >= 2 && tce) {
         // Idle during the K loop: Bcat, and the token tables when the ids may
         // be read before the wait.
-        stage_bcat(a, bcat, n0, (int)threadIdx.x - 64, kSkThreads - 64);
-        if (a.ids_early) expand_tables(a, msc, tact, srank, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64);
+        stage_bcat(a, sv, bcat, n0, (int)threadIdx.x - 64, kSkThreads - 64);
+        if (a.ids_early) expand_tables(a, sv, msc, tact, srank, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64);
     } else if (warp >= 2 && late_u && a.ids_early) {
         // Idle during the K loop: group the tokens and fetch B's rows to L2.
-        group_tokens(a, gp, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64, n_lo, n_rows, rows_per);
+        group_tokens(a, sv, gp, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64, n_lo, n_rows, rows_per);
     }
     __syncwarp();
     const int row = (warp & 3) * 32 + lane;         // the accumulator row (TMEM lane) this thread reads
@@ -507,7 +513,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
             // U (and, when the host could not rule out that the kernel ahead
             // writes them, the ids) come from the kernels before this one.
             pdl_wait();
-            if (!a.ids_early) expand_tables(a, msc, tact, srank, t0, n_tok, (int)threadIdx.x, kSkThreads);
+            if (!a.ids_early) expand_tables(a, sv, msc, tact, srank, t0, n_tok, (int)threadIdx.x, kSkThreads);
         }
         __syncthreads();
         const size_t lo_off = (size_t)TN * kChunkRowBytes;
@@ -660,7 +666,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         const int v8 = n_rows >> 3;                   // n_rows is a multiple of 8
         for (int q = threadIdx.x; q < n_tok * v8; q += kSkThreads) {
             const int t = q / v8, c = q - t * v8;
-            *reinterpret_cast<uint4*>(yp + (size_t)(t0 + t) * a.N + n_lo + c * 8) =
+            *reinterpret_cast<uint4*>(yp + (size_t)(t0 + t) * a.ldy + n_lo + c * 8) =
                 *reinterpret_cast<const uint4*>(ystage + (size_t)t * rows_per + c * 8);
         }
     } else {
@@ -682,12 +688,12 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // computed) and finishes every token of the piece:
         //   y[t, n] = bf16( sum_z partial_z[t, n] + sum_j U[t, j] B[s, n, j] ),
         // z in rank order, j ascending; slot-0 groups only sum the partials.
-        const __nv_bfloat16* __restrict__ Bp = a.ex.B;
+        const __nv_bfloat16* __restrict__ Bp = sv.B;
         const bool u_smem = a.stage_u != 0;
         auto load_b = [&](int item, uint4 (&b)[8]) {
             const int g = item >> lg, ln = item & (rows_per - 1);
             const int r8 = gp.gr8[g];
-            const uint4* brow = reinterpret_cast<const uint4*>(Bp + ((size_t)gp.gslot[g] * a.N + (n_lo + ln)) * R);
+            const uint4* brow = reinterpret_cast<const uint4*>(Bp + ((size_t)gp.gslot[g] * sv.nb + (n_lo - sv.noff + ln)) * R);
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 b[c] = (c * 8 < r8 && ln < n_rows) ? __ldg(brow + c) : make_uint4(0, 0, 0, 0);
@@ -705,7 +711,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
         // epilogue depend on them.
         pdl_wait();
         if (!a.ids_early)
-            group_tokens(a, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
+            group_tokens(a, sv, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
         if (a.stage_u) {
             const int R4 = R >> 2;
             for (int q = threadIdx.x; q < n_tok * R4; q += kSkThreads) {
@@ -755,15 +761,15 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
                             }
                         }
                         if (r8 > 64) {
-                            const __nv_bfloat16* brow = Bp + ((size_t)gp.gslot[g] * a.N + n) * R;
+                            const __nv_bfloat16* brow = Bp + ((size_t)gp.gslot[g] * sv.nb + (n - sv.noff)) * R;
                             da = expand_dot_from(ua, brow, 64, r8, da);
                             db = expand_dot_from(ub, brow, 64, r8, db);
                         }
                         va += da;
                         vb += db;
                     }
-                    yp[(size_t)(t0 + ta) * a.N + n] = __float2bfloat16_rn(va);
-                    if (two) yp[(size_t)(t0 + tb) * a.N + n] = __float2bfloat16_rn(vb);
+                    yp[(size_t)(t0 + ta) * a.ldy + n] = __float2bfloat16_rn(va);
+                    if (two) yp[(size_t)(t0 + tb) * a.ldy + n] = __float2bfloat16_rn(vb);
                 }
             }
 #pragma unroll
@@ -777,8 +783,7 @@ gemm_skinny_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constan
     }
 }
 
-cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmA,
-                          const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream) {
+cudaError_t launch_skinny(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream) {
     (void)num_sms;
     const size_t smem = a.smem;
     cudaError_t e = ensure_smem_attr((const void*)gemm_skinny_kernel, 1, smem);
@@ -802,7 +807,7 @@ cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const 
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel, tmW, tmX, tmA, a);
+    return cudaLaunchKernelEx(&cfg, gemm_skinny_kernel, maps, a);
 }
 
 // How many clusters of `ks` CTAs of this configuration can be resident at once.

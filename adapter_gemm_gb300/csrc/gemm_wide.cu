@@ -283,7 +283,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int i = m0 + row;
             const bool valid = i < a.T;
             const int t = valid ? (a.token_order ? a.token_order[i] : i) : 0;
-            __nv_bfloat16* yrow = a.y + (size_t)t * a.N;
+            __nv_bfloat16* yrow = a.y + (size_t)t * a.ldy;
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(as * kWdBN);
             for (int c = 0; c < kWdBN; c += 16) {
                 float v[16];

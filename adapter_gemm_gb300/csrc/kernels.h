@@ -54,17 +54,34 @@ struct ShrinkArgs {
 struct ExpandArgs {
     const int32_t* ids;            // [T] the step's raw slot ids (invalid ones mean slot 0)
     const float* U;                // [T, R_max] by token (shrink kernel ahead)
-    const __nv_bfloat16* B;        // [S, N, R_max]
-    const int32_t* rank;           // [S]
-    const float* scale;            // [S] alpha / r (fused shrink)
     int R_max;
     int S;
 };
 
+// Projections that share x (QKV, gate/up) in one decode GEMM: W and y hold the
+// slices' output columns side by side; each slice has its own pool.
+constexpr int kMaxSlices = 4;
+struct SliceExpand {
+    const __nv_bfloat16* B;        // [S, nb, R_max] of this slice's pool
+    const int32_t* rank;           // [S]
+    const float* scale;            // [S] alpha / r
+    int nb;                        // the slice's output columns
+    int noff;                      // its first output column
+    int tile_end;                  // one past its last 128-row weight tile
+};
+
+struct SkinnyMaps {
+    CUtensorMap w, x;              // W [N][K], x [T][K]
+    CUtensorMap a[kMaxSlices];     // fused: each slice's A pool
+};
+
 struct SkinnyArgs {
-    __nv_bfloat16* y;  // [T, N]
+    __nv_bfloat16* y;  // [T, ldy]
     ExpandArgs ex;
-    int T, K, N;
+    SliceExpand sl[kMaxSlices];
+    int n_slices;
+    int T, K, N;       // N: output columns of all slices
+    int ldy;           // row pitch of y in elements
     int TN;            // token columns per tile (multiple of 16, <= 256)
     int kb_total;      // ceil(K / 64)
     int ks;            // K splits = cluster size along y
@@ -81,7 +98,8 @@ struct SkinnyArgs {
 };
 
 struct WideArgs {
-    __nv_bfloat16* y;               // [T, N]
+    __nv_bfloat16* y;               // [T, ldy]
+    int ldy;                        // row pitch of y in elements
     const int32_t* token_order;     // [T] row of each plan position, or null (identity)
     const int32_t* mt_ptr;          // per 128-row block, first adapter segment (null: base only)
     const int4* mt_seg;             // adapter segments per block (slot, row begin, row end, block)
@@ -95,8 +113,7 @@ struct WideArgs {
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream);
-cudaError_t launch_skinny(const CUtensorMap& tmW, const CUtensorMap& tmX, const CUtensorMap& tmA,
-                          const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream);
+cudaError_t launch_skinny(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream);
 cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
                         const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
 cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);

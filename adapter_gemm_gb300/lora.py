@@ -65,6 +65,9 @@ _SIGS = {
     "lora_linear": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(lora_pool),
                              ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p]),
     "lora_linear_path": (_c_int, [_c_int, _c_int, _c_int]),
+    "lora_linear_sliced": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(_c_int32),
+                                    ctypes.POINTER(ctypes.POINTER(lora_pool)), ctypes.POINTER(lora_plan_t),
+                                    _c_void_p, _c_void_p]),
     "lora_profile_gemm_events": (_c_int, [_c_void_p, _c_void_p]),
     "lora_linear_static_scratch": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(lora_pool),
                                             _c_void_p, _c_void_p, _c_void_p]),
@@ -245,6 +248,30 @@ def linear(x: torch.Tensor, W: torch.Tensor, pool: Pool | None = None, plan: Pla
                               ctypes.byref(pool.c) if plan is not None else None,
                               ctypes.byref(plan.c) if plan is not None else None,
                               _ptr(y, torch.bfloat16, "y"), _stream(stream)), "lora_linear")
+    return y
+
+
+def linear_sliced(x: torch.Tensor, W: torch.Tensor, d_outs, pools=None, plan: Plan | None = None,
+                  y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Projections that share x: W [sum(d_outs), d_in] stacks the slices'
+    weights, pools[i] holds slice i's adapters; y [T, sum(d_outs)] gets each
+    slice's outputs in its columns (plan=None: base projection only)."""
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1]:
+        raise ValueError("x [T, d_in] and W [N, d_in] expected")
+    d_outs = [int(d) for d in d_outs]
+    if sum(d_outs) != W.shape[0]:
+        raise ValueError("the slices' d_out must add up to W's rows")
+    T, d_in = x.shape
+    if y is None:
+        y = torch.empty((T, W.shape[0]), dtype=torch.bfloat16, device=x.device)
+    if plan is not None and (pools is None or len(pools) != len(d_outs)):
+        raise ValueError("a plan needs one pool per slice")
+    n = len(d_outs)
+    douts = (_c_int32 * n)(*d_outs)
+    pptrs = (ctypes.POINTER(lora_pool) * n)(*[ctypes.pointer(p.c) for p in pools]) if plan is not None else None
+    _check(_lib().lora_linear_sliced(_ptr(x, torch.bfloat16, "x"), _ptr(W, torch.bfloat16, "W"), T, d_in, n, douts,
+                                     pptrs, ctypes.byref(plan.c) if plan is not None else None,
+                                     _ptr(y, torch.bfloat16, "y"), _stream(stream)), "lora_linear_sliced")
     return y
 
 

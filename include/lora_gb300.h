@@ -178,6 +178,38 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
  * split-K across a thread-block cluster), 1 = wide (persistent 128x256 tiles). */
 int lora_linear_path(int T, int d_in, int d_out);
 
+/* Most output slices one lora_linear_sliced call takes. */
+#define LORA_MAX_SLICES 4
+
+/* Projections that share their input x: the query, key and value projections,
+ * or the gate and up projections of an MLP. The LoRA-serving page, section
+ * "vLLM: preallocated stacked buffers plus a Punica-style Triton kernel",
+ * keeps one stacked A and B per output slice (n_slices), shrinks into
+ * [num_slices, num_tokens, rank] and expands over output_slices. Its worked
+ * example notes that the merged QKV and gate/up wrappers fuse their slices into
+ * one launch.
+ *   W [N, d_in] bf16 device: the slices' weights stacked along the output
+ *     dimension, N = d_outs[0] + .. + d_outs[n_slices - 1]; slice i owns the
+ *     rows (and y's columns) from d_outs[0] + .. + d_outs[i - 1] on;
+ *   y [T, N] bf16 device, each slice's outputs in its own columns;
+ *   pools[i]: slice i's adapters over the common slots, with pools[i]->S ==
+ *     plan->S, pools[i]->R_max == plan->R_max, pools[i]->d_in == d_in and
+ *     pools[i]->d_out == d_outs[i] (each pool holds its own ranks and scales).
+ * Result: for every slice i, y's columns of slice i are exactly what
+ * lora_linear returns for (x, W_i, pools[i], plan). 1 <= n_slices <=
+ * LORA_MAX_SLICES; every d_outs[i] a multiple of 8. plan == NULL (pools
+ * ignored) runs the base projection of all N outputs.
+ * Dispatch: the slices run as a single GEMM launch when every condition holds:
+ *   - the batch is decode-sized;
+ *   - the pools' adapters fit the shrink fused into the GEMM;
+ *   - every slice but the last has a multiple of 128 outputs.
+ * Otherwise there is one lora_linear per slice.
+ * Asynchronous and stream-ordered like lora_linear; LORA_EINVAL / LORA_ESHAPE
+ * for bad arguments, before anything is launched. */
+lora_status lora_linear_sliced(const void* x, const void* W, int T, int d_in, int n_slices,
+                               const int32_t* d_outs, const lora_pool* const* pools,
+                               const lora_plan_t* plan, void* y, void* stream);
+
 /* Profiling hook: when both are non-NULL cudaEvent_t handles, every following
  * lora_linear records `start` on its stream right before it launches the GEMM
  * kernel and `stop` right after it, so the caller can time that kernel alone

@@ -17,6 +17,10 @@ What it computes, and where the pages define it:
   correction at all. alpha_s / r_s uses the adapter's true rank (Chapter 43,
   AdapterBank.load; conventions table "alpha / rank (PEFT convention)").
 
+* Several projections that share x (LoRA serving page, the vLLM section's
+  per-slice stacked A and B): each output slice is the layer above with its
+  own adapters; the slices' outputs sit side by side.
+
 * The plan (LoRA serving page, "The metadata is a sort and a unique" and the
   worked three-request example; mstar LoraAddressing): a stable sort of token
   rows by slot, the per-slot counts, their exclusive prefix sum (segment start
@@ -134,6 +138,18 @@ def lora_linear(x, W, A, B, rank, alpha, ids, rows=None) -> np.ndarray:
         u = xs @ A[s, :r].T                    # shrink: [n, r]
         y[sel] += slot_scale(alpha[s], r) * (u @ B[s, :, :r].T)   # expand + add
     return y
+
+
+def lora_linear_sliced(x, Ws, As, Bs, ranks, alphas, ids, rows=None) -> np.ndarray:
+    """Projections that share x, such as query/key/value or gate/up (LoRA
+    serving page, "vLLM: preallocated stacked buffers plus a Punica-style
+    Triton kernel": one stacked A and one stacked B per output slice, a shrink
+    into [num_slices, num_tokens, rank], an expand over output_slices). Slice i
+    is the layer of (x, Ws[i], As[i], Bs[i], ranks[i], alphas[i]) with the
+    common ids; the slices' outputs are placed side by side, in slice order.
+    Returns float64 [len(rows) or T, sum of the slices' d_out]."""
+    return np.concatenate([lora_linear(x, W, A, B, r, a, ids, rows=rows)
+                           for W, A, B, r, a in zip(Ws, As, Bs, ranks, alphas)], axis=1)
 
 
 def lora_linear_indexed(x, W, A, B, rank, alpha, ids) -> np.ndarray:

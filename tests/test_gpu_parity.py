@@ -420,3 +420,78 @@ def test_shrink_kernel_when_pool_exceeds_one_tile():
     y = dw.run(0)
     assert L.launch_count() - n0 == 2
     assert_parity(y, dw.oracle(0), "shrink kernel")
+
+
+# ------------------------------------------ projections that share x (slices) ----
+
+def _sliced(seed, T, K, d_outs, S, R, ranks=None):
+    ws = [WL.random_case(seed=seed + i, T=T, K=K, N=n, S=S, R_max=R, ranks=ranks) for i, n in enumerate(d_outs)]
+    ts = [w.targets[0] for w in ws]
+    x = ws[0].x.to(DEV)
+    ids_np = ws[0].ids.astype(np.int32)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    W = torch.cat([t.W for t in ts], 0).to(DEV)
+    pools = []
+    for t, n in zip(ts, d_outs):
+        p = L.Pool(S, R, K, n, device=DEV)
+        p.load_padded(t.A, t.B, t.rank, t.alpha)
+        pools.append(p)
+    plan = L.Plan(T, S, R, K, device=DEV).build(ids)
+    torch.cuda.synchronize()
+    ref = O.lora_linear_sliced(f64(x), [f64(t.W) for t in ts], [f64(t.A) for t in ts], [f64(t.B) for t in ts],
+                               [t.rank for t in ts], [t.alpha for t in ts], ids_np)
+    return x, W, pools, plan, ids_np, ref
+
+
+@pytest.mark.parametrize("d_outs,kernels", [([256, 128, 128], 1), ([256, 136], 1), ([136, 256], 2)])
+def test_sliced_decode_fused(d_outs, kernels):
+    """QKV-like slices, shrink fused in: one GEMM for every slice when no weight
+    tile straddles two slices, else one per slice."""
+    x, W, pools, plan, ids_np, ref = _sliced(60, 64, 512, d_outs, S=9, R=16, ranks=[0, 16, 9, 16, 4, 16, 12, 16, 1])
+    n0 = L.launch_count()
+    y = L.linear_sliced(x, W, d_outs, pools, plan)
+    assert L.launch_count() - n0 == kernels
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    assert_parity(y, ref, f"slices {d_outs}")
+    if kernels == 1:
+        # one launch splits K as the base-only projection of every output does
+        yb = L.linear_sliced(x, W, d_outs)
+        torch.cuda.synchronize()
+        base = np.nonzero(ids_np == 0)[0]
+        assert len(base) > 0
+        for r in base:
+            assert torch.equal(y[int(r)].view(torch.int16), yb[int(r)].view(torch.int16))
+
+
+def test_sliced_decode_shrink_kernel():
+    """(S - 1) * R_max > 128: one shrink kernel and one GEMM per slice."""
+    d_outs = [256, 128]
+    x, W, pools, plan, ids_np, ref = _sliced(70, 48, 512, d_outs, S=20, R=16)
+    n0 = L.launch_count()
+    y = L.linear_sliced(x, W, d_outs, pools, plan)
+    assert L.launch_count() - n0 == 4
+    torch.cuda.synchronize()
+    assert_parity(y, ref, "slices, shrink kernel")
+
+
+def test_sliced_prefill():
+    """The wide kernel, one call per slice, each writing its columns of y."""
+    d_outs = [256, 128, 136]
+    x, W, pools, plan, ids_np, ref = _sliced(80, 300, 256, d_outs, S=12, R=16)
+    y = L.linear_sliced(x, W, d_outs, pools, plan)
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    assert_parity(y, ref, "slices, prefill")
+
+
+def test_sliced_argument_errors():
+    """Pools that do not match their slice, or too many slices, are refused
+    before anything runs."""
+    x, W, pools, plan, ids_np, ref = _sliced(90, 16, 256, [128, 256], S=5, R=16)
+    n0 = L.launch_count()
+    with pytest.raises(L.LoraError):
+        L.linear_sliced(x, W, [128, 256], [pools[1], pools[0]], plan)   # d_out of each pool mismatched
+    with pytest.raises(L.LoraError):
+        L.linear_sliced(x, torch.cat([W] * 3, 0), [128, 256] * 3, pools * 3, plan)   # 6 > LORA_MAX_SLICES
+    assert L.launch_count() == n0

@@ -184,6 +184,66 @@ def test_integer_bruteforce_exact(seed):
             assert Fraction(y[t, n]) == exact[t][n], (t, n)
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_sliced_integer_exact(seed):
+    """Slices with their own adapters, integer inputs: each slice's columns
+    equal the exact integer layer of that slice, in slice order."""
+    rng = np.random.default_rng(300 + seed)
+    T, K, S, R = int(rng.integers(1, 7)), int(rng.integers(1, 13)), 4, 4
+    n_sl = int(rng.integers(1, 4))
+    d_outs = [int(rng.integers(1, 9)) for _ in range(n_sl)]
+    ids = rng.integers(-1, S + 1, size=T)
+    x = rng.integers(-2, 3, size=(T, K))
+    Ws, As, Bs, ranks_l, alphas_l, exact_cols = [], [], [], [], [], []
+    for n in d_outs:
+        ranks = [0] + [int(v) for v in rng.integers(0, R + 1, size=S - 1)]
+        alpha = [0.0] + [float(r * 2.0 ** int(rng.integers(-1, 3))) for r in ranks[1:]]
+        W = rng.integers(-2, 3, size=(n, K))
+        A = np.zeros((S, R, K), dtype=np.int64)
+        B = np.zeros((S, n, R), dtype=np.int64)
+        for s in range(1, S):
+            A[s, :ranks[s]] = rng.integers(-2, 3, size=(ranks[s], K))
+            B[s, :, :ranks[s]] = rng.integers(-2, 3, size=(n, ranks[s]))
+        scales = [Fraction(0)] + [Fraction(alpha[s]) / ranks[s] if ranks[s] else Fraction(0) for s in range(1, S)]
+        exact_cols.append(_exact_int_layer(x.tolist(), W.tolist(), A.tolist(), B.tolist(), ranks, scales, ids.tolist()))
+        Ws.append(W); As.append(A); Bs.append(B); ranks_l.append(ranks); alphas_l.append(alpha)
+    y = O.lora_linear_sliced(x, Ws, As, Bs, ranks_l, alphas_l, ids)
+    assert y.shape == (T, sum(d_outs))
+    off = 0
+    for n, ex in zip(d_outs, exact_cols):
+        for t in range(T):
+            for c in range(n):
+                assert Fraction(y[t, off + c]) == ex[t][c], (t, off + c)
+        off += n
+
+
+def test_sliced_split_of_one_layer():
+    """One adapter layer split by output rows into slices (W and B split, A
+    shared) gives the unsliced layer's columns, in order."""
+    rng = np.random.default_rng(7)
+    T, K, N, S, R = 9, 24, 20, 5, 8
+    x = rng.standard_normal((T, K))
+    W = rng.standard_normal((N, K))
+    A = rng.standard_normal((S, R, K))
+    B = rng.standard_normal((S, N, R))
+    ranks = [0, 8, 3, 5, 8]
+    for s in range(S):
+        A[s, ranks[s]:] = 0
+        B[s, :, ranks[s]:] = 0
+    alpha = [0.0, 16.0, 3.0, 10.0, 8.0]
+    ids = rng.integers(0, S, size=T)
+    cuts = [0, 7, 15, N]
+    parts = list(zip(cuts[:-1], cuts[1:]))
+    y = O.lora_linear_sliced(x, [W[a:b] for a, b in parts], [A] * 3, [B[:, a:b] for a, b in parts],
+                             [ranks] * 3, [alpha] * 3, ids)
+    full = O.lora_linear(x, W, A, B, ranks, alpha, ids)
+    np.testing.assert_allclose(y, full, rtol=1e-12, atol=1e-12)
+    # swapping two slices' inputs moves their columns
+    y_sw = O.lora_linear_sliced(x, [W[7:15], W[0:7]], [A, A], [B[:, 7:15], B[:, 0:7]], [ranks] * 2, [alpha] * 2, ids)
+    np.testing.assert_allclose(y_sw[:, :8], full[:, 7:15], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y_sw[:, 8:], full[:, 0:7], rtol=1e-12, atol=1e-12)
+
+
 def test_transposed_or_dropped_terms_are_caught():
     """The integer pin distinguishes the plausible slips: a transposed B, a
     dropped scale, a rank-padded scale, a wrong sign."""
