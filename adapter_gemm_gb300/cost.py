@@ -88,3 +88,15 @@ def roofline_time(w: Work, peak_tflops: float, peak_gbs: float) -> tuple[float, 
     t_c = w.flops / (peak_tflops * 1e12)
     t_m = w.bytes / (peak_gbs * 1e9)
     return (t_c, "tensor") if t_c >= t_m else (t_m, "hbm")
+
+
+def sliced_layer(T: int, d_in: int, d_outs, ids, ranks_list) -> Work:
+    """Projections that share x: each slice's layer, with x read once."""
+    ws = [layer(T, d_in, n, ids, r) for n, r in zip(d_outs, ranks_list)]
+    return Work(sum(w.flops for w in ws), sum(w.bytes for w in ws) - 2.0 * T * d_in * (len(ws) - 1))
+
+
+def sliced_gemm_kernel(T: int, d_in: int, d_outs, ids=None, ranks_list=None) -> Work:
+    """The GEMM over every slice, with x read once."""
+    ws = [gemm_kernel(T, d_in, n, ids, r) for n, r in zip(d_outs, ranks_list or [None] * len(d_outs))]
+    return Work(sum(w.flops for w in ws), sum(w.bytes for w in ws) - 2.0 * T * d_in * (len(ws) - 1))

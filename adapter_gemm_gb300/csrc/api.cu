@@ -766,15 +766,22 @@ lora_status lora_linear_sliced(const void* x, const void* W, int T, int d_in, in
         }
         return linear_impl(x, W, T, d_in, N, pools[0], plan, y, N, &set, stream);
     }
+    // With the profiling hook on, one pair of events brackets every kernel of
+    // the per-slice calls.
+    cudaEvent_t p0 = g_prof_start, p1 = g_prof_stop;
+    g_prof_start = g_prof_stop = nullptr;
+    lora_status r = LORA_OK;
+    if (p0 && p1 && cudaEventRecord(p0, st) != cudaSuccess) r = LORA_ECUDA;
     int off = 0;
-    for (int q = 0; q < n_slices; ++q) {
-        const lora_status r = linear_impl(x, static_cast<const __nv_bfloat16*>(W) + (size_t)off * d_in, T, d_in,
-                                          d_outs[q], pools[q], plan, static_cast<__nv_bfloat16*>(y) + off, N,
-                                          nullptr, stream);
-        if (r != LORA_OK) return r;
+    for (int q = 0; q < n_slices && r == LORA_OK; ++q) {
+        r = linear_impl(x, static_cast<const __nv_bfloat16*>(W) + (size_t)off * d_in, T, d_in, d_outs[q], pools[q],
+                        plan, static_cast<__nv_bfloat16*>(y) + off, N, nullptr, stream);
         off += d_outs[q];
     }
-    return LORA_OK;
+    if (r == LORA_OK && p0 && p1 && cudaEventRecord(p1, st) != cudaSuccess) r = LORA_ECUDA;
+    g_prof_start = p0;
+    g_prof_stop = p1;
+    return r;
 }
 
 lora_status lora_profile_gemm_events(void* start, void* stop) {

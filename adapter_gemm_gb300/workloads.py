@@ -10,9 +10,11 @@ rerankers, pooling", symbols paragraph), rank-16 adapters with alpha = 32,
 x ~ N(0, 1), W, A, B ~ N(0, 0.02) drawn in fp32 and rounded to bf16 (round to
 nearest even). Slot 0 is the zero adapter; it is never given weights.
 
-Five workloads:
+Workloads:
   tiny          T=64,  256->256,     slots 1-3 rank 8, alpha 16, ids uniform {0..3}
   q_decode      T=64,  4096->4096,   8 adapters r16, 8 contiguous rows each
+  qkv_decode    q_decode's batch over the q/k/v projections (4096 -> 4096 +
+                1024 + 1024) as one call over three output slices
   gateup_prefill T=4096, 4096->14336, 16 adapters r16, power-law (1.1) segment
                 lengths by largest remainder, 10 % of rows on slot 0, contiguous
                 segments in a seeded order
@@ -20,7 +22,8 @@ Five workloads:
                 i.i.d.: 25 % slot 0, else truncated power law (1.2), interleaved
   layer_sweep   the seven Llama-3-8B targets, 50 resident adapters r16 per
                 target, T in {1,8,64,512,4096}, ids i.i.d.: 10 % slot 0 else
-                uniform over 1..50
+                uniform over 1..50; layer_sweep_sliced runs q/k/v and gate/up
+                as one call each
 """
 from __future__ import annotations
 
@@ -66,6 +69,21 @@ class Workload:
     ids: np.ndarray            # [T] int32 token slot ids
     x: torch.Tensor            # [T, d_in] bf16 (d_in of the first target)
     targets: list = field(default_factory=list)
+    # targets that share their input and run as one call over output slices
+    # (tuples of target indices); every other target runs on its own
+    groups: list = field(default_factory=list)
+
+    def units(self) -> list:
+        """The calls of one step, in target order: tuples of target indices."""
+        grouped = {i: g for g in self.groups for i in g}
+        out, seen = [], set()
+        for i in range(len(self.targets)):
+            if i in seen:
+                continue
+            g = tuple(grouped.get(i, (i,)))
+            seen.update(g)
+            out.append(g)
+        return out
 
     @property
     def d_in(self) -> int:
@@ -149,6 +167,21 @@ def q_decode(seed: int = 1002) -> Workload:
     return Workload("q_decode", T, S, r, ids, x, [t])
 
 
+def qkv_decode(seed: int = 1005) -> Workload:
+    """The query, key and value projections of one decode step as one call over
+    three output slices (4096 + 1024 + 1024), with q_decode's batch: T=64, 8
+    adapters of rank 16, 8 contiguous rows each; each slice has its own
+    adapter factors."""
+    T, K, S, r = 64, 4096, 9, 16
+    streams = _streams(seed, 5)
+    g_x = streams[1]
+    ids = np.repeat(np.arange(1, S, dtype=np.int32), T // (S - 1))
+    x = to_bf16(_normal(g_x, (T, K), 1.0))
+    tl = [make_target(g, name, K, n, [0] + [r] * (S - 1), [0.0] + [32.0] * (S - 1), r)
+          for (name, _, n), g in zip(LLAMA3_8B_TARGETS[:3], streams[2:])]
+    return Workload("qkv_decode", T, S, r, ids, x, tl, groups=[(0, 1, 2)])
+
+
 def gateup_ids(rng: np.random.Generator, T: int = 4096, n_adapters: int = 16,
                base_frac: float = 0.1, power: float = 1.1) -> np.ndarray:
     n0 = int(round(base_frac * T))
@@ -190,10 +223,11 @@ def sweep_ids(rng: np.random.Generator, T: int, n_adapters: int = 50,
     return np.where(base, 0, pick).astype(np.int32)
 
 
-def layer_sweep(T: int, seed: int | None = None, targets=LLAMA3_8B_TARGETS) -> Workload:
+def layer_sweep(T: int, seed: int | None = None, targets=LLAMA3_8B_TARGETS, sliced: bool = False) -> Workload:
     """All seven targets of one decoder layer share the step's ids. x is drawn
     for d_in = 4096; the down projection gets its own [T, 14336] input, stored
-    on that target as `x_in` (use `input_for`)."""
+    on that target as `x_in` (use `input_for`). With `sliced`, q/k/v and
+    gate/up run as one call each over their output slices."""
     seed = 5000 + T if seed is None else seed
     S, r = 51, 16
     streams = _streams(seed, 3 + len(targets))
@@ -209,6 +243,8 @@ def layer_sweep(T: int, seed: int | None = None, targets=LLAMA3_8B_TARGETS) -> W
                 x_ffn = to_bf16(_normal(g_x2, (T, k), 1.0))
             t.x_in = x_ffn
         tl.append(t)
+    if sliced:
+        return Workload(f"layer_sweep_sliced_T{T}", T, S, r, ids, x, tl, groups=[(0, 1, 2), (4, 5)])
     return Workload(f"layer_sweep_T{T}", T, S, r, ids, x, tl)
 
 
@@ -225,6 +261,10 @@ def by_name(name: str) -> Workload:
         return gateup_prefill()
     if name == "mixed_down":
         return mixed_down()
+    if name == "qkv_decode":
+        return qkv_decode()
+    if name.startswith("layer_sweep_sliced_T"):
+        return layer_sweep(int(name[len("layer_sweep_sliced_T"):]), sliced=True)
     if name.startswith("layer_sweep_T"):
         return layer_sweep(int(name[len("layer_sweep_T"):]))
     raise KeyError(name)

@@ -257,32 +257,51 @@ def main():
         k = id(WL.input_for(w, t))
         if k not in xs:
             xs[k] = WL.input_for(w, t).to(dev)
-    x_of = [xs[id(WL.input_for(w, t))] for t in w.targets]
     ids = torch.from_numpy(w.ids).to(dev)
-    base_targets = []
-    for t in w.targets:
-        W = t.W.to(dev)
-        pool = L.Pool(w.S, w.R_max, t.d_in, t.d_out, device=dev)
-        pool.load_padded(t.A, t.B, t.rank, t.alpha)
-        base_targets.append((W, pool))
-    copies = [base_targets]
+    # The step's calls: a target on its own, or targets that share x as one
+    # call over their output slices (W stacked by rows, one pool per slice).
+    units = w.units()
+    u_name = ["+".join(w.targets[i].name for i in u) for u in units]
+    u_dout = [[w.targets[i].d_out for i in u] for u in units]
+    u_key = [id(WL.input_for(w, w.targets[u[0]])) for u in units]
+    x_of = [xs[k] for k in u_key]
+    base_units = []
+    for u in units:
+        W = torch.cat([w.targets[i].W for i in u], 0).to(dev)
+        pools = []
+        for i in u:
+            t = w.targets[i]
+            pool = L.Pool(w.S, w.R_max, t.d_in, t.d_out, device=dev)
+            pool.load_padded(t.A, t.B, t.rank, t.alpha)
+            pools.append(pool)
+        base_units.append((W, pools))
+    copies = [base_units]
     for _ in range(n_copies - 1):
         c = []
-        for (W, pool) in base_targets:
-            p2 = L.Pool(w.S, w.R_max, pool.d_in, pool.d_out, device=dev)
-            p2.A.copy_(pool.A); p2.B.copy_(pool.B); p2.scale.copy_(pool.scale); p2.rank.copy_(pool.rank)
-            c.append((W.clone(), p2))
+        for (W, pools) in base_units:
+            p2s = []
+            for pool in pools:
+                p2 = L.Pool(w.S, w.R_max, pool.d_in, pool.d_out, device=dev)
+                p2.A.copy_(pool.A); p2.B.copy_(pool.B); p2.scale.copy_(pool.scale); p2.rank.copy_(pool.rank)
+                p2s.append(p2)
+            c.append((W.clone(), p2s))
         copies.append(c)
     d_cap = max(t.d_in for t in w.targets)
     plans = [L.Plan(T, w.S, w.R_max, d_cap, device=dev) for _ in range(n_copies)]
-    ys = [torch.empty((T, t.d_out), dtype=torch.bfloat16, device=dev) for t in w.targets]
+    ys = [torch.empty((T, sum(d)), dtype=torch.bfloat16, device=dev) for d in u_dout]
     torch.cuda.synchronize()
+
+    def call(j, x, W, pools, plan, y):
+        if len(pools) == 1:
+            L.linear(x, W, pools[0], plan, y)
+        else:
+            L.linear_sliced(x, W, u_dout[j], pools, plan, y)
 
     def step(i):
         c = i % n_copies
         plans[c].build(ids)
-        for j, (W, pool) in enumerate(copies[c]):
-            L.linear(x_of[j], W, pool, plans[c], ys[j])
+        for j, (W, pools) in enumerate(copies[c]):
+            call(j, x_of[j], W, pools, plans[c], ys[j])
 
 
     # ---- warmup (eager), then CUDA graphs: one holding a run of G steps (the
@@ -294,6 +313,11 @@ def main():
     n0 = L.launch_count()
     step(0)
     launches_per_step = L.launch_count() - n0       # the library's own kernels in one step
+    u_launch = []                                   # kernels of each call (the plan excluded)
+    for j, (W, pools) in enumerate(copies[0]):
+        n0 = L.launch_count()
+        call(j, x_of[j], W, pools, plans[0], ys[j])
+        u_launch.append(L.launch_count() - n0)
     torch.cuda.synchronize()
     use_graph = not args.no_graph
     G = n_copies * max(1, -(-16 // n_copies))
@@ -360,10 +384,10 @@ def main():
     # intervals hold GPU time only; a chunk whose sleep ended before the host
     # finished queueing is redone with a longer sleep.
     ksteps = max(10, min(args.kernel_steps, args.steps))
-    per_target_ms = np.zeros(len(w.targets))
-    nt = len(w.targets)
+    nt = len(units)
+    per_target_ms = np.zeros(nt)
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in w.targets] for _ in range(ksteps)]
+            for _ in units] for _ in range(ksteps)]
     for row in evs:            # torch times only events it has recorded once itself;
         for a, b in row:       # the library's later records on the same handles win
             a.record()
@@ -381,10 +405,10 @@ def main():
         for i in range(i0, i0 + n_ch):
             c = i % n_copies
             plans[c].build(ids)
-            for j, (W, pool) in enumerate(copies[c]):
+            for j, (W, pools) in enumerate(copies[c]):
                 a, b = evs[i][j]
                 L.profile_gemm_events(a, b)
-                L.linear(x_of[j], W, pool, plans[c], ys[j])
+                call(j, x_of[j], W, pools, plans[c], ys[j])
         L.profile_gemm_events(None, None)
         if slept.query():                 # the GPU caught up with the host
             starved_chunks += 1
@@ -400,9 +424,10 @@ def main():
             per_target_ms[j] += a.elapsed_time(b)
     per_target_ms /= ksteps
     jdom = int(np.argmax(per_target_ms))
-    td = w.targets[jdom]
+    td = w.targets[units[jdom][0]]
+    d_in_dom, n_dom = td.d_in, sum(u_dout[jdom])
     hbm, tf_burst, tf_sus, src = peaks()
-    gw = cost.gemm_kernel(T, td.d_in, td.d_out, w.ids, td.rank)
+    gw = cost.sliced_gemm_kernel(T, td.d_in, u_dout[jdom], w.ids, [w.targets[i].rank for i in units[jdom]])
     t_k = per_target_ms[jdom] / 1e3
     _, bound = cost.roofline_time(gw, tf_sus, hbm)
     if bound == "hbm":
@@ -413,17 +438,19 @@ def main():
         peak, unit = tf_sus, "TFLOP/s"
     roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.config),
-            "kernel": "gemm_skinny_kernel" if L.linear_path(T, td.d_in, td.d_out) == 0 else "gemm_wide_kernel",
-            "target": td.name, "kernel_us": round(t_k * 1e6, 3),
-            "per_target_us": {t.name: round(v * 1e3, 3) for t, v in zip(w.targets, per_target_ms)},
+            "kernel": ("gemm_skinny_kernel" if L.linear_path(T, d_in_dom, n_dom) == 0 else "gemm_wide_kernel")
+                      if len(units[jdom]) == 1 or u_launch[jdom] == 1
+                      else f"all {u_launch[jdom]} kernels of the per-slice calls",
+            "target": u_name[jdom], "kernel_us": round(t_k * 1e6, 3),
+            "per_target_us": {nm: round(v * 1e3, 3) for nm, v in zip(u_name, per_target_ms)},
             "timing": "events around each launch, queued behind a sleep kernel (no host gaps, no overlap)",
             "starved_chunks_redone": starved_chunks,
             "algorithmic_bytes": gw.bytes, "algorithmic_flops": gw.flops,
             "peak_source": f"{src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops_sustained'})"}
     # whole-step roofline (all targets, every kernel): the layer's fraction
     t_roof = 0.0
-    for t in w.targets:
-        lw = cost.layer(T, t.d_in, t.d_out, w.ids, t.rank)
+    for u, d in zip(units, u_dout):
+        lw = cost.sliced_layer(T, w.targets[u[0]].d_in, d, w.ids, [w.targets[i].rank for i in u])
         t_roof += cost.roofline_time(lw, tf_sus, hbm)[0]
     step_frac = t_roof / (ms_per_step / 1e3)
 
@@ -435,16 +462,14 @@ def main():
     hy = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
     dx = {k: torch.empty_like(v) for k, v in xs.items()}
     dids = torch.empty_like(ids)
-    keys = [id(WL.input_for(w, t)) for t in w.targets]
-
     def e2e_step(i):
         c = i % n_copies
         for k in hx:
             dx[k].copy_(hx[k], non_blocking=True)
         dids.copy_(hids, non_blocking=True)
         plans[c].build(dids)
-        for j, (W, pool) in enumerate(copies[c]):
-            L.linear(dx[keys[j]], W, pool, plans[c], ys[j])
+        for j, (W, pools) in enumerate(copies[c]):
+            call(j, dx[u_key[j]], W, pools, plans[c], ys[j])
             hy[j].copy_(ys[j], non_blocking=True)
 
     for i in range(3):
@@ -486,12 +511,14 @@ def main():
         cpu = {"value": round(v, 2), "unit": "tokens/s", "cores": int(cores), "kind": "oracle", "sample": sample}
 
     total_flops = sum(cost.layer(T, t.d_in, t.d_out, w.ids, t.rank).flops for t in w.targets)
+    groups = [u_name[j] for j, u in enumerate(units) if len(u) > 1]
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; random-init weights and adapters)",
         "config": {"workload": w.name, "T": T, "targets": [[t.name, t.d_in, t.d_out] for t in w.targets],
+                   "sliced_calls": groups,
                    "slots": w.S, "R_max": w.R_max, "parallelism": f"replicas x{world}",
                    "l2": f"{n_copies} rotating weight/pool copies ({n_copies * per_copy / 2**20:.0f} MiB > 2x L2)",
                    "launch": f"CUDA graphs of {G} steps" if use_graph else "eager"},

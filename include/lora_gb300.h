@@ -213,8 +213,10 @@ lora_status lora_linear_sliced(const void* x, const void* W, int T, int d_in, in
 /* Profiling hook: when both are non-NULL cudaEvent_t handles, every following
  * lora_linear records `start` on its stream right before it launches the GEMM
  * kernel and `stop` right after it, so the caller can time that kernel alone
- * with cudaEventElapsedTime. (NULL, NULL) turns it off. Process-global; not
- * for use while a stream is being captured. */
+ * with cudaEventElapsedTime. A lora_linear_sliced that runs as one call per
+ * slice records the pair around all of those calls' kernels instead.
+ * (NULL, NULL) turns it off. Process-global; not for use while a stream is
+ * being captured. */
 lora_status lora_profile_gemm_events(void* start, void* stop);
 
 /* The layer for callers that cannot allocate device memory (no counterpart on
