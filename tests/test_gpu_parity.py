@@ -412,6 +412,43 @@ def test_tensor_core_expand_with_ids_from_previous_output():
     assert_parity(y, ref, "shrink kernel, tensor-core expand")
 
 
+FUSED_EDGES = [
+    # T, K, N, S, R_max: every adapter slot's ranks (rounded up to 16) fit 128 pairs
+    (64, 256, 256, 2, 128),      # one slot of rank 128: eight chunks of pairs
+    (64, 256, 256, 9, 8),        # rank 8 < 16: pad positions of every slot stay zero
+    (16, 192, 136, 5, 24),       # R16 = 32; three K slices; a ragged weight tile
+    (1, 64, 8, 3, 16),           # one row, one K slice, eight outputs
+    (63, 4160, 264, 3, 64),      # 65 K slices; T one short of a full tile
+]
+
+
+@pytest.mark.parametrize("T,K,N,S,R", FUSED_EDGES)
+def test_fused_shrink_edge_shapes(T, K, N, S, R):
+    w = WL.random_case(seed=T * 13 + K + S, T=T, K=K, N=N, S=S, R_max=R)
+    dw = DeviceWorkload(w, DEV)
+    n0 = L.launch_count()
+    y = dw.run(0)
+    assert L.launch_count() - n0 == 1                    # the shrink is fused in
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    assert_parity(y, dw.oracle(0), f"fused {T},{K},{N},{S},{R}")
+    slot0 = torch.as_tensor(w.ids == 0, device=DEV)
+    yb = dw.run(0, base_only=True)
+    assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [64, 300])
+def test_most_slots(T):
+    """S = 1024 slots, ids over all of them: the decode path's CUDA-core expand
+    and the prefill path's segment lists."""
+    w = WL.random_case(seed=1024 + T, T=T, K=128, N=136, S=1024, R_max=8, base_frac=0.05)
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    assert_parity(y, dw.oracle(0), f"S=1024, T={T}")
+
+
 def test_shrink_kernel_when_pool_exceeds_one_tile():
     """(S - 1) * R_max > 128: U comes from the shrink kernel ahead of the GEMM."""
     w = WL.random_case(seed=22, T=48, K=512, N=384, S=10, R_max=16)
