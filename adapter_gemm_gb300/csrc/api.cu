@@ -723,6 +723,31 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     return linear_impl(x, W, T, d_in, d_out, pool, plan, y, d_out, nullptr, stream);
 }
 
+lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* y_host, int T, int d_in,
+                             int d_out, const void* W, const lora_pool* pool, lora_plan_t* plan,
+                             void* x_dev, int32_t* ids_dev, void* y_dev, void* stream) {
+    if (T < 0 || d_in < 8 || d_out < 8) return LORA_EINVAL;
+    if ((d_in % 8) != 0 || (d_out % 8) != 0) return LORA_ESHAPE;
+    if (T == 0) return LORA_OK;
+    if (!x_host || !y_host || !x_dev || !y_dev || !W) return LORA_EINVAL;
+    if (plan && (!ids_host || !ids_dev || !aligned16(ids_dev))) return LORA_EINVAL;
+    if (!aligned16(x_dev) || !aligned16(y_dev)) return LORA_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(x_dev, x_host, (size_t)T * d_in * 2, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return LORA_ECUDA;
+    if (plan) {
+        if (cudaMemcpyAsync(ids_dev, ids_host, (size_t)T * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return LORA_ECUDA;
+        const lora_status r = lora_plan(ids_dev, T, plan, stream);
+        if (r != LORA_OK) return r;
+    }
+    const lora_status r = lora_linear(x_dev, W, T, d_in, d_out, plan ? pool : nullptr, plan, y_dev, stream);
+    if (r != LORA_OK) return r;
+    if (cudaMemcpyAsync(y_host, y_dev, (size_t)T * d_out * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return LORA_ECUDA;
+    return LORA_OK;
+}
+
 lora_status lora_linear_sliced(const void* x, const void* W, int T, int d_in, int n_slices, const int32_t* d_outs,
                                const lora_pool* const* pools, const lora_plan_t* plan, void* y, void* stream) {
     if (T < 0 || d_in < 8 || n_slices < 1 || n_slices > LORA_MAX_SLICES || !d_outs) return LORA_EINVAL;

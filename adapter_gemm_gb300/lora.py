@@ -65,6 +65,9 @@ _SIGS = {
     "lora_linear": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(lora_pool),
                              ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p]),
     "lora_linear_path": (_c_int, [_c_int, _c_int, _c_int]),
+    "lora_linear_host": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
+                                  ctypes.POINTER(lora_pool), ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p,
+                                  _c_void_p, _c_void_p]),
     "lora_linear_sliced": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(_c_int32),
                                     ctypes.POINTER(ctypes.POINTER(lora_pool)), ctypes.POINTER(lora_plan_t),
                                     _c_void_p, _c_void_p]),
@@ -249,6 +252,37 @@ def linear(x: torch.Tensor, W: torch.Tensor, pool: Pool | None = None, plan: Pla
                               ctypes.byref(plan.c) if plan is not None else None,
                               _ptr(y, torch.bfloat16, "y"), _stream(stream)), "lora_linear")
     return y
+
+
+def linear_host(x_host: torch.Tensor, W: torch.Tensor, y_host: torch.Tensor, x_dev: torch.Tensor,
+                y_dev: torch.Tensor, pool: Pool | None = None, plan: Plan | None = None,
+                ids_host: torch.Tensor | None = None, ids_dev: torch.Tensor | None = None, stream=None):
+    """The layer on host buffers (pinned CPU tensors x_host [T, d_in], y_host
+    [T, d_out], ids_host [T] int32): copies in, plan, layer, copy out, all
+    queued on the stream, through the device staging tensors x_dev, ids_dev,
+    y_dev."""
+    if x_host.device.type != "cpu" or y_host.device.type != "cpu":
+        raise ValueError("x_host and y_host must be host tensors")
+    T, d_in = x_host.shape
+    d_out = W.shape[0]
+    if plan is not None:
+        if pool is None or ids_host is None or ids_dev is None:
+            raise ValueError("a plan needs a pool, ids_host and ids_dev")
+        if ids_host.dtype != torch.int32 or not ids_host.is_contiguous():
+            raise ValueError("ids_host must be contiguous int32")
+        plan.ids = ids_dev
+    for nm, t, dt in (("x_host", x_host, torch.bfloat16), ("y_host", y_host, torch.bfloat16)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{nm} must be contiguous {dt}")
+    _check(_lib().lora_linear_host(_c_void_p(x_host.data_ptr()),
+                                   _c_void_p(ids_host.data_ptr()) if plan is not None else None,
+                                   _c_void_p(y_host.data_ptr()), T, d_in, d_out, _ptr(W, torch.bfloat16, "W"),
+                                   ctypes.byref(pool.c) if plan is not None else None,
+                                   ctypes.byref(plan.c) if plan is not None else None,
+                                   _ptr(x_dev, torch.bfloat16, "x_dev"),
+                                   _ptr(ids_dev, torch.int32, "ids_dev") if plan is not None else None,
+                                   _ptr(y_dev, torch.bfloat16, "y_dev"), _stream(stream)), "lora_linear_host")
+    return y_host
 
 
 def linear_sliced(x: torch.Tensor, W: torch.Tensor, d_outs, pools=None, plan: Plan | None = None,

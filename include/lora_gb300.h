@@ -174,6 +174,24 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
                         const lora_pool* pool, const lora_plan_t* plan, void* y,
                         void* stream);
 
+/* The layer on host buffers, for callers whose step inputs and outputs live in
+ * host memory. On `stream`:
+ *   1. copy x_host ([T, d_in] bf16) into x_dev;
+ *   2. with a plan, copy ids_host ([T] int32) into ids_dev and build the plan;
+ *   3. run lora_linear(x_dev, ..., y_dev);
+ *   4. copy y_dev ([T, d_out] bf16) back to y_host.
+ * x_dev, ids_dev and y_dev are the caller's device staging buffers (16-byte
+ * aligned); the host buffers should be pinned (cudaHostAlloc or
+ * cudaHostRegister) for the copies to be asynchronous. Asynchronous:
+ * y_host holds the result once `stream` reaches the end of this call. Calls on
+ * two streams, each with its own staging buffers and plan, overlap one call's
+ * copies with the other's kernels. plan == NULL runs the base projection
+ * (pool, ids_host and ids_dev ignored). Arguments otherwise as for lora_plan
+ * and lora_linear; LORA_EINVAL for missing buffers, before anything is queued. */
+lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* y_host, int T, int d_in,
+                             int d_out, const void* W, const lora_pool* pool, lora_plan_t* plan,
+                             void* x_dev, int32_t* ids_dev, void* y_dev, void* stream);
+
 /* The kernel family lora_linear picks for these sizes: 0 = skinny (swap-AB,
  * split-K across a thread-block cluster), 1 = wide (persistent 128x256 tiles). */
 int lora_linear_path(int T, int d_in, int d_out);

@@ -135,6 +135,33 @@ def test_linear_argument_errors(lib):
     assert lib.lora_linear(x, W, 300, 8192, 4096, ctypes.byref(pl4), ctypes.byref(q), y, None) == ESHAPE
 
 
+def test_sliced_and_host_argument_errors(lib):
+    """lora_linear_sliced and lora_linear_host refuse bad arguments before they
+    queue anything."""
+    x = W = y = FAKE
+    d = (ctypes.c_int32 * 5)(128, 128, 128, 128, 128)
+    assert lib.lora_linear_sliced(x, W, 64, 4096, 0, d, None, None, y, None) == EINVAL
+    assert lib.lora_linear_sliced(x, W, 64, 4096, 5, d, None, None, y, None) == EINVAL      # > LORA_MAX_SLICES
+    bad = (ctypes.c_int32 * 2)(128, 100)
+    assert lib.lora_linear_sliced(x, W, 64, 4096, 2, bad, None, None, y, None) == ESHAPE
+    assert lib.lora_linear_sliced(x, W, 0, 4096, 2, d, None, None, y, None) == OK           # empty batch
+    p = L.lora_plan_t()
+    n = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)
+    assert lib.lora_plan_init(ctypes.byref(p), FAKE, n, 64, 9, 16, 4096) == OK
+    assert lib.lora_linear_sliced(x, W, 64, 4096, 2, d, None, ctypes.byref(p), y, None) == EINVAL  # no pools
+    pl = _pool(S=9, R=16, K=4096, N=256)
+    pools = (ctypes.POINTER(L.lora_pool) * 2)(ctypes.pointer(pl), ctypes.pointer(pl))
+    assert lib.lora_linear_sliced(x, W, 64, 4096, 2, d, pools, ctypes.byref(p), y, None) == ESHAPE  # d_out 256 != 128
+    h = ctypes.c_void_p(4096)
+    assert lib.lora_linear_host(None, None, h, 64, 4096, 4096, W, None, None, x, None, y, None) == EINVAL
+    assert lib.lora_linear_host(h, None, None, 64, 4096, 4096, W, None, None, x, None, y, None) == EINVAL
+    assert lib.lora_linear_host(h, None, h, 64, 4096, 4096, W, None, None, None, None, y, None) == EINVAL
+    assert lib.lora_linear_host(h, None, h, 64, 4096, 4095, W, None, None, x, None, y, None) == ESHAPE
+    assert lib.lora_linear_host(h, None, h, 64, 4096, 4096, W, ctypes.byref(pl), ctypes.byref(p), x, None, y,
+                                None) == EINVAL                                               # ids buffers missing
+    assert lib.lora_linear_host(h, None, h, 0, 4096, 4096, W, None, None, x, None, y, None) == OK
+
+
 def test_plan_argument_errors(lib):
     p = L.lora_plan_t()
     n = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)

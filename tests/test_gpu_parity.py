@@ -532,3 +532,60 @@ def test_sliced_argument_errors():
     with pytest.raises(L.LoraError):
         L.linear_sliced(x, torch.cat([W] * 3, 0), [128, 256] * 3, pools * 3, plan)   # 6 > LORA_MAX_SLICES
     assert L.launch_count() == n0
+
+
+# ------------------------------------------------------------ host buffers ----
+
+def test_host_buffers_match_device_call():
+    """lora_linear_host (copies in, plan, layer, copy out) gives the device
+    call's bits, with and without a plan."""
+    w = WL.random_case(seed=95, T=64, K=1024, N=384, S=9, R_max=16)
+    dw = DeviceWorkload(w, DEV)
+    t = dw.targets[0]
+    y_dev_ref = dw.run(0)
+    yb_ref = dw.run(0, base_only=True)
+    x_h = w.x.contiguous().pin_memory()
+    ids_h = torch.from_numpy(w.ids.astype(np.int32)).pin_memory()
+    y_h = torch.empty((64, 384), dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty((64, 1024), dtype=torch.bfloat16, device=DEV)
+    ids_d = torch.empty(64, dtype=torch.int32, device=DEV)
+    y_d = torch.empty((64, 384), dtype=torch.bfloat16, device=DEV)
+    plan = L.Plan(64, w.S, w.R_max, 1024, device=DEV)
+    L.linear_host(x_h, t.W, y_h, x_d, y_d, t.pool, plan, ids_h, ids_d)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h.view(torch.int16), y_dev_ref.cpu().view(torch.int16))
+    L.linear_host(x_h, t.W, y_h, x_d, y_d)
+    torch.cuda.synchronize()
+    assert torch.equal(y_h.view(torch.int16), yb_ref.cpu().view(torch.int16))
+
+
+def test_host_buffers_two_streams_without_sync():
+    """Steps alternate between two streams, each with its own staging buffers
+    and plan, with no synchronisation in between: every step's output is
+    right."""
+    T, K, N, S, R = 48, 512, 256, 9, 16
+    w = WL.random_case(seed=96, T=T, K=K, N=N, S=S, R_max=R)
+    t = w.targets[0]
+    W = t.W.to(DEV)
+    pool = L.Pool(S, R, K, N, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    rng = np.random.default_rng(97)
+    n_steps = 6
+    xs = [torch.from_numpy(rng.standard_normal((T, K), dtype=np.float32)).to(torch.bfloat16).pin_memory()
+          for _ in range(n_steps)]
+    idss = [torch.from_numpy(rng.integers(0, S, size=T).astype(np.int32)).pin_memory() for _ in range(n_steps)]
+    ys = [torch.empty((T, N), dtype=torch.bfloat16).pin_memory() for _ in range(n_steps)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    stage = [dict(x=torch.empty((T, K), dtype=torch.bfloat16, device=DEV),
+                  ids=torch.empty(T, dtype=torch.int32, device=DEV),
+                  y=torch.empty((T, N), dtype=torch.bfloat16, device=DEV),
+                  plan=L.Plan(T, S, R, K, device=DEV)) for _ in range(2)]
+    torch.cuda.synchronize()
+    for k in range(n_steps):
+        b, st = stage[k % 2], streams[k % 2]
+        L.linear_host(xs[k], W, ys[k], b["x"], b["y"], pool, b["plan"], idss[k], b["ids"], stream=st)
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    for k in range(n_steps):
+        ref = O.lora_linear(f64(xs[k]), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, idss[k].numpy())
+        assert_parity(ys[k], ref, f"step {k}")
