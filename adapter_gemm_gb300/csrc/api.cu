@@ -723,6 +723,26 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
     return linear_impl(x, W, T, d_in, d_out, pool, plan, y, d_out, nullptr, stream);
 }
 
+lora_status lora_linear_rows(const void* x_all, int T_all, const int32_t* rows, int T, int d_in, int d_out,
+                             const void* W, const lora_pool* pool, const lora_plan_t* plan, void* x_rows, void* y,
+                             void* stream) {
+    if (T < 0 || T_all < 0 || d_in < 8 || d_out < 8) return LORA_EINVAL;
+    if ((d_in % 8) != 0 || (d_out % 8) != 0) return LORA_ESHAPE;
+    if (T == 0) return LORA_OK;
+    if (!x_all || !rows || !x_rows || !y || !W) return LORA_EINVAL;
+    if (!aligned16(x_all) || !aligned16(x_rows)) return LORA_EINVAL;
+    if (plan) {
+        if (!pool || !pool->A || !pool->B || !pool->rank || !pool->scale) return LORA_EINVAL;
+        if (!pool_valid(pool, plan, T, d_in, d_out)) return (!aligned16(pool->A) || !aligned16(pool->B)) ? LORA_EINVAL
+                                                                                                         : LORA_ESHAPE;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (counted(launch_gather_rows(static_cast<const __nv_bfloat16*>(x_all), rows, T, T_all, d_in,
+                                   static_cast<__nv_bfloat16*>(x_rows), st)) != cudaSuccess)
+        return LORA_ECUDA;
+    return lora_linear(x_rows, W, T, d_in, d_out, pool, plan, y, stream);
+}
+
 lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* y_host, int T, int d_in,
                              int d_out, const void* W, const lora_pool* pool, lora_plan_t* plan,
                              void* x_dev, int32_t* ids_dev, void* y_dev, void* stream) {

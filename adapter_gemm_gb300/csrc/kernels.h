@@ -117,6 +117,8 @@ cudaError_t launch_skinny(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl,
 cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
                         const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
 cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* rows, int T, int T_all, int d_in,
+                               __nv_bfloat16* out, cudaStream_t stream);
 
 // Read and clear the bounded-wait error words of the GEMM translation units.
 cudaError_t skinny_take_error(int* code);

@@ -329,6 +329,28 @@ cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pd
 }
 
 // Count bf16 words that encode Inf or NaN (exponent bits all ones).
+// x_rows[i, :] = x[rows[i], :] for i < T, 16 bytes per thread step; an index
+// outside [0, T_all) gives a zero row.
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ rows, int T, int T_all,
+                                   int chunks_per_row, uint4* __restrict__ out) {
+    const size_t n = (size_t)T * chunks_per_row;
+    for (size_t q = (size_t)blockIdx.x * blockDim.x + threadIdx.x; q < n; q += (size_t)gridDim.x * blockDim.x) {
+        const int i = (int)(q / chunks_per_row), c = (int)(q - (size_t)i * chunks_per_row);
+        const int r = rows[i];
+        out[q] = (r >= 0 && r < T_all) ? x[(size_t)r * chunks_per_row + c] : make_uint4(0, 0, 0, 0);
+    }
+}
+
+cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* rows, int T, int T_all, int d_in,
+                               __nv_bfloat16* out, cudaStream_t stream) {
+    const int cpr = d_in / 8;
+    const size_t n = (size_t)T * cpr;
+    const unsigned blocks = (unsigned)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+    gather_rows_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(x), rows, T, T_all, cpr,
+                                                     reinterpret_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
 __global__ void count_nonfinite_kernel(const uint16_t* __restrict__ p, size_t n, int32_t* out) {
     int cnt = 0;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)

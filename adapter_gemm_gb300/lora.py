@@ -65,6 +65,9 @@ _SIGS = {
     "lora_linear": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(lora_pool),
                              ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p]),
     "lora_linear_path": (_c_int, [_c_int, _c_int, _c_int]),
+    "lora_linear_rows": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
+                                  ctypes.POINTER(lora_pool), ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p,
+                                  _c_void_p]),
     "lora_linear_host": (_c_int, [_c_void_p, _c_void_p, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
                                   ctypes.POINTER(lora_pool), ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p,
                                   _c_void_p, _c_void_p]),
@@ -251,6 +254,29 @@ def linear(x: torch.Tensor, W: torch.Tensor, pool: Pool | None = None, plan: Pla
                               ctypes.byref(pool.c) if plan is not None else None,
                               ctypes.byref(plan.c) if plan is not None else None,
                               _ptr(y, torch.bfloat16, "y"), _stream(stream)), "lora_linear")
+    return y
+
+
+def linear_rows(x_all: torch.Tensor, rows: torch.Tensor, W: torch.Tensor, pool: Pool | None = None,
+                plan: Plan | None = None, x_rows: torch.Tensor | None = None, y: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
+    """The layer on rows `rows` ([T] int32 CUDA) of x_all [T_all, d_in]: y [T,
+    d_out], with the plan built for those rows' slots."""
+    T_all, d_in = x_all.shape
+    T = rows.numel()
+    d_out = W.shape[0]
+    if x_rows is None:
+        x_rows = torch.empty((T, d_in), dtype=torch.bfloat16, device=x_all.device)
+    if y is None:
+        y = torch.empty((T, d_out), dtype=torch.bfloat16, device=x_all.device)
+    if plan is not None and pool is None:
+        raise ValueError("a plan needs a pool")
+    _check(_lib().lora_linear_rows(_ptr(x_all, torch.bfloat16, "x_all"), T_all, _ptr(rows, torch.int32, "rows"), T,
+                                   d_in, d_out, _ptr(W, torch.bfloat16, "W"),
+                                   ctypes.byref(pool.c) if plan is not None else None,
+                                   ctypes.byref(plan.c) if plan is not None else None,
+                                   _ptr(x_rows, torch.bfloat16, "x_rows"), _ptr(y, torch.bfloat16, "y"),
+                                   _stream(stream)), "lora_linear_rows")
     return y
 
 

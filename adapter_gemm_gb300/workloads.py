@@ -15,6 +15,8 @@ Workloads:
   q_decode      T=64,  4096->4096,   8 adapters r16, 8 contiguous rows each
   qkv_decode    q_decode's batch over the q/k/v projections (4096 -> 4096 +
                 1024 + 1024) as one call over three output slices
+  lm_head_prefill  64 sequences x 64 tokens; the LM head (4096 -> 128256) on
+                each sequence's last position, 8 adapters r16
   gateup_prefill T=4096, 4096->14336, 16 adapters r16, power-law (1.1) segment
                 lengths by largest remainder, 10 % of rows on slot 0, contiguous
                 segments in a seeded order
@@ -72,6 +74,9 @@ class Workload:
     # targets that share their input and run as one call over output slices
     # (tuples of target indices); every other target runs on its own
     groups: list = field(default_factory=list)
+    # the layer runs on these rows of x only (the LM head's sampled positions);
+    # T and ids then count the selected rows
+    sel: np.ndarray | None = None
 
     def units(self) -> list:
         """The calls of one step, in target order: tuples of target indices."""
@@ -182,6 +187,20 @@ def qkv_decode(seed: int = 1005) -> Workload:
     return Workload("qkv_decode", T, S, r, ids, x, tl, groups=[(0, 1, 2)])
 
 
+def lm_head_prefill(seed: int = 1006) -> Workload:
+    """The LM head's adapter on a prefill batch: 64 sequences of 64 tokens
+    (x [4096, 4096]); the head runs on each sequence's last position only (64
+    selected rows), into the 128256-entry vocabulary of Llama 3. Eight adapters
+    of rank 16, eight sequences each."""
+    n_seq, L_seq, K, N, S, r = 64, 64, 4096, 128256, 9, 16
+    g_x, g_w = _streams(seed, 2)
+    x = to_bf16(_normal(g_x, (n_seq * L_seq, K), 1.0))
+    sel = (np.arange(n_seq, dtype=np.int32) + 1) * L_seq - 1
+    ids = np.repeat(np.arange(1, S, dtype=np.int32), n_seq // (S - 1))
+    t = make_target(g_w, "lm_head", K, N, [0] + [r] * (S - 1), [0.0] + [32.0] * (S - 1), r)
+    return Workload("lm_head_prefill", n_seq, S, r, ids, x, [t], sel=sel)
+
+
 def gateup_ids(rng: np.random.Generator, T: int = 4096, n_adapters: int = 16,
                base_frac: float = 0.1, power: float = 1.1) -> np.ndarray:
     n0 = int(round(base_frac * T))
@@ -252,6 +271,12 @@ def input_for(w: Workload, t: Target) -> torch.Tensor:
     return t.x_in if t.x_in is not None else w.x
 
 
+def rows_input(w: Workload, t: Target) -> torch.Tensor:
+    """The rows the layer sees: the target's input, or its selected rows."""
+    x = input_for(w, t)
+    return x if w.sel is None else x[torch.from_numpy(w.sel.astype(np.int64))]
+
+
 def by_name(name: str) -> Workload:
     if name == "tiny":
         return tiny()
@@ -263,6 +288,8 @@ def by_name(name: str) -> Workload:
         return mixed_down()
     if name == "qkv_decode":
         return qkv_decode()
+    if name == "lm_head_prefill":
+        return lm_head_prefill()
     if name.startswith("layer_sweep_sliced_T"):
         return layer_sweep(int(name[len("layer_sweep_sliced_T"):]), sliced=True)
     if name.startswith("layer_sweep_T"):

@@ -190,7 +190,7 @@ def oracle_tokens_per_s(w, seconds: float):
         threads = os.cpu_count()
     prep = []
     for t in w.targets:
-        x = WL.input_for(w, t).double().numpy()
+        x = WL.rows_input(w, t).double().numpy()
         prep.append((x, t.W.double().numpy(), t.A.double().numpy(), t.B.double().numpy(), t.rank, t.alpha))
     T = w.T
     # bounded sample: whole steps if one is cheap, else a subset of rows
@@ -291,8 +291,14 @@ def main():
     ys = [torch.empty((T, sum(d)), dtype=torch.bfloat16, device=dev) for d in u_dout]
     torch.cuda.synchronize()
 
+    sel_dev = torch.from_numpy(w.sel).to(dev) if w.sel is not None else None
+    x_rows = [torch.empty((T, w.targets[u[0]].d_in), dtype=torch.bfloat16, device=dev) for u in units] \
+        if w.sel is not None else None
+
     def call(j, x, W, pools, plan, y):
-        if len(pools) == 1:
+        if sel_dev is not None:
+            L.linear_rows(x, sel_dev, W, pools[0], plan, x_rows[j], y)
+        elif len(pools) == 1:
             L.linear(x, W, pools[0], plan, y)
         else:
             L.linear_sliced(x, W, u_dout[j], pools, plan, y)
@@ -470,7 +476,7 @@ def main():
     dx = [{k: torch.empty_like(v) for k, v in xs.items()} for _ in range(NP)]
     dids = [torch.empty_like(ids) for _ in range(NP)]
     dy = [[torch.empty_like(y) for y in ys] for _ in range(NP)]
-    host_api = len(units) == 1 and len(units[0]) == 1
+    host_api = len(units) == 1 and len(units[0]) == 1 and w.sel is None
 
     def e2e_step(i):
         b, c = i % NP, i % n_copies
@@ -593,7 +599,7 @@ def run_reference(args, rank, world):
     w = WL.by_name(args.config)
     prep = []
     for t in w.targets:
-        x = WL.input_for(w, t).double().numpy()
+        x = WL.rows_input(w, t).double().numpy()
         prep.append((x, t.W.double().numpy(), t.A.double().numpy(), t.B.double().numpy(), t.rank, t.alpha))
     T = w.T
 

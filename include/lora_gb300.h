@@ -174,6 +174,20 @@ lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out
                         const lora_pool* pool, const lora_plan_t* plan, void* y,
                         void* stream);
 
+/* The layer on selected rows of x, for the LM head's adapter: it runs only on
+ * the positions that are sampled. In the LoRA-serving page's worked example
+ * (step 6), LogitsProcessorWithLoRA maps each sampled position to its adapter
+ * through sampler_indices, not each scheduled token.
+ *   x_all [T_all, d_in] bf16 device;
+ *   rows [T] int32 device: the selected rows of x_all; an index outside
+ *     [0, T_all) reads a zero row;
+ *   x_rows [T, d_in] bf16 device: the caller's staging buffer for those rows;
+ *   plan: built for the T selected rows, from their slots.
+ * One gather kernel, then lora_linear(x_rows, W, ..., y). Asynchronous. */
+lora_status lora_linear_rows(const void* x_all, int T_all, const int32_t* rows, int T, int d_in, int d_out,
+                             const void* W, const lora_pool* pool, const lora_plan_t* plan, void* x_rows,
+                             void* y, void* stream);
+
 /* The layer on host buffers, for callers whose step inputs and outputs live in
  * host memory. On `stream`:
  *   1. copy x_host ([T, d_in] bf16) into x_dev;

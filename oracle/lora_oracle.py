@@ -152,6 +152,20 @@ def lora_linear_sliced(x, Ws, As, Bs, ranks, alphas, ids, rows=None) -> np.ndarr
                            for W, A, B, r, a in zip(Ws, As, Bs, ranks, alphas)], axis=1)
 
 
+def lora_linear_rows(x_all, sel, W, A, B, rank, alpha, ids) -> np.ndarray:
+    """The layer on selected positions only: the LM head's adapter runs on the
+    sampled positions, each mapped to its own adapter (LoRA serving page, the
+    worked example's step 6: sampler_indices, one entry per sampled position).
+    Row i is the layer of x_all[sel[i]] (a zero row when sel[i] is outside
+    [0, T_all)) with slot ids[i]."""
+    x_all = np.asarray(x_all, dtype=np.float64)
+    sel = np.asarray(sel)
+    ok = (sel >= 0) & (sel < x_all.shape[0])
+    x = np.zeros((len(sel), x_all.shape[1]))
+    x[ok] = x_all[sel[ok]]
+    return lora_linear(x, W, A, B, rank, alpha, ids)
+
+
 def lora_linear_indexed(x, W, A, B, rank, alpha, ids) -> np.ndarray:
     """The same layer row by row, in the indexed (BGMV-like) form: each row
     looks up its own slot. Slow; for small cases only."""

@@ -160,6 +160,11 @@ def test_sliced_and_host_argument_errors(lib):
     assert lib.lora_linear_host(h, None, h, 64, 4096, 4096, W, ctypes.byref(pl), ctypes.byref(p), x, None, y,
                                 None) == EINVAL                                               # ids buffers missing
     assert lib.lora_linear_host(h, None, h, 0, 4096, 4096, W, None, None, x, None, y, None) == OK
+    assert lib.lora_linear_rows(x, 100, None, 8, 4096, 4096, W, None, None, x, y, None) == EINVAL   # no rows
+    assert lib.lora_linear_rows(x, 100, x, 8, 4096, 4096, W, None, None, None, y, None) == EINVAL   # no staging
+    assert lib.lora_linear_rows(x, -1, x, 8, 4096, 4096, W, None, None, x, y, None) == EINVAL
+    assert lib.lora_linear_rows(x, 100, x, 8, 4096, 4092, W, None, None, x, y, None) == ESHAPE
+    assert lib.lora_linear_rows(x, 100, x, 0, 4096, 4096, W, None, None, x, y, None) == OK
 
 
 def test_plan_argument_errors(lib):

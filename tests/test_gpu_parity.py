@@ -589,3 +589,90 @@ def test_host_buffers_two_streams_without_sync():
     for k in range(n_steps):
         ref = O.lora_linear(f64(xs[k]), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, idss[k].numpy())
         assert_parity(ys[k], ref, f"step {k}")
+
+
+# ------------------------------------- plans in CUDA graphs, padded batches ----
+
+def test_graph_replays_with_new_ids_and_inputs():
+    """The plan and the layer are captured once in a CUDA graph; each replay
+    reads whatever ids and x the same buffers hold, so one graph serves every
+    step of a fixed batch size."""
+    T, K, N, S, R = 64, 512, 256, 9, 16
+    w = WL.random_case(seed=120, T=T, K=K, N=N, S=S, R_max=R)
+    t = w.targets[0]
+    W = t.W.to(DEV)
+    pool = L.Pool(S, R, K, N, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    x_buf = torch.zeros((T, K), dtype=torch.bfloat16, device=DEV)
+    ids_buf = torch.zeros(T, dtype=torch.int32, device=DEV)
+    y_buf = torch.empty((T, N), dtype=torch.bfloat16, device=DEV)
+    plan = L.Plan(T, S, R, K, device=DEV)
+    plan.build(ids_buf)
+    L.linear(x_buf, W, pool, plan, y_buf)               # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            plan.build(ids_buf)
+            L.linear(x_buf, W, pool, plan, y_buf)
+    torch.cuda.current_stream().wait_stream(s)
+    rng = np.random.default_rng(121)
+    for k in range(3):
+        ids_np = rng.integers(0, S, size=T).astype(np.int32)
+        x_new = torch.from_numpy(rng.standard_normal((T, K), dtype=np.float32)).to(torch.bfloat16)
+        ids_buf.copy_(torch.from_numpy(ids_np))
+        x_buf.copy_(x_new)
+        g.replay()
+        torch.cuda.synchronize()
+        ref = O.lora_linear(f64(x_new), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, ids_np)
+        assert_parity(y_buf, ref, f"replay {k}")
+
+
+@pytest.mark.parametrize("T_real,T_cap", [(37, 64), (200, 256), (300, 512)])
+def test_padded_batch_rows_on_slot0(T_real, T_cap):
+    """A batch padded to a fixed capacity with slot-0 rows: the real rows get
+    the unpadded layer's result, the zero padding rows get zeros."""
+    K, N, S, R = 384, 264, 12, 16
+    w = WL.random_case(seed=130 + T_real, T=T_real, K=K, N=N, S=S, R_max=R)
+    t = w.targets[0]
+    W = t.W.to(DEV)
+    pool = L.Pool(S, R, K, N, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    x = torch.zeros((T_cap, K), dtype=torch.bfloat16, device=DEV)
+    x[:T_real] = w.x.to(DEV)
+    ids = torch.zeros(T_cap, dtype=torch.int32, device=DEV)
+    ids[:T_real] = torch.from_numpy(w.ids.astype(np.int32)).to(DEV)
+    plan = L.Plan(T_cap, S, R, K, device=DEV).build(ids)
+    y = L.linear(x, W, pool, plan)
+    torch.cuda.synchronize()
+    ref = O.lora_linear(f64(w.x), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, w.ids)
+    assert_parity(y[:T_real], ref, f"padded {T_real} -> {T_cap}")
+    assert torch.count_nonzero(y[T_real:]) == 0
+
+
+# ------------------------------------------- selected rows (the LM head) ----
+
+@pytest.mark.parametrize("T_all,T,N,S,R", [(300, 37, 1032, 9, 16), (1000, 300, 264, 12, 16)])
+def test_selected_rows(T_all, T, N, S, R):
+    """The layer on sampled positions only, each with its own slot; one
+    selected index lies outside x and reads a zero row."""
+    K = 512
+    w = WL.random_case(seed=140 + T, T=T, K=K, N=N, S=S, R_max=R)
+    t = w.targets[0]
+    rng = np.random.default_rng(141)
+    x_all = torch.from_numpy(rng.standard_normal((T_all, K), dtype=np.float32)).to(torch.bfloat16)
+    sel = rng.choice(T_all, size=T, replace=False).astype(np.int32)
+    sel[3] = T_all + 5                                    # outside x: a zero row
+    W = t.W.to(DEV)
+    pool = L.Pool(S, R, K, N, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    ids = torch.from_numpy(w.ids.astype(np.int32)).to(DEV)
+    plan = L.Plan(T, S, R, K, device=DEV).build(ids)
+    y = L.linear_rows(x_all.to(DEV), torch.from_numpy(sel).to(DEV), W, pool, plan)
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    ref = O.lora_linear_rows(f64(x_all), sel, f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, w.ids)
+    assert_parity(y, ref, f"selected rows {T} of {T_all}")
+    assert torch.count_nonzero(y[3]) == 0

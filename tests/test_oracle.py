@@ -244,6 +244,30 @@ def test_sliced_split_of_one_layer():
     np.testing.assert_allclose(y_sw[:, 8:], full[:, 0:7], rtol=1e-12, atol=1e-12)
 
 
+def test_rows_selection_pins():
+    """The layer on selected positions: selecting every row in order is the
+    layer itself; a reversed selection reverses the rows; an index outside x
+    reads a zero row, which gets exactly zero."""
+    rng = np.random.default_rng(11)
+    T, K, N, S, R = 7, 12, 10, 4, 4
+    x = rng.integers(-2, 3, size=(T, K)).astype(np.float64)
+    W = rng.integers(-2, 3, size=(N, K)).astype(np.float64)
+    A = np.zeros((S, R, K)); B = np.zeros((S, N, R))
+    ranks = [0, 4, 2, 3]
+    for s in range(1, S):
+        A[s, :ranks[s]] = rng.integers(-2, 3, size=(ranks[s], K))
+        B[s, :, :ranks[s]] = rng.integers(-2, 3, size=(N, ranks[s]))
+    alpha = [0.0, 8.0, 4.0, 6.0]
+    ids = rng.integers(0, S, size=T)
+    full = O.lora_linear(x, W, A, B, ranks, alpha, ids)
+    assert np.array_equal(O.lora_linear_rows(x, np.arange(T), W, A, B, ranks, alpha, ids), full)
+    rev = np.arange(T)[::-1]
+    assert np.array_equal(O.lora_linear_rows(x, rev, W, A, B, ranks, alpha, ids[rev]), full[rev])
+    y = O.lora_linear_rows(x, np.array([2, -1, T, 5]), W, A, B, ranks, alpha, np.array([ids[2], 1, 2, ids[5]]))
+    assert np.array_equal(y[0], full[2]) and np.array_equal(y[3], full[5])
+    assert not y[1].any() and not y[2].any()
+
+
 def test_transposed_or_dropped_terms_are_caught():
     """The integer pin distinguishes the plausible slips: a transposed B, a
     dropped scale, a rank-padded scale, a wrong sign."""
