@@ -529,7 +529,16 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
     // The expand runs on the tensor cores (Bcat against U) when every adapter
     // slot's ranks (rounded up to 16) fit 128 pairs; else on the CUDA cores.
     const bool tc_expand = plan && path == 0 && T <= 64 && pool->S >= 2 && (pool->S - 1) * r16 <= 128;
-    const bool fuse = tc_expand && ids_early;
+    // With the shrink fused in, every weight tile re-reads the A tile ((S-1) *
+    // R_max rows of the whole K range) from L2; with the shrink kernel ahead,
+    // A is read once but the call has one more launch. Measured on q_decode
+    // (32 tiles, 33.5 MB of A re-reads) fusing is faster (12.1 against 15.3
+    // us per step); on an LM head of 1002 tiles (1 GB) the shrink kernel is
+    // (198 against 279 us). Sliced calls fuse, for their one launch.
+    const double a_rereads = plan ? (double)((d_out + 127) / 128) * ((T + 63) / 64) * (pool->S - 1) * pool->R_max *
+                                        d_in * 2.0
+                                  : 0.0;
+    const bool fuse = tc_expand && ids_early && (slices || a_rereads <= kFuseMaxAReread);
     if (slices && !fuse) return LORA_EINVAL;                   // callers check this first
     if (plan && !fuse) {
         ShrinkArgs sa;

@@ -15,6 +15,7 @@ constexpr int kSkinnyPathMaxT = 256; // batches up to this many rows take the sw
 constexpr int kStageURank = 64;     // the skinny epilogue stages U rows of rank <= 64
 constexpr int kBySlotMaxT = 64;     // up to this many rows the shrink groups rows by slot itself
 constexpr size_t kSkinnyMaxSmem = (size_t)227 * 1024;   // dynamic shared memory a CTA may have
+constexpr double kFuseMaxAReread = 48.0 * 1024 * 1024;  // A-tile bytes the weight tiles may re-read when fused
 
 struct PlanArgs {
     int32_t* slot_of_token;

@@ -449,6 +449,18 @@ def test_most_slots(T):
     assert_parity(y, dw.oracle(0), f"S=1024, T={T}")
 
 
+def test_wide_output_takes_the_shrink_kernel():
+    """Many weight tiles would re-read the A tile too often: U comes from the
+    shrink kernel ahead (two kernels) and the expand runs on the tensor cores."""
+    w = WL.random_case(seed=24, T=16, K=4096, N=8192, S=9, R_max=16)
+    dw = DeviceWorkload(w, DEV)
+    n0 = L.launch_count()
+    y = dw.run(0)
+    assert L.launch_count() - n0 == 2
+    assert L.last_device_error() == 0
+    assert_parity(y, dw.oracle(0), "shrink kernel, tensor-core expand")
+
+
 def test_shrink_kernel_when_pool_exceeds_one_tile():
     """(S - 1) * R_max > 128: U comes from the shrink kernel ahead of the GEMM."""
     w = WL.random_case(seed=22, T=48, K=512, N=384, S=10, R_max=16)
