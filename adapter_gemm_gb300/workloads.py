@@ -17,6 +17,8 @@ Workloads:
                 1024 + 1024) as one call over three output slices
   lm_head_prefill  64 sequences x 64 tokens; the LM head (4096 -> 128256) on
                 each sequence's last position, 8 adapters r16
+  skewed_prefill  T=4096, 4096->4096, 90 % of rows on one adapter, 5 % on
+                slot 0, the rest over 15 adapters r16
   gateup_prefill T=4096, 4096->14336, 16 adapters r16, power-law (1.1) segment
                 lengths by largest remainder, 10 % of rows on slot 0, contiguous
                 segments in a seeded order
@@ -187,6 +189,21 @@ def qkv_decode(seed: int = 1005) -> Workload:
     return Workload("qkv_decode", T, S, r, ids, x, tl, groups=[(0, 1, 2)])
 
 
+def skewed_prefill(seed: int = 1007) -> Workload:
+    """A skewed load: T=4096 rows of a 4096 -> 4096 projection, 90 % of the
+    rows on one adapter, 5 % on slot 0, the rest spread over 15 more adapters
+    (rank 16), rows shuffled."""
+    T, K, N, S, r = 4096, 4096, 4096, 17, 16
+    g_ids, g_x, g_w = _streams(seed, 3)
+    n_hot, n_base = int(0.9 * T), int(0.05 * T)
+    ids = np.concatenate([np.full(n_hot, 1, np.int32), np.zeros(n_base, np.int32),
+                          g_ids.integers(2, S, size=T - n_hot - n_base).astype(np.int32)])
+    ids = ids[g_ids.permutation(T)].astype(np.int32)
+    x = to_bf16(_normal(g_x, (T, K), 1.0))
+    t = make_target(g_w, "o_proj", K, N, [0] + [r] * (S - 1), [0.0] + [32.0] * (S - 1), r)
+    return Workload("skewed_prefill", T, S, r, ids, x, [t])
+
+
 def lm_head_prefill(seed: int = 1006) -> Workload:
     """The LM head's adapter on a prefill batch: 64 sequences of 64 tokens
     (x [4096, 4096]); the head runs on each sequence's last position only (64
@@ -290,6 +307,8 @@ def by_name(name: str) -> Workload:
         return qkv_decode()
     if name == "lm_head_prefill":
         return lm_head_prefill()
+    if name == "skewed_prefill":
+        return skewed_prefill()
     if name.startswith("layer_sweep_sliced_T"):
         return layer_sweep(int(name[len("layer_sweep_sliced_T"):]), sliced=True)
     if name.startswith("layer_sweep_T"):
