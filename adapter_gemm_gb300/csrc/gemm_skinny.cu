@@ -364,6 +364,32 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
     // holds its own share of U (fused), else rank 0, which holds all of U.
     const bool adds_x = fuse || (tcx && kz == 0);
 
+    // TMA producer (warp 0 lane 0): one copy per operand per stage (a stage
+    // is KK slices of 64 columns: a TMA copy has a fixed cost, so fewer,
+    // larger copies stream faster). Weights are never written by the kernels
+    // this one waits for, so the first `stages` stages of weights are
+    // requested before the wait - right after the barriers exist, while warp 1
+    // still allocates tensor memory - and x too unless the host saw that the
+    // previous kernel writes it. With the shrink fused in, each stage also
+    // holds the A rows of every adapter slot of the pool (slots 1..S-1, R_max
+    // rows each) for the same slices: the A tile.
+    const int nst = (nkb + KK - 1) / KK;                          // stages of this CTA's K range
+    const int pre = min(nst, stages);
+    const uint32_t tx = (uint32_t)KK * (kWTileBytes + x_tile_bytes + (fuse ? a_slice : 0u));
+    // slice index of stage i: kb_lo + i KK (with kk > 1 the tensor maps are
+    // 3-D / 4-D views whose last coordinate counts 64-column slices)
+    auto load_w = [&](uint32_t dst, uint32_t fb, int i) {
+        if (KK == 1) tma_load_2d(dst, &tmW, fb, (kb_lo + i) * kBK, n0);
+        else tma_load_3d(dst, &tmW, fb, 0, n0, kb_lo + i * KK);
+    };
+    auto load_x = [&](uint32_t dst, uint32_t fb, int i) {
+        if (KK == 1) tma_load_2d(dst, &tmX, fb, (kb_lo + i) * kBK, t0);
+        else tma_load_3d(dst, &tmX, fb, 0, t0, kb_lo + i * KK);
+    };
+    auto load_a = [&](uint32_t dst, uint32_t fb, int i) {
+        if (KK == 1) tma_load_3d(dst, &tmA, fb, (kb_lo + i) * kBK, 0, 1);
+        else tma_load_4d(dst, &tmA, fb, 0, 0, 1, kb_lo + i * KK);
+    };
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
@@ -375,6 +401,14 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
         mbar_init(smem_u32(accf), 1);
         mbar_init(smem_u32(accx), 1);
         fence_mbar_init();
+        for (int i = 0; i < pre; ++i) {
+            const uint32_t fb = smem_u32(&full[i]);
+            const uint32_t sb = smem_u32(base + (size_t)i * stage_bytes);
+            mbar_arrive_expect_tx(fb, tx);
+            load_w(sb + w_off, fb, i);
+            if (fuse) load_a(sb + a_off, fb, i);
+            if (a.x_early) load_x(sb + x_off, fb, i);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), tmem_cols);
@@ -389,40 +423,7 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
     pdl_trigger();
 
     bool ok = true;
-    const int nst = (nkb + KK - 1) / KK;                          // stages of this CTA's K range
     if (warp == 0 && lane == 0) {
-        // TMA producer, one copy per operand per stage (a stage is KK slices of
-        // 64 columns: a TMA copy has a fixed cost, so fewer, larger copies
-        // stream faster). Weights are never written by the kernels this one
-        // waits for, so the first `stages` stages of weights are requested
-        // before the wait; x too unless the host saw that the previous kernel
-        // writes it. With the shrink fused in, each stage also holds the A rows
-        // of every adapter slot of the pool (slots 1..S-1, R_max rows each) for
-        // the same slices: the A tile.
-        const int pre = min(nst, stages);
-        const uint32_t tx = (uint32_t)KK * (kWTileBytes + x_tile_bytes + (fuse ? a_slice : 0u));
-        // slice index of stage i: kb_lo + i KK (with kk > 1 the tensor maps
-        // are 3-D / 4-D views whose last coordinate counts 64-column slices)
-        auto load_w = [&](uint32_t dst, uint32_t fb, int i) {
-            if (KK == 1) tma_load_2d(dst, &tmW, fb, (kb_lo + i) * kBK, n0);
-            else tma_load_3d(dst, &tmW, fb, 0, n0, kb_lo + i * KK);
-        };
-        auto load_x = [&](uint32_t dst, uint32_t fb, int i) {
-            if (KK == 1) tma_load_2d(dst, &tmX, fb, (kb_lo + i) * kBK, t0);
-            else tma_load_3d(dst, &tmX, fb, 0, t0, kb_lo + i * KK);
-        };
-        auto load_a = [&](uint32_t dst, uint32_t fb, int i) {
-            if (KK == 1) tma_load_3d(dst, &tmA, fb, (kb_lo + i) * kBK, 0, 1);
-            else tma_load_4d(dst, &tmA, fb, 0, 0, 1, kb_lo + i * KK);
-        };
-        for (int i = 0; i < pre; ++i) {
-            const uint32_t fb = smem_u32(&full[i]);
-            const uint32_t sb = smem_u32(base + (size_t)i * stage_bytes);
-            mbar_arrive_expect_tx(fb, tx);
-            load_w(sb + w_off, fb, i);
-            if (fuse) load_a(sb + a_off, fb, i);
-            if (a.x_early) load_x(sb + x_off, fb, i);
-        }
         if (!a.x_early) pdl_wait();
         int issued = 0;
         for (int i = 0; i < nst && ok; ++i) {
