@@ -650,12 +650,16 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
     } else {
         const void* A = plan ? plan->x_sorted : x;
         // 128 x 256 output tiles, or 128 x 128 for mid-sized grids (fewer
-        // than two waves of wide tiles) when the narrow tiles finish in fewer
-        // wide-tile times: waves x width. Depends on the shape only.
+        // than two waves of wide tiles) when the narrow tiles finish sooner.
+        // A tile's time is set by its operand stream, (128 + width) rows per K
+        // slice, so a wide tile costs 1.5 narrow ones: waves x 2 against
+        // waves x 3 in half-narrow-tile units, ties to the wide tile. (At
+        // T = 512: 4096 outputs run faster narrow, 33.7 against 41.2 us;
+        // 14336 outputs wide, 74 against 84 us.) Depends on the shape only.
         const int m_tiles = (T + 127) / 128;
         const int sms = num_sms();
         const int t256 = m_tiles * ((d_out + 255) / 256), t128 = m_tiles * ((d_out + 127) / 128);
-        const int cost256 = 2 * ((t256 + sms - 1) / sms), cost128 = (t128 + sms - 1) / sms;
+        const int cost256 = 3 * ((t256 + sms - 1) / sms), cost128 = 2 * ((t128 + sms - 1) / sms);
         const int bn = (t256 < 2 * sms && cost128 < cost256) ? 128 : 256;
         // narrow tiles take two K slices per stage (3-D views; x and the
         // plan-ordered copy of x are [T][d_in], W is [d_out][d_in]), so that a
