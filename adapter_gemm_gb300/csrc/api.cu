@@ -653,9 +653,11 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // than two waves of wide tiles) when the narrow tiles finish sooner.
         // A tile's time is set by its operand stream, (128 + width) rows per K
         // slice, so a wide tile costs 1.5 narrow ones: waves x 2 against
-        // waves x 3 in half-narrow-tile units, ties to the wide tile. (At
-        // T = 512: 4096 outputs run faster narrow, 33.7 against 41.2 us;
-        // 14336 outputs wide, 74 against 84 us.) Depends on the shape only.
+        // waves x 3 in half-narrow-tile units, ties to the wide tile. Measured
+        // alone: T = 512 with 4096 outputs runs faster narrow (33.7 against
+        // 41.2 us); wide wins at T = 512 with 14336 outputs (65.5 against 69.6
+        // us), T = 1500 with 4096 (57.3 against 59.4) and T = 4096 with 1288
+        // (55.3 against 57.3). Depends on the shape only.
         const int m_tiles = (T + 127) / 128;
         const int sms = num_sms();
         const int t256 = m_tiles * ((d_out + 255) / 256), t128 = m_tiles * ((d_out + 127) / 128);
