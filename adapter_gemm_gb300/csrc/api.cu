@@ -196,7 +196,8 @@ int skinny_kk(int TN, bool fuse, bool tce, int a_rows, int K) {
 // GEMMs stream their weights side by side; wider tiles may use every SM.
 // `mode`: 0 base only, 1 U from the shrink kernel (expand on the CUDA cores),
 // 2 shrink fused in, 3 U from the shrink kernel with the expand on the tensor
-// cores.
+// cores (rank 0 of the cluster), 4 the same with the expand's chunks dealt over
+// the cluster.
 SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S) {
     SkinnyConfig c;
     const int Tt = T < kSkinnyMaxT ? T : kSkinnyMaxT;
@@ -220,16 +221,17 @@ SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S) {
             break;
         }
     }
-    const bool fuse = mode == 2, tce = mode >= 2;
+    const bool fuse = mode == 2, tce = mode == 2 || mode == 3;   // Bcat and the token tables beside the pipeline
     const int a_rows = fuse ? (S - 1) * R_max : 0;
     c.kk = skinny_kk(c.TN, fuse, tce, a_rows, K);
     c.stages = skinny_stages(c.TN, fuse, tce, c.kk);
     c.stage_u = (mode == 1 && R_max <= kStageURank &&
                  skinny_epi_bytes(c.TN, R_max, true, false, false) + 2048 <= (size_t)200 * 1024) ? 1 : 0;
-    c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, tce, mode == 0, c.kk);
+    const bool y_staged = mode == 0 || mode == 4;             // epilogue: partials + y staging only
+    c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, tce, y_staged, c.kk);
     while (c.stages > 2 && c.smem > kSkinnyMaxSmem) {
         --c.stages;
-        c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, tce, mode == 0, c.kk);
+        c.smem = skinny_smem_bytes(c.TN, c.stages, R_max, c.stage_u != 0, fuse, tce, y_staged, c.kk);
     }
     return c;
 }
@@ -539,6 +541,15 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
                                         d_in * 2.0
                                   : 0.0;
     const bool fuse = tc_expand && ids_early && (slices || a_rereads <= kFuseMaxAReread);
+    // Otherwise, with U from the shrink kernel and more slots than the
+    // rank-0 expand holds, the expand's (slot, 16-rank) chunks are dealt over
+    // the cluster and run on the tensor cores, except for batches of at most
+    // kCoreExpandMaxT rows, whose few (row, token) products the CUDA cores
+    // finish sooner. Measured alone (us per GEMM, tensor / CUDA cores):
+    // T = 256, 14336 -> 4096, ranks 8..64 on 31 slots: 52.4 / 64.1; T = 64,
+    // 4096 -> 4096, 50 rank-16 slots: 26.8 / 30.8; T = 8: 22.7 / 22.6;
+    // T = 1: 22.6 / 20.5.
+    const bool tcl = plan && path == 0 && !tc_expand && T > kCoreExpandMaxT;
     if (slices && !fuse) return LORA_EINVAL;                   // callers check this first
     if (plan && !fuse) {
         ShrinkArgs sa;
@@ -576,7 +587,7 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
 
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_start, st) != cudaSuccess) return LORA_ECUDA;
     if (path == 0) {
-        const int mode = !plan ? 0 : (fuse ? 2 : (tc_expand ? 3 : 1));
+        const int mode = !plan ? 0 : (fuse ? 2 : (tc_expand ? 3 : (tcl ? 4 : 1)));
         const SkinnyConfig c = skinny_config(T, d_in, d_out, mode, plan ? pool->R_max : 8, plan ? pool->S : 1);
         SkinnyMaps maps;
         CUtensorMap& tmW = maps.w;
@@ -627,6 +638,14 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
                 }
             }
         }
+        maps.b = tmX;                  // unused unless the expand's chunks are dealt
+        if (mode == 4) {
+            // B pool [S][d_out][R_max]: one chunk is 128 rows x 16 ranks of a slot
+            const uint64_t db[3] = {(uint64_t)pool->R_max, (uint64_t)d_out, (uint64_t)pool->S};
+            const uint64_t pb[2] = {(uint64_t)pool->R_max * 2, (uint64_t)d_out * pool->R_max * 2};
+            const uint32_t bb[3] = {16, 128, 1};
+            if (!make_tmap_nd(&maps.b, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B)) return LORA_ECUDA;
+        }
         a.y = static_cast<__nv_bfloat16*>(y);
         a.ldy = ldy;
         a.ex = ex;
@@ -642,6 +661,7 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         a.a_rows = fuse ? (pool->S - 1) * pool->R_max : 0;
         a.a_chunks = tc_expand ? (pool->S - 1) * r16 / 16 : 0;
         a.tcx = (tc_expand && !fuse) ? 1 : 0;
+        a.tcl = mode == 4 ? 1 : 0;
         a.kk = c.kk;
         a.smem = c.smem;
         a.x_early = x_early ? 1 : 0;

@@ -28,6 +28,12 @@
 //    and j < r_s, else 0. U_part is split into bf16 high and low halves, two
 //    MMAs per 16 pairs. The expand is linear in U, so the owner's sum over
 //    ranks is the full correction;
+//  - U from the shrink kernel ahead, expand on the tensor cores: the same
+//    MMAs against Ucat built from that U. With few slots (every slot's ranks
+//    in 128 pairs) rank 0 of the cluster adds the whole expand; otherwise the
+//    (slot, 16-rank chunk) pairs of the slots that have tokens in the tile are
+//    dealt round-robin to the cluster's CTAs, which add their chunks in
+//    batches in the idle pipeline buffers;
 //  - U from the shrink kernel ahead: the owner adds U[t, :r] . B[s, n, :r]
 //    (fp32, j ascending) to the summed partials on the CUDA cores.
 // Tokens on slot 0, on a rank-0 slot or with an invalid id get no correction.
@@ -54,6 +60,7 @@ constexpr int kMaxChunks = 8;              // tensor-core expand: (slot, rank) p
 constexpr int kChunkRowBytes = 32;         // one row of a 16-wide bf16 chunk (32-byte swizzle)
 constexpr int kBcatBytes = kMaxChunks * kWRows * kChunkRowBytes;
 constexpr int kMaxASlots = 8;              // adapter slots of the expand (R16 >= 16 pairs each)
+constexpr int kMaxBatch = 32;              // chunk-dealt expand: chunks per batch
 
 // Tensor-core expand: Bcat, then the token tables: msc[a][t] (alpha / r where
 // token t is on slot a + 1, else 0), each token's slot - 1 (or -1) and the
@@ -63,8 +70,12 @@ __host__ __device__ size_t skinny_xtab_bytes(int TN) {
 }
 
 // The tile's tokens grouped by slot (kept apart from the pipeline's buffers,
-// since it is built during the K loop).
-__host__ __device__ size_t skinny_grp_bytes(int TN) { return ((size_t)8 * TN + kMaxAct + 8) * 4; }
+// since it is built during the K loop; the chunk-dealt expand keeps its slot
+// runs in the room after the groups), then that expand's batch table: five
+// ints per entry, then the entry, item and slot-run counts.
+__host__ __device__ size_t skinny_grp_bytes(int TN) {
+    return ((size_t)8 * TN + kMaxAct + 8 + 5 * kMaxBatch + 3) * 4;
+}
 
 // Epilogue scratch after the K loop, in the pipeline's buffers: the received
 // partials [ks][TN][128/ks] (128 x TN floats), then per mode
@@ -285,6 +296,175 @@ __device__ void stage_bcat(const SkinnyArgs& a, const SliceExpand& sv, uint8_t* 
     fence_proxy_async_smem();          // read by the expand MMAs after the K loop
 }
 
+// The tile's slot runs for the chunk-dealt expand (a run is the consecutive
+// groups of one slot): run_g[k] = the run's first group, run_g[n] = G;
+// cbase[k] = 16-rank chunks of the runs before it (runs of tokens with no
+// correction count none), cbase[n] = all chunks; *n_runs = n. By the first
+// warp of the `nthr` threads numbered i0 = 0.. that grouped the tokens.
+__device__ void slot_runs(const TileGroups& gp, int* run_g, int* cbase, int* n_runs, int i0, int nthr) {
+    if (i0 < 32) {
+        const int lane = i0, G = *gp.n_groups;
+        int n = 0, cb = 0;
+        for (int base = 0; base < G; base += 32) {
+            const int g = base + lane;
+            const int sl = g < G ? gp.gslot[g] : -1;
+            const bool start = g < G && (g == 0 || gp.gslot[g - 1] != sl);
+            const int cps = start ? (gp.gr8[g] + 15) >> 4 : 0;
+            const unsigned m = __ballot_sync(0xffffffffu, start);
+            int inc = cps;             // inclusive prefix of the chunks over this round's runs
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, d);
+                if (lane >= d) inc += v;
+            }
+            if (start) {
+                const int k = n + __popc(m & ((1u << lane) - 1u));
+                run_g[k] = g;
+                cbase[k] = cb + inc - cps;
+            }
+            n += __popc(m);
+            cb += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) {
+            run_g[n] = G;
+            cbase[n] = cb;
+            *n_runs = n;
+        }
+    }
+    grp_barrier(nthr);
+}
+
+// Chunk-dealt tensor-core expand, U from the shrink kernel ahead (fp32
+// [T][R_max], alpha / r applied). The (slot, 16-rank chunk) pairs of the
+// tile's slot runs, in slot order (chunk c), are dealt round-robin: CTA kz of
+// the cluster takes c = kz, kz + ks, ... and adds them to its own partial
+// tile, in batches of up to `nb_cap` chunks held in `buf` (the pipeline
+// buffers, idle after the K loop):
+//     partial[n, t] += sum_j B[s, n0 + n, 16 h + j] Ucat[t, j],  j < 16,
+// Ucat[t, j] = U[t, 16 h + j] when token t is on slot s and 16 h + j is below
+// its rank rounded up to 8 (U and B are zero from the rank up), else 0, split
+// into bf16 high and low halves (two MMAs per chunk). The expand is linear in
+// U, so the owners' sums over the cluster hold the whole correction.
+// A batch's B chunks arrive by TMA (one 128 x 16 box each, 32-byte swizzle,
+// zero past the pool's rows and ranks) while the threads zero Ucat and write
+// the tokens' U values, one item per (token, 8 ranks).
+// Needs the slot runs and U (after the wait); returns false when a wait gave
+// up. Every thread of the CTA calls it.
+__device__ bool expand_by_chunks(const SkinnyArgs& a, const CUtensorMap* tmB, const SliceExpand& sv,
+                                 const TileGroups& gp, const int* run_g, const int* cbase, uint8_t* buf, int nb_cap,
+                                 int* tab, uint32_t tmem, uint32_t accx, uint32_t bfull, bool have, int t0, int n0,
+                                 int kz) {
+    const int TN = a.TN, R = a.ex.R_max;
+    const uint32_t u_bytes = 2u * (uint32_t)TN * kChunkRowBytes;   // one chunk of Ucat: high, then low
+    constexpr uint32_t b_bytes = kWRows * kChunkRowBytes;           // one chunk of Bcat
+    uint8_t* ucat = buf;                                            // [nb_cap][2][TN][16] bf16
+    uint8_t* bcat = buf + (size_t)nb_cap * u_bytes;                 // [nb_cap][128][16] bf16
+    int* const t_cnt = tab + 5 * kMaxBatch;
+    const int n_runs = t_cnt[2], C = cbase[n_runs];
+    const int mine = C > kz ? (C - kz + a.ks - 1) / a.ks : 0;       // this CTA's chunks
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int batch = 0; batch * nb_cap < mine; ++batch) {
+        const uint32_t ph = (uint32_t)batch & 1u;
+        const int nb = min(nb_cap, mine - batch * nb_cap);
+        if (warp == 0) {
+            // table entry e (lane e): slot, chunk, first position of the
+            // slot's tokens in the sorted order, 8-rank halves of the chunk
+            // below the rank, first item
+            int cnt = 0, sl = 0, h = 0, pb = 0, nh = 0;
+            if (lane < nb) {
+                const int c = kz + (batch * nb_cap + lane) * a.ks;
+                int lo = 0, hi = n_runs - 1;          // the last run with cbase <= c
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (cbase[mid] <= c) lo = mid;
+                    else hi = mid - 1;
+                }
+                const int g = run_g[lo], r8 = gp.gr8[g];
+                sl = gp.gslot[g];
+                h = c - cbase[lo];
+                pb = gp.gbeg[g];
+                nh = r8 - 16 * h >= 16 ? 2 : 1;
+                cnt = (gp.gbeg[run_g[lo + 1]] - pb) * nh;
+            }
+            int inc = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, d);
+                if (lane >= d) inc += v;
+            }
+            if (lane < nb) {
+                int* en = tab + 5 * lane;
+                en[0] = sl;
+                en[1] = h;
+                en[2] = pb;
+                en[3] = nh;
+                en[4] = inc - cnt;
+            }
+            if (lane == 31) t_cnt[1] = inc;
+            if (have) {
+                if (lane == 0) mbar_arrive_expect_tx(bfull, (uint32_t)nb * b_bytes);
+                __syncwarp();
+                if (lane < nb) tma_load_3d(smem_u32(bcat) + (uint32_t)lane * b_bytes, tmB, bfull, 16 * h, n0 - sv.noff, sl);
+            }
+        }
+        {
+            uint4* z = reinterpret_cast<uint4*>(ucat);
+            const int n16 = nb * (int)u_bytes / 16;
+            for (int q = threadIdx.x; q < n16; q += kSkThreads) z[q] = make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();
+        const int items = t_cnt[1];
+        for (int q = threadIdx.x; q < items; q += kSkThreads) {
+            int e = 0;
+            while (e + 1 < nb && tab[5 * (e + 1) + 4] <= q) ++e;
+            const int* en = tab + 5 * e;
+            const int nh = en[3], k = q - en[4];
+            const int t = gp.order[en[2] + k / nh], hf = k - (k / nh) * nh;
+            const int j0 = en[1] * 16 + hf * 8;
+            const float4* up = reinterpret_cast<const float4*>(a.ex.U + (size_t)(t0 + t) * R + j0);
+            const float4 u0 = __ldg(up), u1 = __ldg(up + 1);
+            const float v[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float h0 = __bfloat162float(__float2bfloat16_rn(v[2 * i]));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(v[2 * i + 1]));
+                hw[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                lw[i] = pack_bf16x2(v[2 * i] - h0, v[2 * i + 1] - h1);
+            }
+            uint8_t* dst = ucat + (size_t)e * u_bytes + sw32_offset(t, hf * 8);
+            *reinterpret_cast<uint4*>(dst) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(dst + (size_t)TN * kChunkRowBytes) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        int got = 1;
+        if (threadIdx.x == 32 && have) {      // warp 1 lane 0, the MMA issuer of the K loop
+            got = mbar_wait(bfull, ph, kErrFullWait) ? 1 : 0;
+            if (got) {
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)TN);
+                const uint32_t su = smem_u32(ucat), sb = smem_u32(bcat);
+                for (int e = 0; e < nb; ++e) {
+                    const uint64_t da = sdesc_sw32(sb + (uint32_t)e * b_bytes);
+                    const uint32_t uc = su + (uint32_t)e * u_bytes;
+                    tc_mma_bf16(tmem, da, sdesc_sw32(uc), idesc, 1u);
+                    tc_mma_bf16(tmem, da, sdesc_sw32(uc + (uint32_t)TN * kChunkRowBytes), idesc, 1u);
+                }
+            }
+            tc_commit(accx);
+        }
+        // the batch's buffers (and the table) are rewritten by the next one
+        // only after its MMAs
+        if (threadIdx.x == 0 && have) got = mbar_wait(accx, ph, kErrAccWait) ? 1 : 0;
+        have = __syncthreads_and(got) && have;
+        tc_fence_after();
+    }
+    return have;
+}
+
 __global__ void __launch_bounds__(kSkThreads, 1)
 gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constant__ SkinnyArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -296,6 +476,7 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
     const bool fuse = a.fuse != 0;                // U computed here
     const bool tcx = a.tcx != 0;                  // U from the kernel ahead, expand on the tensor cores
     const bool tce = fuse || tcx;                 // tensor-core expand
+    const bool tcl = a.tcl != 0;                  // U from the kernel ahead, chunks dealt over the cluster
     const int R = a.ex.R_max;
     const int R16 = (R + 15) & ~15;
     const int KK = a.kk;                                          // K slices per stage
@@ -315,7 +496,8 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
     uint64_t* empty = full + stages;                              // [stages]
     uint64_t* accf = empty + stages;                              // [1] K loop done
     uint64_t* accx = accf + 1;                                    // [1] expand MMAs done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accx + 1);
+    uint64_t* bfull = accx + 1;                                   // [1] chunk-dealt expand: B chunks landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bfull + 1);
     // After the K loop, in the pipeline's buffers: the received partials of
     // the weight rows this CTA finishes, [ks][TN][rows_per] floats, then
     //  - late U on the CUDA cores: the tile's U rows [TN][R] when staged;
@@ -334,6 +516,9 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
                         gmem + 4 * TN,
                         gmem + 5 * TN,
                         gmem + 6 * TN + 1};
+    int* run_g = gmem + 6 * TN + 2;                               // chunk-dealt expand: slot runs [TN + 1]
+    int* cbase = run_g + TN + 1;                                   //   and their first chunks [TN + 1]
+    int* tab = gmem + 8 * TN + kMaxAct + 8;                        //   and the batch table
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tile = blockIdx.x;
@@ -359,7 +544,7 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
     const uint32_t tmem_cols = acc_cols <= 32 ? 32u : (acc_cols <= 64 ? 64u : (acc_cols <= 128 ? 128u : 256u));
     // Expand on the CUDA cores, after U from the kernel ahead: y is stored
     // straight from the items.
-    const bool late_u = a.ex.ids != nullptr && !tce;
+    const bool late_u = a.ex.ids != nullptr && !tce && !tcl;
     // The CTA that adds the expand to its partial tile: every one when it
     // holds its own share of U (fused), else rank 0, which holds all of U.
     const bool adds_x = fuse || (tcx && kz == 0);
@@ -400,6 +585,8 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
         }
         mbar_init(smem_u32(accf), 1);
         mbar_init(smem_u32(accx), 1);
+        mbar_init(smem_u32(bfull), 1);
+        if (tcl) tma_prefetch_desc(&maps.b);
         fence_mbar_init();
         for (int i = 0; i < pre; ++i) {
             const uint32_t fb = smem_u32(&full[i]);
@@ -482,9 +669,10 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
         // be read before the wait.
         stage_bcat(a, sv, bcat, n0, (int)threadIdx.x - 64, kSkThreads - 64);
         if (a.ids_early) expand_tables(a, sv, msc, tact, srank, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64);
-    } else if (warp >= 2 && late_u && a.ids_early) {
+    } else if (warp >= 2 && (late_u || tcl) && a.ids_early) {
         // Idle during the K loop: group the tokens and fetch B's rows to L2.
         group_tokens(a, sv, gp, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64, n_lo, n_rows, rows_per);
+        if (tcl) slot_runs(gp, run_g, cbase, tab + 5 * kMaxBatch + 2, (int)threadIdx.x - 64, kSkThreads - 64);
     }
     __syncwarp();
     const int row = (warp & 3) * 32 + lane;         // the accumulator row (TMEM lane) this thread reads
@@ -609,8 +797,23 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
         }
         __syncwarp();
         if (a.ks > 1) cluster_wait_acquire();    // every peer's buffers are free
-    } else if (a.ks > 1) {
-        cluster.sync();                // every peer's stage buffers are free
+    } else {
+        if (tcl) {
+            // U (and, when the host could not rule out that the kernel ahead
+            // writes them, the ids) come from the kernels before this one.
+            pdl_wait();
+            if (!a.ids_early) {
+                group_tokens(a, sv, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
+                slot_runs(gp, run_g, cbase, tab + 5 * kMaxBatch + 2, (int)threadIdx.x, kSkThreads);
+            }
+            __syncthreads();
+            const size_t body = pipe > epi_bytes ? pipe : epi_bytes;
+            const size_t chunk = (size_t)kWRows * kChunkRowBytes + (size_t)2 * TN * kChunkRowBytes;
+            const int nb_cap = (int)min((size_t)kMaxBatch, body / chunk);
+            have = expand_by_chunks(a, &maps.b, sv, gp, run_g, cbase, base, nb_cap, tab, tmem, smem_u32(accx),
+                                    smem_u32(bfull), have, t0, n0, kz);
+        }
+        if (a.ks > 1) cluster.sync();  // every peer's stage buffers are free
     }
     // Split-K reduction. CTA rank c owns weight rows [c*rows_per, (c+1)*rows_per)
     // of the tile. Each CTA pushes its partial rows straight from TMEM into the

@@ -13,6 +13,7 @@ constexpr int kMaxRank = 128;       // R_max cap: shrink keeps R_max/8 MMA colum
 constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 256)
 constexpr int kSkinnyPathMaxT = 256; // batches up to this many rows take the swap-AB kernel
 constexpr int kStageURank = 64;     // the skinny epilogue stages U rows of rank <= 64
+constexpr int kCoreExpandMaxT = 8;  // decode batches up to this many rows expand on the CUDA cores
 constexpr int kBySlotMaxT = 64;     // up to this many rows the shrink groups rows by slot itself
 constexpr size_t kSkinnyMaxSmem = (size_t)227 * 1024;   // dynamic shared memory a CTA may have
 constexpr double kFuseMaxAReread = 48.0 * 1024 * 1024;  // A-tile bytes the weight tiles may re-read when fused
@@ -74,6 +75,7 @@ struct SliceExpand {
 struct SkinnyMaps {
     CUtensorMap w, x;              // W [N][K], x [T][K]
     CUtensorMap a[kMaxSlices];     // fused: each slice's A pool
+    CUtensorMap b;                 // chunk-dealt expand: the B pool [S][N][R_max], 128 x 16 boxes, 32-byte swizzle
 };
 
 struct SkinnyArgs {
@@ -94,6 +96,7 @@ struct SkinnyArgs {
     int a_rows;        // rows of the A tile: (S - 1) * R_max, at most 128
     int a_chunks;      // tensor-core expand: (S - 1) * R16 / 16 chunks of 16 (slot, rank) pairs, at most 8
     int tcx;           // U from the shrink kernel ahead, expand on the tensor cores (rank 0 of the cluster)
+    int tcl;           // U from the shrink kernel ahead, expand on the tensor cores (chunks dealt over the cluster)
     int kk;            // 64-column K slices per pipeline stage (> 1: 3-D / 4-D tensor maps)
     size_t smem;       // dynamic shared memory of the launch
 };

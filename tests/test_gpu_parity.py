@@ -439,14 +439,34 @@ def test_fused_shrink_edge_shapes(T, K, N, S, R):
 
 @pytest.mark.parametrize("T", [64, 300])
 def test_most_slots(T):
-    """S = 1024 slots, ids over all of them: the decode path's CUDA-core expand
-    and the prefill path's segment lists."""
+    """S = 1024 slots, ids over all of them: the decode path's chunk-dealt
+    expand and the prefill path's segment lists."""
     w = WL.random_case(seed=1024 + T, T=T, K=128, N=136, S=1024, R_max=8, base_frac=0.05)
     dw = DeviceWorkload(w, DEV)
     y = dw.run(0)
     torch.cuda.synchronize()
     assert L.last_device_error() == 0
     assert_parity(y, dw.oracle(0), f"S=1024, T={T}")
+
+
+@pytest.mark.parametrize("T,K,N,S,R", [
+    (256, 64, 128, 33, 128),     # one CTA per cluster: 32 slots x 8 chunks, many batches
+    (200, 192, 384, 40, 128),    # ragged token tile, two CTAs per cluster
+    (9, 4096, 256, 60, 64),      # eight CTAs per cluster, a few chunks: some CTAs get none
+])
+def test_chunk_dealt_expand_batches(T, K, N, S, R):
+    """The decode path's expand with U from the shrink kernel, when the slots'
+    ranks exceed what one CTA's expand holds: the (slot, 16-rank chunk) pairs
+    are dealt over the cluster's CTAs and added in batches."""
+    w = WL.random_case(seed=T * 13 + S, T=T, K=K, N=N, S=S, R_max=R, base_frac=0.1)
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    assert_parity(y, dw.oracle(0), f"chunk-dealt expand {T},{K},{N},{S},{R}")
+    slot0 = torch.as_tensor(w.ids == 0, device=DEV)
+    yb = dw.run(0, base_only=True)
+    assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
 
 
 def test_wide_output_takes_the_shrink_kernel():
