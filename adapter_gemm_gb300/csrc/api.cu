@@ -118,7 +118,10 @@ bool valid_sizes(int S, int R_max, int d_in) {
 
 int max_tiles_for(int T, int S) { return (T + kTileRows - 1) / kTileRows + S; }
 
-bool plan_needs_xsorted(int T) { return T > kSkinnyPathMaxT; }
+// Plans for batches that a target may send to the prefill kernel hold the
+// plan-ordered copy of x (and its expand operands); decode-sized plans stay
+// small (the static-scratch entry point relies on it).
+bool plan_needs_xsorted(int T) { return T > kSkinnyOnlyMaxT; }
 
 // Sub-buffer sizes of the plan workspace, in carve order.
 constexpr int kPlanParts = 14;
@@ -467,9 +470,22 @@ lora_status lora_plan_check(const lora_plan_t* plan, void* stream, int32_t* n_in
 }
 
 int lora_linear_path(int T, int d_in, int d_out) {
-    (void)d_in;
-    (void)d_out;
-    return T <= kSkinnyPathMaxT ? 0 : 1;
+    if (T <= kSkinnyOnlyMaxT) return 0;
+    if (T > kSkinnyPathMaxT) return 1;
+    // In between, the swap-AB kernel while its weight tiles (128 rows x 256
+    // tokens) can split K over clusters of two CTAs on every SM; with fewer
+    // splits the persistent kernel streams its operands better. Measured
+    // alone with adapters (us, swap-AB / persistent): 512 x 4096 -> 1024:
+    // 24.6 / 28.7; 300 x 4096 -> 4096: 29.1 / 30.7; 512 x 14336 -> 4096: 67.6 /
+    // 69.6; 512 x 4096 -> 4096: 30.6 / 28.7 (two splits, the one loss);
+    // 512 x 4096 -> 14336: 96.9 / 65.5 (one split). Up to 256 rows the plan
+    // holds no plan-ordered copy of x, so the swap-AB kernel runs there even
+    // where the persistent one would be faster (256 x 4096 -> 14336: 53.2 /
+    // 45.1; even at 160 rows, and slower below).
+    const int TN = ((T < kSkinnyMaxT ? T : kSkinnyMaxT) + 15) / 16 * 16;
+    const int units = ((d_out + 127) / 128) * ((T + TN - 1) / TN);
+    const int kb = (d_in + 63) / 64;
+    return (kb >= 2 && units * 2 <= num_sms()) ? 0 : 1;
 }
 
 static_assert(kMaxSlices == LORA_MAX_SLICES, "slice limit of the C ABI and the kernels");

@@ -11,7 +11,8 @@ constexpr int kTileRows = 16;       // plan work tiles, rows (== LORA_TILE_ROWS)
 constexpr int kMaxSlots = 1024;     // one plan thread per slot in the scans
 constexpr int kMaxRank = 128;       // R_max cap: shrink keeps R_max/8 MMA column tiles
 constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 256)
-constexpr int kSkinnyPathMaxT = 256; // batches up to this many rows take the swap-AB kernel
+constexpr int kSkinnyOnlyMaxT = 256; // batches up to this many rows always take the swap-AB kernel
+constexpr int kSkinnyPathMaxT = 640; // batches above this many rows always take the persistent 128 x 256 kernel
 constexpr int kStageURank = 64;     // the skinny epilogue stages U rows of rank <= 64
 constexpr int kCoreExpandMaxT = 8;  // decode batches up to this many rows expand on the CUDA cores
 constexpr int kBySlotMaxT = 64;     // up to this many rows the shrink groups rows by slot itself

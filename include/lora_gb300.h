@@ -206,8 +206,11 @@ lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* 
                              int d_out, const void* W, const lora_pool* pool, lora_plan_t* plan,
                              void* x_dev, int32_t* ids_dev, void* y_dev, void* stream);
 
-/* The kernel family lora_linear picks for these sizes: 0 = skinny (swap-AB,
- * split-K across a thread-block cluster), 1 = wide (persistent 128x256 tiles). */
+/* The kernel family lora_linear picks for these sizes on the current device:
+ * 0 = skinny (swap-AB, split-K across a thread-block cluster), 1 = wide
+ * (persistent 128x256 tiles). Up to 256 rows always 0, above 640 always 1; in
+ * between 0 while the skinny kernel's weight tiles can split K in two on
+ * every SM. */
 int lora_linear_path(int T, int d_in, int d_out);
 
 /* Most output slices one lora_linear_sliced call takes. */

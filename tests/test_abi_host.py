@@ -176,9 +176,17 @@ def test_plan_argument_errors(lib):
     assert lib.lora_plan(FAKE, 64, None, None) == EINVAL
 
 
-def test_path_choice_depends_on_shape_only(lib):
+def test_path_choice(lib):
+    """Decode-sized batches take the swap-AB kernel, large ones the persistent
+    kernel; in between, the swap-AB kernel while its weight tiles can split K
+    over clusters of two CTAs (the SM count on a host without a GPU is 148)."""
     assert lib.lora_linear_path(1, 4096, 4096) == 0
+    assert lib.lora_linear_path(128, 4096, 14336) == 0
     assert lib.lora_linear_path(256, 14336, 4096) == 0
-    assert lib.lora_linear_path(257, 4096, 4096) == 1
-    assert lib.lora_linear_path(512, 14336, 4096) == 1
+    assert lib.lora_linear_path(512, 4096, 1024) == 0
+    assert lib.lora_linear_path(256, 4096, 14336) == 0      # decode-sized plans hold no x_sorted
+    assert lib.lora_linear_path(300, 4096, 14336) == 1
+    assert lib.lora_linear_path(512, 4096, 14336) == 1
+    assert lib.lora_linear_path(300, 64, 1024) == 1          # one 64-column K slice: no split
+    assert lib.lora_linear_path(700, 4096, 1024) == 1
     assert lib.lora_linear_path(4096, 4096, 14336) == 1

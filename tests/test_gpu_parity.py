@@ -469,6 +469,23 @@ def test_chunk_dealt_expand_batches(T, K, N, S, R):
     assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
 
 
+@pytest.mark.parametrize("T,K,N,path", [
+    (640, 512, 1024, 0),         # three token tiles on the swap-AB kernel
+    (641, 512, 1024, 1),         # past the swap-AB kernel's range
+    (300, 512, 20480, 1),        # too many weight tiles to split K: the persistent kernel
+])
+def test_mid_sized_batches_on_either_kernel(T, K, N, path):
+    assert L.linear_path(T, K, N) == path
+    w = WL.random_case(seed=T + N, T=T, K=K, N=N, S=20, R_max=32, base_frac=0.1)
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    rows = sample_rows(w.ids, 160)
+    assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(0, rows=rows), f"T={T} N={N} path {path}")
+    slot0 = torch.as_tensor(w.ids == 0, device=DEV)
+    yb = dw.run(0, base_only=True)
+    assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
+
+
 def test_wide_output_takes_the_shrink_kernel():
     """Many weight tiles would re-read the A tile too often: U comes from the
     shrink kernel ahead (two kernels) and the expand runs on the tensor cores."""
