@@ -383,12 +383,18 @@ def test_fused_shrink_invalid_ids_and_mixed_ranks():
         assert torch.equal(y[r].view(torch.int16), yb[r].view(torch.int16))
 
 
-def test_tensor_core_expand_with_ids_from_previous_output():
+@pytest.mark.parametrize("T,S,R", [
+    (40, 6, 16),     # every slot's ranks fit one CTA's expand (rank 0 of the cluster adds it)
+    (40, 40, 32),    # the expand's chunks dealt over the cluster
+    (6, 40, 32),     # a batch of at most 8 rows: the CUDA-core expand
+])
+def test_tensor_core_expand_with_ids_from_previous_output(T, S, R):
     """The step's ids lie in the previous call's output on the same stream, so
     the GEMM may not read them before its wait: U comes from the shrink kernel
-    ahead (two kernels) and the expand still runs on the tensor cores."""
-    T, K, N = 40, 512, 256
-    w = WL.random_case(seed=23, T=T, K=K, N=N, S=6, R_max=16, ranks=[0, 16, 5, 12, 16, 9])
+    ahead (two kernels), and the GEMM groups the tokens after its wait."""
+    K, N = 512, 256
+    ranks = [0, 16, 5, 12, 16, 9] if S == 6 else None
+    w = WL.random_case(seed=23 + S + T, T=T, K=K, N=N, S=S, R_max=R, ranks=ranks)
     t = w.targets[0]
     W = t.W.to(DEV)
     pool = L.Pool(w.S, w.R_max, K, N, device=DEV)
@@ -408,8 +414,8 @@ def test_tensor_core_expand_with_ids_from_previous_output():
     torch.cuda.synchronize()
     assert L.last_device_error() == 0
     ref = O.lora_linear(f64(x), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, w.ids)
-    assert_parity(first, ref, "fused shrink")
-    assert_parity(y, ref, "shrink kernel, tensor-core expand")
+    assert_parity(first, ref, "first call")
+    assert_parity(y, ref, "ids from the previous output")
 
 
 FUSED_EDGES = [
