@@ -703,19 +703,39 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // plan-ordered copy of x are [T][d_in], W is [d_out][d_in]), so that a
         // stage's copies are as large as a wide tile's
         const int kk = (bn == 128 && d_in % 64 == 0 && d_in >= 128) ? 2 : 1;
-        CUtensorMap tmA, tmB, tmU, tmBs;
+        // With a short last wave of wide tiles (at most half the CTAs busy),
+        // that wave's tiles are split into 128-column halves, which need W's
+        // and B's maps with 128-row boxes too. Measured alone with adapters
+        // (us, split / not): T = 4096, 4096 -> 4096 (512 wide tiles on 152
+        // SMs): 100.9 / 104.4; 4096 x 14336 -> 4096: 325.6 / 335.9; 1500 x 4096
+        // -> 4096: 53.2 / 57.3; 2048 x 4096 -> 8192: 102.4 / 106.5.
+        const int m_tiles_w = m_tiles, t_w = m_tiles * ((d_out + bn - 1) / bn);
+        const int sm_w = num_sms();
+        int n_wide = t_w, tiles_total = t_w;
+        if (bn == 256 && d_out % 256 == 0 && t_w > sm_w) {
+            const int r = t_w % sm_w;
+            if (r > 0 && 2 * r <= sm_w) {
+                n_wide = t_w - r;
+                tiles_total = n_wide + 2 * r;
+            }
+        }
+        const bool halves = tiles_total > n_wide;
+        WideMaps maps;
         if (kk == 1) {
-            if (!make_tmap(&tmA, A, (uint64_t)d_in, (uint64_t)T, 64, 128) ||
-                !make_tmap(&tmB, W, (uint64_t)d_in, (uint64_t)d_out, 64, (uint32_t)bn))
+            if (!make_tmap(&maps.a, A, (uint64_t)d_in, (uint64_t)T, 64, 128) ||
+                !make_tmap(&maps.b, W, (uint64_t)d_in, (uint64_t)d_out, 64, (uint32_t)bn) ||
+                (halves && !make_tmap(&maps.b_half, W, (uint64_t)d_in, (uint64_t)d_out, 64, (uint32_t)bn / 2)))
                 return LORA_ECUDA;
         } else {
             const uint64_t da[3] = {64, (uint64_t)T, (uint64_t)d_in / 64}, pa[2] = {(uint64_t)d_in * 2, 128};
             const uint64_t db[3] = {64, (uint64_t)d_out, (uint64_t)d_in / 64}, pb[2] = {(uint64_t)d_in * 2, 128};
-            const uint32_t ba[3] = {64, 128, 2}, bbx[3] = {64, (uint32_t)bn, 2};
-            if (!make_tmap_nd(&tmA, A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B) ||
-                !make_tmap_nd(&tmB, W, 3, db, pb, bbx, CU_TENSOR_MAP_SWIZZLE_128B))
+            const uint32_t ba[3] = {64, 128, 2}, bbx[3] = {64, (uint32_t)bn, 2}, bbh[3] = {64, (uint32_t)bn / 2, 2};
+            if (!make_tmap_nd(&maps.a, A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                !make_tmap_nd(&maps.b, W, 3, db, pb, bbx, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                (halves && !make_tmap_nd(&maps.b_half, W, 3, db, pb, bbh, CU_TENSOR_MAP_SWIZZLE_128B)))
                 return LORA_ECUDA;
         }
+        if (!halves) maps.b_half = maps.b;     // unused
         const int R16 = plan ? (pool->R_max + 15) / 16 * 16 : 16;
         if (plan) {
             // expand operands: U hi|lo [T][2*R16] in plan order, B_pool [S][N][R_max]
@@ -723,13 +743,16 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
             const uint32_t bu[2] = {16, 128};
             const uint64_t db[3] = {(uint64_t)pool->R_max, (uint64_t)d_out, (uint64_t)pool->S};
             const uint64_t pb[2] = {(uint64_t)pool->R_max * 2, (uint64_t)d_out * pool->R_max * 2};
-            const uint32_t bb[3] = {16, (uint32_t)bn, 1};
-            if (!make_tmap_nd(&tmU, plan->U_hl, 2, du, pu, bu, CU_TENSOR_MAP_SWIZZLE_32B) ||
-                !make_tmap_nd(&tmBs, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B))
+            const uint32_t bb[3] = {16, (uint32_t)bn, 1}, bbh[3] = {16, (uint32_t)bn / 2, 1};
+            if (!make_tmap_nd(&maps.u, plan->U_hl, 2, du, pu, bu, CU_TENSOR_MAP_SWIZZLE_32B) ||
+                !make_tmap_nd(&maps.bs, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B) ||
+                (halves && !make_tmap_nd(&maps.bs_half, pool->B, 3, db, pb, bbh, CU_TENSOR_MAP_SWIZZLE_32B)))
                 return LORA_ECUDA;
+            if (!halves) maps.bs_half = maps.bs;
         } else {
-            tmU = tmA;                 // unused without a plan
-            tmBs = tmB;
+            maps.u = maps.a;           // unused without a plan
+            maps.bs = maps.b;
+            maps.bs_half = maps.b;
         }
         WideArgs a;
         a.y = static_cast<__nv_bfloat16*>(y);
@@ -743,14 +766,16 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         a.T = T;
         a.K = d_in;
         a.N = d_out;
-        a.m_tiles = m_tiles;
+        a.m_tiles = m_tiles_w;
         a.n_tiles = (d_out + bn - 1) / bn;
         a.bn = bn;
         a.kk = kk;
         a.kb_total = (d_in + 63) / 64;
-        int grid = a.m_tiles * a.n_tiles;
-        if (grid > num_sms()) grid = num_sms();
-        if (counted(launch_wide(tmA, tmB, tmU, tmBs, a, pdl, grid, st)) != cudaSuccess) return LORA_ECUDA;
+        a.n_wide = n_wide;
+        a.tiles_total = tiles_total;
+        int grid = tiles_total;
+        if (grid > sm_w) grid = sm_w;
+        if (counted(launch_wide(maps, a, pdl, grid, st)) != cudaSuccess) return LORA_ECUDA;
     }
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;
     set_last_out(st, y, y_bytes);

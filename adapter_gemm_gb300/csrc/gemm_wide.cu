@@ -17,6 +17,11 @@
 // The epilogue then only rounds and scatters each row back to its token, once.
 // Without a plan xs = x, t_i = i, and there are no expand steps.
 //
+// When the wide tiles end in a short last wave (at most half the CTAs), the
+// tiles of that wave are split into 128-column halves: every CTA's share then
+// ends within two thirds of a wide tile of the others' (a tile's time follows
+// its operand stream, 128 + width rows per K slice).
+//
 // One CTA per SM. Warp 0 lane 0 streams A (128 x 64) and B (256 x 64) tiles,
 // and the expand operands (U 128 x 16 hi and lo, B_s 256 x 16, 32-byte
 // swizzle), with TMA into a 4-stage ring; warp 1 lane 0 issues tcgen05.mma
@@ -57,11 +62,28 @@ struct WideCfg {
     static constexpr size_t kSmem = 1024 + (size_t)kStageBytes * kStages + 256 + 2 * (size_t)kMaxSegs * 16 + 16;
 };
 
+// Tile `tile` of the schedule: its 128-row block, first output column and
+// width. Tiles below n_wide walk the (block, BN-column strip) pairs with the
+// blocks fastest; each later pair is split into two tiles of BN / 2 columns.
+template <int BN>
+__device__ __forceinline__ void wide_tile(const WideArgs& a, int tile, int& mt, int& n0, int& wd) {
+    int p = tile, h = 0;
+    wd = BN;
+    if (tile >= a.n_wide) {
+        const int j = tile - a.n_wide;
+        p = a.n_wide + (j >> 1);
+        h = j & 1;
+        wd = BN / 2;
+    }
+    mt = p % a.m_tiles;
+    n0 = (p / a.m_tiles) * BN + h * (BN / 2);
+}
+
 template <int BN, int KK>
 __global__ void __launch_bounds__(kWdThreads, 1)
-gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmBs,
-                 WideArgs a) {
+gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
+    const CUtensorMap& tmA = maps.a;
+    const CUtensorMap& tmU = maps.u;
     using C = WideCfg<BN, KK>;
     constexpr int kWdBN = BN;
     constexpr int kWdStages = C::kStages;
@@ -82,15 +104,17 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     int* xcount = reinterpret_cast<int*>(xlist + 2 * kMaxSegs);                               // [2]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles_total = a.m_tiles * a.n_tiles;
+    const int n_tiles_total = a.tiles_total;
     const bool expand = a.mt_ptr != nullptr;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&maps.b);
+        if (n_tiles_total > a.n_wide) tma_prefetch_desc(&maps.b_half);
         if (expand) {
             tma_prefetch_desc(&tmU);
-            tma_prefetch_desc(&tmBs);
+            tma_prefetch_desc(&maps.bs);
+            if (n_tiles_total > a.n_wide) tma_prefetch_desc(&maps.bs_half);
         }
         for (int i = 0; i < kWdStages; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
@@ -122,22 +146,25 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             int it = 0, issued = 0, lt = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x, ++lt) {
-                const int mt = tile % a.m_tiles;
+                int mt, n0, wd;
+                wide_tile<BN>(a, tile, mt, n0, wd);
                 const int m0 = mt * kWdBM;
-                const int n0 = (tile / a.m_tiles) * kWdBN;
+                const CUtensorMap* tmB = wd == BN ? &maps.b : &maps.b_half;
+                const CUtensorMap* tmBs = wd == BN ? &maps.bs : &maps.bs_half;
+                const uint32_t stage_tx = KK * (kWdABytes + (uint32_t)wd * kWdBK * 2);
                 for (int ksi = 0; ksi < n_kst; ++ksi, ++it) {
                     const int st = it % kWdStages;
                     const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                     if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
                     const uint32_t sA = smem_u32(base + (size_t)st * kWdStageBytes);
                     const uint32_t fb = smem_u32(&full[st]);
-                    mbar_arrive_expect_tx(fb, kWdStageBytes);
+                    mbar_arrive_expect_tx(fb, stage_tx);
                     if (KK == 1) {
                         tma_load_2d(sA, &tmA, fb, ksi * kWdBK, m0);
-                        tma_load_2d(sA + kWdABytes, &tmB, fb, ksi * kWdBK, n0);
+                        tma_load_2d(sA + kWdABytes, tmB, fb, ksi * kWdBK, n0);
                     } else {           // KK slices of A, then KK slices of B
                         tma_load_3d(sA, &tmA, fb, 0, m0, ksi * KK);
-                        tma_load_3d(sA + KK * kWdABytes, &tmB, fb, 0, n0, ksi * KK);
+                        tma_load_3d(sA + KK * kWdABytes, tmB, fb, 0, n0, ksi * KK);
                     }
                     ++issued;
                 }
@@ -173,11 +200,11 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                         if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
                         const uint32_t sU = smem_u32(base + (size_t)st * kWdStageBytes);
                         const uint32_t fb = smem_u32(&full[st]);
-                        mbar_arrive_expect_tx(fb, 2 * kXuBytes + (uint32_t)n_sel * kXbBytes);
+                        mbar_arrive_expect_tx(fb, 2 * kXuBytes + (uint32_t)n_sel * (uint32_t)wd * 32u);
                         tma_load_2d(sU, &tmU, fb, ks * 16, m0);                       // U hi
                         tma_load_2d(sU + kXuBytes, &tmU, fb, a.R16 + ks * 16, m0);    // U lo
                         for (int j = 0; j < n_sel; ++j)                                // B_s
-                            tma_load_3d(sU + 2 * kXuBytes + (uint32_t)j * kXbBytes, &tmBs, fb, ks * 16, n0,
+                            tma_load_3d(sU + 2 * kXuBytes + (uint32_t)j * kXbBytes, tmBs, fb, ks * 16, n0,
                                         xlist[as * kMaxSegs + sel[j]].x);
                         ++issued;
                         ++it;
@@ -192,10 +219,16 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     } else if (warp == 1) {
         if (lane == 0) {
             // MMA issuer.
-            const uint32_t idesc = idesc_bf16_f32(kWdBM, kWdBN);
+            const uint32_t idesc_w = idesc_bf16_f32(kWdBM, kWdBN), idesc_h = idesc_bf16_f32(kWdBM, kWdBN / 2);
             int it = 0, lt = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < n_tiles_total && ok; tile += gridDim.x, ++lt) {
+                int mt_unused, n0_unused, wd;
+                wide_tile<BN>(a, tile, mt_unused, n0_unused, wd);
+                (void)mt_unused;
+                (void)n0_unused;
+                const uint32_t idesc = wd == BN ? idesc_w : idesc_h;
+                const uint32_t b_slice = (uint32_t)wd * kWdBK * 2;      // one K slice of the weight tile
                 const int as = lt & 1;
                 const uint32_t use = (uint32_t)(lt >> 1);
                 if (!mbar_wait(smem_u32(&tempty[as]), (use & 1u) ^ 1u, kErrAccFreeWait)) { ok = false; break; }
@@ -211,7 +244,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     const int n_sl = min(KK, a.kb_total - ksi * KK);
                     for (int q = 0; q < n_sl; ++q) {
                         const uint32_t sA = KK == 1 ? sA0 : sA0 + (uint32_t)q * kWdABytes;
-                        const uint32_t sB = KK == 1 ? sA0 + kWdABytes : sA0 + KK * kWdABytes + (uint32_t)q * C::kBBytes;
+                        const uint32_t sB = KK == 1 ? sA0 + kWdABytes : sA0 + KK * kWdABytes + (uint32_t)q * b_slice;
 #pragma unroll
                         for (int kk = 0; kk < kWdBK / 16; ++kk)
                             tc_mma_bf16(d, sdesc_sw128(sA + kk * 32), sdesc_sw128(sB + kk * 32), idesc,
@@ -272,8 +305,9 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++lt) {
             const int as = lt & 1;
             const uint32_t use = (uint32_t)(lt >> 1);
-            const int m0 = (tile % a.m_tiles) * kWdBM;
-            const int n0 = (tile / a.m_tiles) * kWdBN;
+            int mt, n0, wd;
+            wide_tile<BN>(a, tile, mt, n0, wd);
+            const int m0 = mt * kWdBM;
             // lane 0 of each epilogue warp waits (sleeping between tries)
             bool got = true;
             if (lane == 0) got = mbar_wait_sleep(smem_u32(&tfull[as]), use & 1u, kErrAccWait);
@@ -285,7 +319,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int t = valid ? (a.token_order ? a.token_order[i] : i) : 0;
             __nv_bfloat16* yrow = a.y + (size_t)t * a.ldy;
             const uint32_t tbase = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(as * kWdBN);
-            for (int c = 0; c < kWdBN; c += 16) {
+            for (int c = 0; c < wd; c += 16) {
                 float v[16];
                 tc_ld16(tbase + (uint32_t)c, v);
                 const int n = n0 + c;
@@ -313,9 +347,7 @@ gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 }
 
 template <int BN, int KK>
-static cudaError_t launch_wide_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
-                                  const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid,
-                                  cudaStream_t stream) {
+static cudaError_t launch_wide_bn(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
     const size_t smem = WideCfg<BN, KK>::kSmem;
     cudaError_t e = ensure_smem_attr((const void*)gemm_wide_kernel<BN, KK>, (BN == 256 ? 2 : 3) + (KK == 1 ? 0 : 2),
                                      smem);
@@ -334,16 +366,15 @@ static cudaError_t launch_wide_bn(const CUtensorMap& tmA, const CUtensorMap& tmB
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, gemm_wide_kernel<BN, KK>, tmA, tmB, tmU, tmBs, a);
+    return cudaLaunchKernelEx(&cfg, gemm_wide_kernel<BN, KK>, maps, a);
 }
 
-cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
-                        const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
+cudaError_t launch_wide(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
     if (a.kk == 2)
-        return a.bn == 128 ? launch_wide_bn<128, 2>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream)
-                           : launch_wide_bn<256, 2>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream);
-    return a.bn == 128 ? launch_wide_bn<128, 1>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream)
-                       : launch_wide_bn<256, 1>(tmA, tmB, tmU, tmBs, a, pdl, grid, stream);
+        return a.bn == 128 ? launch_wide_bn<128, 2>(maps, a, pdl, grid, stream)
+                           : launch_wide_bn<256, 2>(maps, a, pdl, grid, stream);
+    return a.bn == 128 ? launch_wide_bn<128, 1>(maps, a, pdl, grid, stream)
+                       : launch_wide_bn<256, 1>(maps, a, pdl, grid, stream);
 }
 
 cudaError_t wide_take_error(int* code) {

@@ -114,13 +114,21 @@ struct WideArgs {
     int m_tiles, n_tiles, kb_total;
     int bn;                         // output tile width: 256 or 128
     int kk;                         // 64-column K slices per stage: 1 or 2 (3-D tensor maps)
+    int n_wide;                     // tiles 0..n_wide-1 are bn wide, in (m, strip) order;
+    int tiles_total;                //   the rest split the following (m, strip) pairs in halves
+};
+
+// The prefill GEMM's operands: x (or x_sorted) [T][d_in] and W [d_out][d_in]
+// in 64-column slices, U hi|lo and the B pool for the expand steps; b_half and
+// bs_half are W's and B's maps with half-width boxes, for the split tail tiles.
+struct WideMaps {
+    CUtensorMap a, b, u, bs, b_half, bs_half;
 };
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream);
 cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream);
 cudaError_t launch_skinny(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream);
-cudaError_t launch_wide(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmU,
-                        const CUtensorMap& tmBs, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
+cudaError_t launch_wide(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
 cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* rows, int T, int T_all, int d_in,
                                __nv_bfloat16* out, cudaStream_t stream);
