@@ -709,12 +709,11 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // (us, split / not): T = 4096, 4096 -> 4096 (512 wide tiles on 152
         // SMs): 100.9 / 104.4; 4096 x 14336 -> 4096: 325.6 / 335.9; 1500 x 4096
         // -> 4096: 53.2 / 57.3; 2048 x 4096 -> 8192: 102.4 / 106.5.
-        const int m_tiles_w = m_tiles, t_w = m_tiles * ((d_out + bn - 1) / bn);
-        const int sm_w = num_sms();
+        const int t_w = m_tiles * ((d_out + bn - 1) / bn);
         int n_wide = t_w, tiles_total = t_w;
-        if (bn == 256 && d_out % 256 == 0 && t_w > sm_w) {
-            const int r = t_w % sm_w;
-            if (r > 0 && 2 * r <= sm_w) {
+        if (bn == 256 && d_out % 256 == 0 && t_w > sms) {
+            const int r = t_w % sms;
+            if (r > 0 && 2 * r <= sms) {
                 n_wide = t_w - r;
                 tiles_total = n_wide + 2 * r;
             }
@@ -766,15 +765,14 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         a.T = T;
         a.K = d_in;
         a.N = d_out;
-        a.m_tiles = m_tiles_w;
-        a.n_tiles = (d_out + bn - 1) / bn;
+        a.m_tiles = m_tiles;
         a.bn = bn;
         a.kk = kk;
         a.kb_total = (d_in + 63) / 64;
         a.n_wide = n_wide;
         a.tiles_total = tiles_total;
         int grid = tiles_total;
-        if (grid > sm_w) grid = sm_w;
+        if (grid > sms) grid = sms;
         if (counted(launch_wide(maps, a, pdl, grid, st)) != cudaSuccess) return LORA_ECUDA;
     }
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;

@@ -17,7 +17,7 @@
 // timing), rounds to bf16 and writes y once. No fp32 atomics, no extra pass
 // over y.
 //
-// The low-rank correction (SGMV's expand) is added in one of two ways:
+// The low-rank correction (SGMV's expand) is added in one of four ways:
 //  - shrink fused in (one token tile, every adapter's A rows in one 128-row
 //    tile): each CTA computes its K slice's share of U for every slot on the
 //    tensor cores (the A tile against the same x slices), and adds that
@@ -34,13 +34,14 @@
 //    (slot, 16-rank chunk) pairs of the slots that have tokens in the tile are
 //    dealt round-robin to the cluster's CTAs, which add their chunks in
 //    batches in the idle pipeline buffers;
-//  - U from the shrink kernel ahead: the owner adds U[t, :r] . B[s, n, :r]
-//    (fp32, j ascending) to the summed partials on the CUDA cores.
+//  - U from the shrink kernel ahead, at most 8 token rows and too many slots
+//    for one CTA's expand: the owner adds U[t, :r] . B[s, n, :r] (fp32, j
+//    ascending) to the summed partials on the CUDA cores.
 // Tokens on slot 0, on a rank-0 slot or with an invalid id get no correction.
 //
 // Roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues MMAs, warp 1 owns the
-// TMEM allocation; warps 2..7 read the tokens' slots (and, fused, stage Bcat)
-// during the K loop; all eight warps drain the accumulator (warp w reads TMEM
+// TMEM allocation; warps 2..7 read the tokens' slots (and, with one CTA's
+// expand, stage Bcat; with the dealt one, list the slot runs) during the K loop; all eight warps drain the accumulator (warp w reads TMEM
 // lanes 32 (w % 4).. and half of the token columns) and do the reduction.
 #include <cstdint>
 #include <cooperative_groups.h>
@@ -81,7 +82,8 @@ __host__ __device__ size_t skinny_grp_bytes(int TN) {
 // partials [ks][TN][128/ks] (128 x TN floats), then per mode
 //   late U on the CUDA cores:  U rows [TN][R_max] when staged;
 //   tensor-core expand:        Ucat high and low halves [chunk][2][TN][16] bf16, y staging;
-//   base only:                 y staging [TN][<= 128] bf16.
+//   base only, or the dealt expand (its batches use the whole region before
+//   the push):                 y staging [TN][<= 128] bf16.
 __host__ __device__ size_t skinny_epi_bytes(int TN, int R_max, bool stage_u, bool tc_expand, bool base_only) {
     const size_t red = (size_t)kWRows * TN * 4;
     const size_t ystage = (size_t)TN * kWRows * 2;

@@ -111,7 +111,7 @@ struct WideArgs {
     const int32_t* rank;            // [S]
     int R_max, R16;
     int T, K, N;
-    int m_tiles, n_tiles, kb_total;
+    int m_tiles, kb_total;          // 128-row blocks of T; 64-column K slices
     int bn;                         // output tile width: 256 or 128
     int kk;                         // 64-column K slices per stage: 1 or 2 (3-D tensor maps)
     int n_wide;                     // tiles 0..n_wide-1 are bn wide, in (m, strip) order;
