@@ -591,6 +591,13 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         const bool by_slot = path == 0 && T <= kBySlotMaxT;
         const int grid_x = by_slot ? pool->S - 1 : plan->max_tiles;
         sa.ks = by_slot ? slot_splits(grid_x, d_in) : shrink_splits(plan->max_tiles, d_in);
+        // Decode batches on the work-tile grid with a long K range: clusters of
+        // 8. Their shrink runs on the SMs the GEMM leaves free, and its U is
+        // what the GEMM's epilogue waits for. Measured on T = 256, 14336 ->
+        // 4096, 31 slots of ranks 8..64: 64.0 us per step with 8 splits, 78.4
+        // with 2 (the rule above) or 4. (The by-slot grid at T = 64 is slower
+        // with 8: 166.4 against 160.7 us per layer.)
+        if (path == 0 && !by_slot && d_in >= 8192) sa.ks = 8;
         if (grid_x > 0 && counted(launch_shrink(sa, grid_x, by_slot, pdl, st)) != cudaSuccess) return LORA_ECUDA;
         pdl = true;                    // the GEMM follows the shrink, which waited
     }
