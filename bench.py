@@ -587,7 +587,7 @@ def main():
 
 
 def run_reference(args, rank, world):
-    """The reference arm for this build is the CPU oracle, timed as it stands.
+    """The reference arm is the CPU oracle, timed as it stands.
 
     Each step runs the oracle on a bounded sample of the batch's rows (every
     target), sized so that warm-up plus timed steps take about

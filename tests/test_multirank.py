@@ -1,6 +1,6 @@
 """The N > 1 bench path on CPU: world-size-2 `gloo` process groups.
 
-The layer does not shard in this build: `bench.py --gpus N` runs N replicas
+The layer does not shard: `bench.py --gpus N` runs N replicas
 of the same per-GPU workload (weak scaling), with a barrier around the timed
 region and the slowest rank's time. These tests exercise that host logic
 without a GPU: the max-over-ranks reduction and the job throughput, each
