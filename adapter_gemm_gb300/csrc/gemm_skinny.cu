@@ -67,8 +67,7 @@ constexpr int kMaxBatch = 32;              // chunk-dealt expand: chunks per bat
 // token t is on slot a + 1, else 0), each token's slot - 1 (or -1) and the
 // slots' ranks.
 __host__ __device__ size_t skinny_xtab_bytes(int TN) {
-    // rounded to 16 bytes: the mbarriers placed after it need 8-byte alignment
-    return ((size_t)kBcatBytes + ((size_t)kMaxASlots * TN + TN + kMaxASlots) * 4 + 15) & ~(size_t)15;
+    return (size_t)kBcatBytes + ((size_t)kMaxASlots * TN + TN + kMaxASlots) * 4;
 }
 
 // The tile's tokens grouped by slot (kept apart from the pipeline's buffers,
