@@ -248,11 +248,11 @@ cudaError_t counted(cudaError_t e) {
     return e;
 }
 
-// The kernels of a lora_linear call start (programmatic dependent launch)
-// before the kernel ahead of them on the stream has finished, and read their
-// inputs early. The only kernels of this library that write caller-visible
-// memory are the GEMMs (y), so per stream the output range of the last
-// lora_linear is kept: an input that overlaps it is read only after the wait.
+// The kernels of a call start (programmatic dependent launch) before the
+// kernel ahead of them on the stream has finished, and request their first
+// stages of weights before they wait for it. The GEMMs write y, so per stream
+// the output range of the last lora_linear is kept: weights or a pool that
+// overlap it (never expected) turn the early start off.
 struct Range { uintptr_t lo = 0, hi = 0; };
 std::mutex g_range_mu;
 std::map<cudaStream_t, Range> g_last_out;
@@ -451,10 +451,8 @@ lora_status lora_plan(const int32_t* ids, int T, lora_plan_t* plan, void* stream
     p.S = plan->S;
     plan->ids = ids;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The plan kernel reads the ids before it waits for the kernels ahead of it,
-    // unless they alias the output of the previous lora_linear on this stream.
-    const bool pdl = !overlaps(last_out(st), ids, (size_t)T * 4);
-    if (counted(launch_plan(ids, T, p, pdl, st)) != cudaSuccess) return LORA_ECUDA;
+    // The plan kernel waits for the kernel ahead of it before it reads the ids.
+    if (counted(launch_plan(ids, T, p, true, st)) != cudaSuccess) return LORA_ECUDA;
     return LORA_OK;
 }
 
@@ -524,12 +522,12 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
     const int n_sl = slices ? slices->n : 1;
     const size_t y_bytes = ((size_t)(T - 1) * ldy + d_out) * 2;
 
-    // Inputs written by the previous lora_linear on this stream are read only
-    // after the wait; weights or pool aliasing it (never expected) turn the
-    // early start off altogether.
+    // The first kernel of the call reads x and the ids only after its wait for
+    // the kernel ahead, which may be the one that wrote them. Weights or a
+    // pool aliasing the previous output on this stream (never expected) turn
+    // the early start off altogether.
     const Range prev = last_out(st);
-    const bool x_early = !overlaps(prev, x, (size_t)T * d_in * 2) &&
-                         !(plan && overlaps(prev, plan->ids, (size_t)T * 4));
+    bool x_early = false, ids_early = false;
     bool pdl = !overlaps(prev, W, (size_t)d_out * d_in * 2);
     if (plan)
         for (int q = 0; q < n_sl; ++q)
@@ -538,11 +536,8 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
     // Decode batches of one token tile, with a pool whose adapter slots
     // (1..S-1, R_max ranks each, rounded up to 16) fit one 128-row tile,
     // compute U and the expand inside the GEMM (tensor cores: that A tile
-    // against each K slice of x, then Bcat against U): no shrink kernel, and
-    // everything but the stores of y comes before the GEMM's wait. The tokens'
-    // slots are read during the K loop, so the ids must not come from the
-    // kernel ahead.
-    const bool ids_early = !plan || !overlaps(prev, plan->ids, (size_t)T * 4);
+    // against each K slice of x, then Bcat against U): no shrink kernel. The
+    // tokens' slots are read during the K loop by otherwise idle warps.
     const int r16 = plan ? (pool->R_max + 15) / 16 * 16 : 0;
     // The expand runs on the tensor cores (Bcat against U) when every adapter
     // slot's ranks (rounded up to 16) fit 128 pairs; else on the CUDA cores.
@@ -556,7 +551,7 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
     const double a_rereads = plan ? (double)((d_out + 127) / 128) * ((T + 63) / 64) * (pool->S - 1) * pool->R_max *
                                         d_in * 2.0
                                   : 0.0;
-    const bool fuse = tc_expand && ids_early && (slices || a_rereads <= kFuseMaxAReread);
+    const bool fuse = tc_expand && (slices || a_rereads <= kFuseMaxAReread);
     // Otherwise, with U from the shrink kernel and more slots than the
     // rank-0 expand holds, the expand's (slot, 16-rank) chunks are dealt over
     // the cluster and run on the tensor cores, except for batches of at most
@@ -584,7 +579,6 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         sa.T = T;
         sa.K = d_in;
         sa.R_max = pool->R_max;
-        sa.x_early = x_early ? 1 : 0;
         // Small decode batches group rows by slot inside the shrink, so it need
         // not wait for the plan kernel; larger ones use the plan's work tiles,
         // which spread a heavily used adapter's rows over many CTAs.
@@ -598,8 +592,14 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // with 2 (the rule above) or 4. (The by-slot grid at T = 64 is slower
         // with 8: 166.4 against 160.7 us per layer.)
         if (path == 0 && !by_slot && d_in >= 8192) sa.ks = 8;
-        if (grid_x > 0 && counted(launch_shrink(sa, grid_x, by_slot, pdl, st)) != cudaSuccess) return LORA_ECUDA;
-        pdl = true;                    // the GEMM follows the shrink, which waited
+        if (grid_x > 0) {
+            if (counted(launch_shrink(sa, grid_x, by_slot, pdl, st)) != cudaSuccess) return LORA_ECUDA;
+            // The GEMM follows the shrink kernel, which waited for every kernel
+            // ahead of it before it let the GEMM start and writes neither x nor
+            // the ids: the GEMM may read both before its own wait (for U).
+            pdl = true;
+            x_early = ids_early = true;
+        }
     }
 
     ExpandArgs ex;
@@ -878,9 +878,7 @@ lora_status lora_linear_sliced(const void* x, const void* W, int T, int d_in, in
     // shrink fused in) and no weight tile straddles two slices; else one
     // call per slice, each writing its columns of y.
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const Range prev = last_out(st);
-    const bool ids_early = !overlaps(prev, plan->ids, (size_t)T * 4);
-    bool one = lora_linear_path(T, d_in, N) == 0 && T <= 64 && ids_early && plan->S >= 2 &&
+    bool one = lora_linear_path(T, d_in, N) == 0 && T <= 64 && plan->S >= 2 &&
                (plan->S - 1) * ((plan->R_max + 15) / 16 * 16) <= 128;
     for (int q = 0; q + 1 < n_slices; ++q) one = one && d_outs[q] % 128 == 0;
     if (one) {

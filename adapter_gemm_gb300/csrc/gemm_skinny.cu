@@ -556,10 +556,11 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
     // larger copies stream faster). Weights are never written by the kernels
     // this one waits for, so the first `stages` stages of weights are
     // requested before the wait - right after the barriers exist, while warp 1
-    // still allocates tensor memory - and x too unless the host saw that the
-    // previous kernel writes it. With the shrink fused in, each stage also
-    // holds the A rows of every adapter slot of the pool (slots 1..S-1, R_max
-    // rows each) for the same slices: the A tile.
+    // still allocates tensor memory - and x too when the kernel ahead is this
+    // call's shrink kernel (which waited for x's producer and does not write
+    // x). With the shrink fused in, each stage also holds the A rows of every
+    // adapter slot of the pool (slots 1..S-1, R_max rows each) for the same
+    // slices: the A tile.
     const int nst = (nkb + KK - 1) / KK;                          // stages of this CTA's K range
     const int pre = min(nst, stages);
     const uint32_t tx = (uint32_t)KK * (kWTileBytes + x_tile_bytes + (fuse ? a_slice : 0u));
@@ -608,12 +609,9 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // The next kernel of the stream may start its prologue now.
-    pdl_trigger();
-
     bool ok = true;
     if (warp == 0 && lane == 0) {
-        if (!a.x_early) pdl_wait();
+        if (!a.x_early) pdl_wait_trigger();     // x may come from the kernel ahead
         int issued = 0;
         for (int i = 0; i < nst && ok; ++i) {
             const int st = i % stages;
@@ -667,12 +665,15 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
         }
         tc_commit(smem_u32(accf));     // fires once every MMA above has completed
     } else if (warp >= 2 && tce) {
-        // Idle during the K loop: Bcat, and the token tables when the ids may
-        // be read before the wait.
+        // Idle during the K loop: Bcat (a weight), then, once the ids may be
+        // read (they may come from the kernel ahead), the token tables.
         stage_bcat(a, sv, bcat, n0, (int)threadIdx.x - 64, kSkThreads - 64);
-        if (a.ids_early) expand_tables(a, sv, msc, tact, srank, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64);
-    } else if (warp >= 2 && (late_u || tcl) && a.ids_early) {
-        // Idle during the K loop: group the tokens and fetch B's rows to L2.
+        if (!a.ids_early) pdl_wait_trigger();
+        expand_tables(a, sv, msc, tact, srank, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64);
+    } else if (warp >= 2 && (late_u || tcl)) {
+        // Idle during the K loop: once the ids may be read, group the tokens
+        // and fetch B's rows to L2.
+        if (!a.ids_early) pdl_wait_trigger();
         group_tokens(a, sv, gp, t0, n_tok, (int)threadIdx.x - 64, kSkThreads - 64, n_lo, n_rows, rows_per);
         if (tcl) slot_runs(gp, run_g, cbase, tab + 5 * kMaxBatch + 2, (int)threadIdx.x - 64, kSkThreads - 64);
     }
@@ -700,12 +701,7 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
             const int n16 = a.a_chunks * 2 * TN * kChunkRowBytes / 16;
             for (int q = threadIdx.x; q < n16; q += kSkThreads) z[q] = make_uint4(0, 0, 0, 0);
         }
-        if (tcx) {
-            // U (and, when the host could not rule out that the kernel ahead
-            // writes them, the ids) come from the kernels before this one.
-            pdl_wait();
-            if (!a.ids_early) expand_tables(a, sv, msc, tact, srank, t0, n_tok, (int)threadIdx.x, kSkThreads);
-        }
+        if (tcx) pdl_wait_trigger();           // U comes from the kernel ahead
         __syncthreads();
         const size_t lo_off = (size_t)TN * kChunkRowBytes;
         if (fuse) {
@@ -801,13 +797,7 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
         if (a.ks > 1) cluster_wait_acquire();    // every peer's buffers are free
     } else {
         if (tcl) {
-            // U (and, when the host could not rule out that the kernel ahead
-            // writes them, the ids) come from the kernels before this one.
-            pdl_wait();
-            if (!a.ids_early) {
-                group_tokens(a, sv, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
-                slot_runs(gp, run_g, cbase, tab + 5 * kMaxBatch + 2, (int)threadIdx.x, kSkThreads);
-            }
+            pdl_wait_trigger();                // U comes from the kernel ahead
             __syncthreads();
             const size_t body = pipe > epi_bytes ? pipe : epi_bytes;
             const size_t chunk = (size_t)kWRows * kChunkRowBytes + (size_t)2 * TN * kChunkRowBytes;
@@ -868,7 +858,7 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
                            pack_bf16x2(s1.z, s1.w));
         }
         __syncthreads();
-        pdl_wait();
+        pdl_wait_trigger();
         const int v8 = n_rows >> 3;                   // n_rows is a multiple of 8
         for (int q = threadIdx.x; q < n_tok * v8; q += kSkThreads) {
             const int t = q / v8, c = q - t * v8;
@@ -906,18 +896,12 @@ gemm_skinny_kernel(const __grid_constant__ SkinnyMaps maps, const __grid_constan
         };
         uint4 bc[8], bn[8];
         // B is a weight: the first item's row is requested before the wait
-        // when the groups are already known
-        bool b_loaded = false;
-        if (a.ids_early && (int)threadIdx.x < (*gp.n_groups << lg)) {
-            load_b(threadIdx.x, bc);
-            b_loaded = true;
-        }
-        // U comes from the kernels before this one, and so do the ids when
-        // the host could not rule that out: only from here on does the
-        // epilogue depend on them.
-        pdl_wait();
-        if (!a.ids_early)
-            group_tokens(a, sv, gp, t0, n_tok, (int)threadIdx.x, kSkThreads, n_lo, n_rows, rows_per);
+        // (the groups were built during the K loop)
+        const bool b_loaded = (int)threadIdx.x < (*gp.n_groups << lg);
+        if (b_loaded) load_b(threadIdx.x, bc);
+        // U comes from the kernel ahead: only from here on does the epilogue
+        // depend on it.
+        pdl_wait_trigger();
         if (a.stage_u) {
             const int R4 = R >> 2;
             for (int q = threadIdx.x; q < n_tok * R4; q += kSkThreads) {

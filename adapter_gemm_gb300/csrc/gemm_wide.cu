@@ -137,8 +137,8 @@ gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    pdl_trigger();
-    pdl_wait();
+    // x (or x_sorted), U and the plan come from the kernels ahead.
+    pdl_wait_trigger();
 
     if (warp == 0) {
         if (lane == 0) {

@@ -32,7 +32,6 @@ struct PlanArgs {
     int32_t* mt_ptr;        // [ceil(T/128)+1] or null: per 128-row block, first entry of mt_seg
     int32_t* mt_seg;        // [ceil(T/128)+S][4]: (slot, first row, end row, block), rows block-local
     int S;
-    int stage;              // build the row arrays in shared memory, store them after the wait
 };
 
 struct ShrinkArgs {
@@ -49,7 +48,6 @@ struct ShrinkArgs {
     int R16;                     // R_max rounded up to 16
     __nv_bfloat16* x_sorted;     // [T, K] or null
     int T, K, R_max, ks;
-    int x_early;                 // x is not written by the kernel this one follows
 };
 
 // Expand operands of the decode GEMM's epilogue. ids == null means base only

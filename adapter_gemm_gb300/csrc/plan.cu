@@ -20,10 +20,9 @@
 // Then the active-slot list and the work tiles (each slot's segment cut every
 // LORA_TILE_ROWS rows) come from two more prefix sums over slots.
 //
-// The kernel is launched as a dependent of the previous kernel of the stream,
-// whose kernels may still read the plan arrays. It reads only the ids before
-// it waits for them, and, when the batch's row arrays fit in shared memory,
-// builds the whole plan before the wait, so that after it only stores remain.
+// The kernel is launched as a dependent of the previous kernel of the stream.
+// That kernel may still read the plan arrays, and may be the one that wrote
+// the ids, so the plan kernel waits for it before it reads or writes anything.
 #include <cstdint>
 #include <cuda_runtime.h>
 #include "ptx.cuh"
@@ -69,14 +68,13 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     const int S = p.S;
     int* wc = smem;                       // [kPlanWarps][S] per-warp slot counts, then cursors
     int* tot = smem + kPlanWarps * S;     // [S] per-slot totals
-    int* st_order = tot + S;              // [T] token_order, staged (p.stage)
-    int* st_slot = st_order + T;          // [T] slot_of_token, staged (p.stage)
     __shared__ int warp_tot[33];
     __shared__ int s_invalid;
 
-    // The next kernel of the chain may start its prologue; it waits for this
-    // grid to finish before it reads the plan.
-    pdl_trigger();
+    // The ids may come from the kernel ahead, which may also still read the
+    // plan arrays: wait for it, then let the next kernel start its prologue
+    // (it waits for this grid before it reads the plan).
+    pdl_wait_trigger();
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < kPlanWarps * S; i += kPlanThreads) wc[i] = 0;
@@ -101,11 +99,6 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) n_bad += __shfl_xor_sync(0xffffffffu, n_bad, d);
     if (lane == 0 && n_bad) atomicAdd(&s_invalid, n_bad);
-    // The plan arrays may still be read by the kernels ahead of this one, so no
-    // global write comes before the wait. With staging, the whole plan is built
-    // in shared memory and registers first and only stored after the wait;
-    // without it (batches too large to stage) the wait comes here.
-    if (!p.stage) pdl_wait();
     __syncthreads();
 
     // Per slot: exclusive prefix over warps (in place) and the slot total.
@@ -129,8 +122,8 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     __syncthreads();
 
     // Pass 2: stable scatter of row ids.
-    int32_t* order_out = p.stage ? st_order : p.token_order;
-    int32_t* slot_out = p.stage ? st_slot : p.slot_of_token;
+    int32_t* order_out = p.token_order;
+    int32_t* slot_out = p.slot_of_token;
     for (int base = lo; base < hi; base += 32) {
         const int t = base + lane;
         const bool valid = t < hi;
@@ -157,14 +150,6 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     int n_tiles = 0;
     const int t_pos = block_exclusive_scan(n_t, warp_tot, n_tiles);
 
-    if (p.stage) {
-        pdl_wait();
-        __syncthreads();
-        for (int i = tid; i < T; i += kPlanThreads) {
-            p.token_order[i] = st_order[i];
-            p.slot_of_token[i] = st_slot[i];
-        }
-    }
     if (tid < S) {
         p.counts[tid] = my_cnt;
         p.indptr[tid] = start;
@@ -210,21 +195,11 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     }
 }
 
-// Shared memory of the plan kernel; `stage` says whether the row arrays are
-// staged there too (batches whose arrays fit).
-size_t plan_smem_bytes(int T, int S, bool* stage) {
-    const size_t counts = sizeof(int) * (size_t)(kPlanWarps + 1) * S;
-    const size_t rows = sizeof(int) * (size_t)2 * T;
-    const bool st = counts + rows <= (size_t)160 * 1024;
-    if (stage) *stage = st;
-    return counts + (st ? rows : 0);
-}
+// Shared memory of the plan kernel: per-warp slot counts and slot totals.
+size_t plan_smem_bytes(int S) { return sizeof(int) * (size_t)(kPlanWarps + 1) * S; }
 
-cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p_in, bool pdl, cudaStream_t stream) {
-    PlanArgs p = p_in;
-    bool stage = false;
-    const size_t smem = plan_smem_bytes(T, p.S, &stage);
-    p.stage = stage ? 1 : 0;
+cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream) {
+    const size_t smem = plan_smem_bytes(p.S);
     cudaError_t e = ensure_smem_attr((const void*)plan_kernel, 0, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

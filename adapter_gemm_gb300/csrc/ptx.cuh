@@ -176,11 +176,25 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------- PDL -------
+// Programmatic dependent launch. Every kernel of this library lets the next
+// kernel of its stream start (launch_dependents) only after its own wait for
+// the kernels ahead of it has returned: when a kernel starts, every kernel
+// before its immediate predecessor has then completed and its writes are
+// visible, so the only work that may still run beside it is that predecessor.
+// A kernel reads, before its own wait, only weights (W and the pool, which no
+// running kernel writes) and buffers that its immediate predecessor - a kernel
+// of the same library call that does not write them - left untouched.
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// The wait, then the trigger: the one form used before a kernel's first read
+// of anything the kernels ahead of it may write.
+__device__ __forceinline__ void pdl_wait_trigger() {
+    pdl_wait();
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------- tcgen05 ---

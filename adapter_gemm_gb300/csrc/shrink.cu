@@ -115,13 +115,12 @@ __device__ __forceinline__ void store_u(float* U, __nv_bfloat16* U_hl, const int
 // pushes its partial of those rows into the owner's `recv` (plain stores into
 // the peer's shared memory), then the owner sums what it received in rank
 // order. Earlier readers of U must be done before the stores: the caller has
-// waited for them, or passes wait_first and the wait comes right before the
-// stores, after the reduction.
+// waited for them.
 template <int NT>
 __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], float (*part)[16][NT * 8 + 1],
                                                     float* recv, const int* tok, int n, int rc8, float sc,
                                                     float* U, int R_max, int ks, __nv_bfloat16* U_hl = nullptr,
-                                                    int R16 = 0, int pos0 = 0, bool wait_first = false) {
+                                                    int R16 = 0, int pos0 = 0) {
     constexpr int RC = NT * 8;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -148,7 +147,6 @@ __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], f
             st_cluster_f32(mapa_shared(rbase, (uint32_t)owner) + (uint32_t)(((me * rows_per + lr) * RC + col) * 4), v);
         }
         cluster.sync();                               // every push has landed
-        if (wait_first) pdl_wait();
         const int wc = U_hl ? R16 : rc8;
         for (int el = threadIdx.x; el < rows_per * wc; el += kShrinkThreads) {
             const int lr = el / wc, col = el % wc;
@@ -161,7 +159,6 @@ __device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], f
             if (row < n) store_u(U, U_hl, tok, row, col, col < rc8 ? sc * v : 0.f, R_max, R16, pos0);
         }
     } else {
-        if (wait_first) pdl_wait();
         const int wc = U_hl ? R16 : rc8;
         for (int el = threadIdx.x; el < 16 * wc; el += kShrinkThreads) {
             const int row = el / wc, col = el % wc;
@@ -185,10 +182,10 @@ shrink_tiles_kernel(ShrinkArgs a) {
     __shared__ float recv[16 * RC];
     __shared__ int tok[16];
 
-    // The next kernel may start its prologue; this one needs the plan, and the
-    // previous call's readers of U / x_sorted must be done, before it goes on.
-    pdl_trigger();
-    pdl_wait();
+    // This kernel needs the plan, and the previous call's readers of U /
+    // x_sorted must be done, before it goes on; then the next kernel may start
+    // its prologue.
+    pdl_wait_trigger();
 
     const int n_tiles = *a.n_tiles;
     const int tile_idx = blockIdx.x;
@@ -224,9 +221,8 @@ shrink_tiles_kernel(ShrinkArgs a) {
 
 // Decode-sized batches (T <= 256): one cluster of ks CTAs (split along K) per
 // adapter slot s >= 1. The CTA finds the rows on its slot from the step's ids
-// itself (ascending, so the same grouping the plan would give), which lets it
-// run before the plan kernel has finished: it reads only inputs (ids, x, the
-// pool) until it stores U, and waits for the kernels before it only then.
+// itself (ascending, so the same grouping the plan would give); it needs no
+// plan arrays.
 template <int NT>
 __global__ void __launch_bounds__(kShrinkThreads)
 shrink_by_slot_kernel(ShrinkArgs a) {
@@ -236,7 +232,9 @@ shrink_by_slot_kernel(ShrinkArgs a) {
     __shared__ int rows[kSkinnyMaxT];
     __shared__ int wtot[4];
 
-    pdl_trigger();
+    // The ids and x may come from the kernel ahead, which may also still read
+    // U: wait for it first.
+    pdl_wait_trigger();
     const int s = blockIdx.x + 1;
     const int r = min(a.rank[s], a.R_max);           // written only by the synchronous install
     // rows on slot s, ascending: two ids per thread, then a block prefix sum
@@ -263,11 +261,7 @@ shrink_by_slot_kernel(ShrinkArgs a) {
     const int pos = before + inc - f_a - f_b;
     if (f_a) rows[pos] = t_a;
     if (f_b) rows[pos + f_a] = t_b;
-    if (n_rows == 0) {                 // no rows (or rank 0): same for the whole cluster
-        pdl_wait();
-        return;
-    }
-    if (!a.x_early) pdl_wait();        // x may come from the kernel before this one
+    if (n_rows == 0) return;           // no rows (or rank 0): same for the whole cluster
     __syncthreads();
 
     const int g = lane >> 2;
@@ -284,10 +278,8 @@ shrink_by_slot_kernel(ShrinkArgs a) {
         float acc[NT][4];
         shrink_accumulate<NT>(acc, a.x + (size_t)t0 * K, a.x + (size_t)t1 * K, v0, v1, nullptr, nullptr,
                               Ablk, K, nt_used, k_lo, k_hi, true);
-        // earlier readers of U must be done before it is written: the wait
-        // comes after the cluster's reduction, right before the stores
         shrink_reduce_store<NT>(acc, part, recv, rows + g0, min(16, n_rows - g0), nt_used * 8, sc, a.U,
-                                a.R_max, a.ks, nullptr, 0, 0, true);
+                                a.R_max, a.ks);
     }
 }
 

@@ -84,12 +84,9 @@ def test_mixed_down_full():
     _full_check(WL.mixed_down())
 
 
-def test_gateup_prefill_sampled():
-    w = WL.gateup_prefill()
-    dw = DeviceWorkload(w, DEV)
-    y = dw.run(0)
-    rows = sample_rows(w.ids, 96)
-    assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(0, rows=rows), w.name)
+def test_gateup_prefill_full():
+    """Every element of the 4096 x 14336 output against the oracle."""
+    _full_check(WL.gateup_prefill())
 
 
 @pytest.mark.parametrize("T", WL.SWEEP_T)
@@ -100,6 +97,16 @@ def test_layer_sweep(T):
     for i, t in enumerate(w.targets):
         y = dw.run(i)
         assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(i, rows=rows), f"{w.name}/{t.name}")
+
+
+def test_layer_sweep_T4096_whole_targets():
+    """The prefill-sized sweep: every element of two targets' outputs (the
+    widest, gate 4096 -> 14336, and the long-K down 14336 -> 4096)."""
+    w = WL.layer_sweep(4096)
+    dw = DeviceWorkload(w, DEV)
+    for i, t in enumerate(w.targets):
+        if t.name in ("gate_proj", "down_proj"):
+            assert_parity(dw.run(i), dw.oracle(i), f"{w.name}/{t.name}")
 
 
 # ------------------------------------------------------------ slot 0 rows ----
@@ -294,11 +301,12 @@ def test_row_offsets_beyond_int32():
 
 
 # --------------------------------------------- back-to-back calls, no sync ----
-# The kernels start before the kernel ahead of them has finished and read their
-# inputs early when the host can tell those are not that kernel's output. These
-# tests chain calls on one stream with no synchronisation in between: each
-# step's input is the previous step's output, and the same plan object (its
-# arrays and U) is rebuilt for every step.
+# The kernels start before the kernel ahead of them has finished (programmatic
+# dependent launch) and request their first weight stages early; a call's
+# first kernel reads x and the ids only after its wait. These tests chain calls
+# on one stream with no synchronisation in between: each step's input is the
+# previous step's output, and the same plan object (its arrays and U) is
+# rebuilt for every step.
 
 def _chained_steps(T, K, S, R, n_steps, base_only=False, seed=3):
     w = WL.random_case(seed=seed, T=T, K=K, N=K, S=S, R_max=R)
@@ -343,6 +351,49 @@ def test_chained_prefill_steps():
     _chained_steps(T=300, K=512, S=12, R=16, n_steps=3)       # the wide kernel
 
 
+@pytest.mark.parametrize("T,K,S,R", [(64, 1024, 9, 16), (48, 1024, 20, 16), (300, 512, 12, 16)])
+def test_input_written_two_calls_back_and_by_a_foreign_kernel(T, K, S, R):
+    """Inputs that are not the previous call's output but may still be in
+    flight: y1 = f(x0); y2 = f(x1); y3 = f(y1) (y1 written two calls back), and
+    x written by a torch kernel right before the call, and ids written by a
+    torch kernel right before the plan - all with no synchronisation. Covers
+    the fused decode shrink, the shrink kernel ahead of the decode GEMM, and the
+    prefill kernel."""
+    w = WL.random_case(seed=77, T=T, K=K, N=K, S=S, R_max=R)
+    t = w.targets[0]
+    W = t.W.to(DEV)
+    pool = L.Pool(S, R, K, K, device=DEV)
+    pool.load_padded(t.A, t.B, t.rank, t.alpha)
+    ids_np = w.ids.astype(np.int32)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    plan = L.Plan(T, S, R, K, device=DEV).build(ids)
+    x0 = w.x.to(DEV)
+    x1 = (x0 * -1).contiguous()
+    x_src = (x0 * 0.5).contiguous()
+    ids_src = torch.from_numpy(np.roll(ids_np, 3)).to(DEV)
+    ids_dst = torch.zeros_like(ids)
+    x_dst = torch.empty_like(x0)
+    plan2 = L.Plan(T, S, R, K, device=DEV)
+    torch.cuda.synchronize()
+    y1 = L.linear(x0, W, pool, plan)
+    y2 = L.linear(x1, W, pool, plan)
+    y3 = L.linear(y1, W, pool, plan)
+    x_dst.copy_(x_src)                       # a torch kernel writes x ...
+    y4 = L.linear(x_dst, W, pool, plan)      # ... right before the call reads it
+    torch.add(ids_src, 0, out=ids_dst)       # a torch kernel writes the ids ...
+    plan2.build(ids_dst)                     # ... right before the plan reads them
+    y5 = L.linear(x0, W, pool, plan2)
+    torch.cuda.synchronize()
+    assert L.last_device_error() == 0
+    f = lambda x, i: O.lora_linear(f64(x), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, i)
+    r1 = f(x0, ids_np)
+    assert_parity(y1, r1, "y1 = f(x0)")
+    assert_parity(y2, f(x1, ids_np), "y2 = f(x1)")
+    assert_parity(y3, f(y1, ids_np), "y3 = f(y1), y1 two calls back")
+    assert_parity(y4, f(x_src, ids_np), "x written by a torch kernel")
+    assert_parity(y5, f(x0, np.roll(ids_np, 3)), "ids written by a torch kernel")
+
+
 def test_one_plan_many_targets_without_sync():
     """Several layers of one step share the plan (and its U), back to back."""
     T, K, S, R = 64, 512, 20, 16
@@ -383,15 +434,16 @@ def test_fused_shrink_invalid_ids_and_mixed_ranks():
         assert torch.equal(y[r].view(torch.int16), yb[r].view(torch.int16))
 
 
-@pytest.mark.parametrize("T,S,R", [
-    (40, 6, 16),     # every slot's ranks fit one CTA's expand (rank 0 of the cluster adds it)
-    (40, 40, 32),    # the expand's chunks dealt over the cluster
-    (6, 40, 32),     # a batch of at most 8 rows: the CUDA-core expand
+@pytest.mark.parametrize("T,S,R,kernels", [
+    (40, 6, 16, 1),     # every slot's ranks fit one CTA's expand: the shrink fused in
+    (40, 40, 32, 2),    # the expand's chunks dealt over the cluster, U from the shrink kernel
+    (6, 40, 32, 2),     # a batch of at most 8 rows: the CUDA-core expand
 ])
-def test_tensor_core_expand_with_ids_from_previous_output(T, S, R):
+def test_tensor_core_expand_with_ids_from_previous_output(T, S, R, kernels):
     """The step's ids lie in the previous call's output on the same stream, so
-    the GEMM may not read them before its wait: U comes from the shrink kernel
-    ahead (two kernels), and the GEMM groups the tokens after its wait."""
+    no kernel may read them before its wait for the kernel ahead: the fused
+    GEMM's idle warps wait before they build the token tables, the shrink
+    kernel waits before it reads them."""
     K, N = 512, 256
     ranks = [0, 16, 5, 12, 16, 9] if S == 6 else None
     w = WL.random_case(seed=23 + S + T, T=T, K=K, N=N, S=S, R_max=R, ranks=ranks)
@@ -410,7 +462,7 @@ def test_tensor_core_expand_with_ids_from_previous_output(T, S, R):
     plan.build(ids_in_y)
     n0 = L.launch_count()
     y = L.linear(x, W, pool, plan)
-    assert L.launch_count() - n0 == 2                    # shrink kernel + GEMM
+    assert L.launch_count() - n0 == kernels
     torch.cuda.synchronize()
     assert L.last_device_error() == 0
     ref = O.lora_linear(f64(x), f64(t.W), f64(t.A), f64(t.B), t.rank, t.alpha, w.ids)
