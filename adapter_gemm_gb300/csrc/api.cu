@@ -276,18 +276,13 @@ void set_last_out(cudaStream_t st, const void* p, size_t bytes) {
     g_last_out[st] = r;
 }
 
-int slot_splits(int n_slots, int K) {
-    // clusters of ks CTAs, one per adapter slot; at most ~2 per SM in flight
-    const int cap = 2 * num_sms();
-    int ks = 1;
-    while (ks < 8 && n_slots * ks * 2 <= cap && K / (ks * 2) >= 256) ks *= 2;
-    return ks;
-}
-
-int shrink_splits(int max_tiles, int K) {
-    const int cap = 2 * num_sms();
-    int ks = 1;
-    while (ks < 8 && max_tiles * ks * 2 <= cap && K / (ks * 2) >= 256) ks *= 2;
+// K splits of the shrink: the largest (<= 8) whose clusters, one per unit of
+// work, fit about one wave (the kernel holds tensor memory: one CTA per SM;
+// `units` may count units that turn out empty), with at least 4 K slices per
+// CTA.
+int shrink_splits(int units, int K) {
+    int ks = 8;
+    while (ks > 1 && (4 * units * ks > 5 * num_sms() || K / ks < 256)) ks /= 2;
     return ks;
 }
 
@@ -566,7 +561,6 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         ShrinkArgs sa;
         sa.x = static_cast<const __nv_bfloat16*>(x);
         sa.ids = plan->ids;
-        sa.A = static_cast<const __nv_bfloat16*>(pool->A);
         sa.scale = pool->scale;
         sa.rank = pool->rank;
         sa.token_order = plan->token_order;
@@ -579,21 +573,39 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         sa.T = T;
         sa.K = d_in;
         sa.R_max = pool->R_max;
-        // Small decode batches group rows by slot inside the shrink, so it need
-        // not wait for the plan kernel; larger ones use the plan's work tiles,
-        // which spread a heavily used adapter's rows over many CTAs.
+        // Small decode batches group rows by slot inside the shrink (one unit
+        // per adapter slot the ids name, at most T of them); larger ones use
+        // the plan's 128-row work tiles.
         const bool by_slot = path == 0 && T <= kBySlotMaxT;
-        const int grid_x = by_slot ? pool->S - 1 : plan->max_tiles;
-        sa.ks = by_slot ? slot_splits(grid_x, d_in) : shrink_splits(plan->max_tiles, d_in);
-        // Decode batches on the work-tile grid with a long K range: clusters of
-        // 8. Their shrink runs on the SMs the GEMM leaves free, and its U is
-        // what the GEMM's epilogue waits for. Measured on T = 256, 14336 ->
-        // 4096, 31 slots of ranks 8..64: 64.0 us per step with 8 splits, 78.4
-        // with 2 (the rule above) or 4. (The by-slot grid at T = 64 is slower
-        // with 8: 166.4 against 160.7 us per layer.)
-        if (path == 0 && !by_slot && d_in >= 8192) sa.ks = 8;
+        const int grid_x = by_slot ? (pool->S - 1 < T ? pool->S - 1 : T) : plan->max_tiles;
+        sa.S = pool->S;
+        sa.by_slot = by_slot ? 1 : 0;
+        sa.ks = shrink_splits(grid_x, d_in);
+        sa.tmem_cols = 32;
+        while (sa.tmem_cols < sa.R16) sa.tmem_cols *= 2;
+        const int xrows = ((T < kTileRows ? T : kTileRows) + 7) / 8 * 8;   // rows of a unit, at most
+        sa.kk = shrink_kk(xrows, sa.R16, d_in);
+        // A pool [S][R_max][d_in]: map g has boxes of 64 columns x 16 (g + 1)
+        // rank rows of one slot (x kk slices: {64, R_max, S, d_in / 64} view)
+        ShrinkMaps smaps;
+        for (int g = 0; g < sa.R16 / 16; ++g) {
+            const uint32_t rows = (uint32_t)(16 * (g + 1));
+            bool okm;
+            if (sa.kk == 1) {
+                const uint64_t da[3] = {(uint64_t)d_in, (uint64_t)pool->R_max, (uint64_t)pool->S};
+                const uint64_t pa[2] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2};
+                const uint32_t ba[3] = {64, rows, 1};
+                okm = make_tmap_nd(&smaps.a[g], pool->A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
+            } else {
+                const uint64_t da[4] = {64, (uint64_t)pool->R_max, (uint64_t)pool->S, (uint64_t)d_in / 64};
+                const uint64_t pa[3] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2, 128};
+                const uint32_t ba[4] = {64, rows, 1, (uint32_t)sa.kk};
+                okm = make_tmap_nd(&smaps.a[g], pool->A, 4, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
+            }
+            if (!okm) return LORA_ECUDA;
+        }
         if (grid_x > 0) {
-            if (counted(launch_shrink(sa, grid_x, by_slot, pdl, st)) != cudaSuccess) return LORA_ECUDA;
+            if (counted(launch_shrink(smaps, sa, grid_x, pdl, st)) != cudaSuccess) return LORA_ECUDA;
             // The GEMM follows the shrink kernel, which waited for every kernel
             // ahead of it before it let the GEMM start and writes neither x nor
             // the ids: the GEMM may read both before its own wait (for U).
@@ -917,9 +929,11 @@ lora_status lora_profile_gemm_events(void* start, void* stop) {
 
 lora_status lora_last_device_error(int32_t* code_out) {
     if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ECUDA;
-    int a = 0, b = 0;
-    if (skinny_take_error(&a) != cudaSuccess || wide_take_error(&b) != cudaSuccess) return LORA_ECUDA;
-    const int v = a ? a : b;
+    int a = 0, b = 0, c = 0;
+    if (skinny_take_error(&a) != cudaSuccess || wide_take_error(&b) != cudaSuccess ||
+        shrink_take_error(&c) != cudaSuccess)
+        return LORA_ECUDA;
+    const int v = a ? a : (b ? b : c);
     if (code_out) *code_out = v;
     return v ? LORA_ETIMEOUT : LORA_OK;
 }

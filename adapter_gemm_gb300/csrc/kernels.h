@@ -7,9 +7,9 @@
 
 namespace lora {
 
-constexpr int kTileRows = 16;       // plan work tiles, rows (== LORA_TILE_ROWS)
+constexpr int kTileRows = 128;      // plan work tiles, rows (== LORA_TILE_ROWS): the shrink's MMA M
 constexpr int kMaxSlots = 1024;     // one plan thread per slot in the scans
-constexpr int kMaxRank = 128;       // R_max cap: shrink keeps R_max/8 MMA column tiles
+constexpr int kMaxRank = 128;       // R_max cap: the shrink's MMA N and TMEM columns
 constexpr int kSkinnyMaxT = 256;    // token columns of one swap-AB MMA (N <= 256)
 constexpr int kSkinnyOnlyMaxT = 256; // batches up to this many rows always take the swap-AB kernel
 constexpr int kSkinnyPathMaxT = 640; // batches above this many rows always take the persistent 128 x 256 kernel
@@ -37,7 +37,6 @@ struct PlanArgs {
 struct ShrinkArgs {
     const __nv_bfloat16* x;      // [T, K]
     const int32_t* ids;          // [T] the step's raw slot ids (by-slot grid)
-    const __nv_bfloat16* A;      // [S, R_max, K]
     const float* scale;          // [S]
     const int32_t* rank;         // [S]
     const int32_t* token_order;  // [T]
@@ -47,7 +46,16 @@ struct ShrinkArgs {
     __nv_bfloat16* U_hl;         // [T, 2*R16] bf16 hi | lo in plan order (wide kernel), or null
     int R16;                     // R_max rounded up to 16
     __nv_bfloat16* x_sorted;     // [T, K] or null
-    int T, K, R_max, ks;
+    int T, K, R_max, S, ks;
+    int by_slot;                 // unit u = the u-th adapter slot the ids name, rows found in the ids (T <= 128)
+    int tmem_cols;               // TMEM columns allocated: a power of two >= max(32, R16)
+    int kk;                      // 64-column K slices per stage (> 1: 4-D views of the A pool)
+};
+
+// The shrink's A-pool maps: map g has boxes of 16 (g + 1) rank rows of one
+// slot, 64 columns, kk slices (a 4-D view when kk > 1).
+struct ShrinkMaps {
+    CUtensorMap a[kMaxRank / 16];
 };
 
 // Expand operands of the decode GEMM's epilogue. ids == null means base only
@@ -124,7 +132,9 @@ struct WideMaps {
 };
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream);
-cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream);
+cudaError_t launch_shrink(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_x, bool pdl, cudaStream_t stream);
+// K slices per shrink stage for units of up to xrows rows (two stages fit the ring).
+int shrink_kk(int xrows, int R16, int K);
 cudaError_t launch_skinny(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream);
 cudaError_t launch_wide(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
 cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);
@@ -134,11 +144,13 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* rows, int 
 // Read and clear the bounded-wait error words of the GEMM translation units.
 cudaError_t skinny_take_error(int* code);
 cudaError_t wide_take_error(int* code);
+cudaError_t shrink_take_error(int* code);
 
 // Raise a kernel's dynamic shared memory limit once per device.
 // One slot per kernel (instantiation) whose dynamic shared memory limit is
-// raised: 0 plan, 1 swap-AB decode, 2..5 wide (tile width x K slices).
-constexpr int kSmemSlots = 8;
+// raised: 0 plan, 1 swap-AB decode, 2..5 wide (tile width x K slices), 6..8
+// shrink (cp.async depth).
+constexpr int kSmemSlots = 10;
 cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
 
 // Shared-memory bytes the skinny kernel needs for a token tile of TN columns

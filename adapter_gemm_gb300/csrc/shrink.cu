@@ -3,292 +3,453 @@
 // inputs [num_tokens, hidden], lora_a [num_loras, rank, hidden], an fp32
 // [tokens, rank] output; Chapter 43's "shrink each row to its adapter's rank").
 //
-// A CTA works on up to 16 rows of one slot, so the slot's A block is read once
-// for those rows and they share it (the SGMV segment idea). The K range is
-// split over the CTAs of a thread-block cluster (ks of them) and over the 4
-// warps of each CTA; partial sums are reduced in a fixed order (warps 0..3,
-// then cluster ranks 0..ks-1 through distributed shared memory), so the
-// result is deterministic. Two grids use this: one CTA per plan work tile (for
-// the wide GEMM), and one cluster per slot (for decode-sized batches).
+// One unit of work is up to 128 rows of one slot (the SGMV segment idea: the
+// slot's A block is brought into shared memory once for all of them). The
+// unit's K range is split over the CTAs of a thread-block cluster (ks of
+// them), and each CTA runs a pipeline whose stages hold kk 64-column K slices:
+//   - A_s: one TMA copy per stage (a 4-D view of the pool, so kk slices of the
+//     slot's rows land as kk consecutive 128-byte swizzled blocks), only the
+//     slot's own rank rounded up to 16 rows, not the pool's R_max. A copy has
+//     a fixed cost of a few hundred ns on this GPU whatever its size, so a
+//     stage's A arrives in one copy, not one per slice;
+//   - x: the unit's rows gathered by cp.async, 16 bytes per thread step,
+//     written into the same 128-byte swizzled layout (row r, 16-byte chunk c
+//     at r * 128 + ((c ^ (r & 7)) << 4)), so the MMA reads it like a TMA tile;
+//   - one elected thread issues tcgen05.mma (M = 128 token rows, N = the
+//     rank rounded up to 16, K = 16) into a TMEM accumulator.
+// After the K loop the accumulator is read with tcgen05.ld; the ks partial
+// rows meet in the owning CTA's shared memory (distributed shared memory
+// stores, one region per sender) and are summed in rank order, so the result
+// does not depend on timing. Rows past the unit's own (rows of the 128-row
+// MMA that the unit does not have) hold whatever the buffer held and are
+// never read back: row i of the product depends on row i of x only.
 //
-// The contraction runs on mma.sync m16n8k16 (bf16 in, fp32 accumulate): the
-// shrink is a small, bandwidth-bound part of the layer (r/d_out of its FLOPs),
-// and a 16-row tile is exactly one MMA row block. Each lane loads 16 bytes
-// (8 consecutive k) per row and per A row, and feeds them to two MMAs; the
-// k order inside the tile's dot product is permuted identically for x and A,
-// which leaves the sum unchanged.
-//
-// For the wide GEMM path the same pass also writes x_sorted, the rows of x in
-// plan order, so the GEMM can load contiguous plan-ordered tiles with TMA.
+// Two grids use this: one unit per plan work tile (slot, begin, end) - for the
+// wide GEMM it also writes x_sorted, the rows of x in plan order - and, for
+// decode batches of at most 64 rows, one unit per adapter slot, whose rows the
+// CTA finds in the raw ids itself.
 #include <cstdint>
-#include <cooperative_groups.h>
+#include <cuda.h>
 #include "ptx.cuh"
 #include "kernels.h"
 
-namespace cg = cooperative_groups;
-
 namespace lora {
 
-constexpr int kShrinkThreads = 128;
+constexpr int kShThreads = 224;              // warp 0 A copies, warp 1 MMA + TMEM, warps 2..5 x rows and U,
+                                             // warp 6 hands landed stages to the MMA
+constexpr int kShM = 128;                    // token rows of the MMA
+constexpr uint32_t kShSlice = 128;           // bytes of one row's 64-column K slice
+constexpr int kShMaxStages = 32;
+constexpr uint32_t kShHeader = 2048;         // barriers, tokens, scratch ints (1024-byte multiple)
+constexpr uint32_t kShRing = 192 * 1024;     // ring of stages; also the partial rows after the K loop
+constexpr uint32_t kShSlack = kShM * kShSlice;  // what an MMA may read past the ring's end
+constexpr size_t kShSmem = 1024 + kShHeader + kShRing + kShSlack;
+static_assert((3 * kShMaxStages + 1) * 8 + (kShM + 40) * 4 <= kShHeader, "shrink header");
+static_assert((size_t)kShM * kMaxRank * 4 <= kShRing, "partial rows of every sender fit the ring");
+static_assert(kShRing >= 2 * (kShM + kMaxRank) * kShSlice, "two one-slice stages of the largest unit");
 
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// -------------------------------------------------------------- cp.async --
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Arrive on the barrier once every cp.async this thread has issued so far has
+// landed; the arrival is one of the barrier's expected arrivals (noinc).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
-// Partial U of one 16-row group over this CTA's K range [k_lo, k_hi): each of
-// the 4 warps takes every 4th 32-wide K step. Lane (g, q) loads 8 consecutive
-// k of rows g and g+8 and of A rows nt*8+g, and feeds them to two MMAs. Rows
-// the group does not have are read as zeros. When xs0/xs1 are given, the rows
-// are also copied there (the plan-ordered copy of x).
-template <int NT>
-__device__ __forceinline__ void shrink_accumulate(float (&acc)[NT][4], const __nv_bfloat16* xr0,
-                                                  const __nv_bfloat16* xr1, bool v0, bool v1,
-                                                  __nv_bfloat16* xs0, __nv_bfloat16* xs1,
-                                                  const __nv_bfloat16* Ablk, int K, int nt_used,
-                                                  int k_lo, int k_hi, bool do_mma) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, q = lane & 3;
-    const uint4 zero4 = make_uint4(0, 0, 0, 0);
-    // KU K steps per batch: every load of the batch is issued before its MMAs,
-    // so one batch costs one memory round trip.
-    constexpr int KU = NT >= 8 ? 1 : 8 / NT;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    for (int k = k_lo + warp * 32; k < k_hi; k += 4 * 32 * KU) {
-        uint4 xa[KU], xb[KU], bw[KU][NT];
-#pragma unroll
-        for (int u = 0; u < KU; ++u) {
-            const int kk = k + u * 4 * 32 + 8 * q;
-            const bool kv = kk < k_hi;
-            xa[u] = (v0 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr0 + kk)) : zero4;
-            xb[u] = (v1 && kv) ? __ldg(reinterpret_cast<const uint4*>(xr1 + kk)) : zero4;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-                bw[u][nt] = (do_mma && nt < nt_used && kv)
-                                ? __ldg(reinterpret_cast<const uint4*>(Ablk + (size_t)(nt * 8 + g) * K + kk))
-                                : zero4;
-        }
-#pragma unroll
-        for (int u = 0; u < KU; ++u) {
-            const int kk = k + u * 4 * 32 + 8 * q;
-            if (kk < k_hi) {
-                if (xs0 && v0) *reinterpret_cast<uint4*>(xs0 + kk) = xa[u];
-                if (xs1 && v1) *reinterpret_cast<uint4*>(xs1 + kk) = xb[u];
-            }
-            if (do_mma) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    if (nt < nt_used) {
-                        mma_bf16_16816(acc[nt], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bw[u][nt].x, bw[u][nt].y);
-                        mma_bf16_16816(acc[nt], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bw[u][nt].z, bw[u][nt].w);
-                    }
-                }
-            }
-        }
-    }
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
 }
 
-// Store U[row, col] = v (already scaled): as fp32 by token into U, or, for the
-// wide GEMM, as a bf16 high part and a bf16 low part (v - high) by plan
-// position into U_hl (columns [0, R16) and [R16, 2*R16)).
-__device__ __forceinline__ void store_u(float* U, __nv_bfloat16* U_hl, const int* tok, int row, int col, float v,
-                                        int R_max, int R16, int pos0) {
-    if (U_hl) {
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// Full cluster barrier (every thread of every CTA), ordering the shared-memory
+// accesses before it with those after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store U[row i of the unit, col] = v (already scaled): fp32 by token into U
+// [T][R_max], or (wide GEMM) a bf16 high part and a bf16 low part (v - high)
+// by plan position into U_hl [T][2 * R16].
+__device__ __forceinline__ void shrink_store(const ShrinkArgs& a, const int* tok, int b, int i, int col, float v) {
+    if (a.U_hl) {
         const __nv_bfloat16 hi = __float2bfloat16_rn(v);
         const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-        __nv_bfloat16* dst = U_hl + (size_t)(pos0 + row) * 2 * R16 + col;
+        __nv_bfloat16* dst = a.U_hl + (size_t)(b + i) * 2 * a.R16 + col;
         dst[0] = hi;
-        dst[R16] = lo;
+        dst[a.R16] = lo;
     } else {
-        U[(size_t)tok[row] * R_max + col] = v;
+        a.U[(size_t)tok[i] * a.R_max + col] = v;
     }
 }
 
-// Sum the group's partials over the 4 warps and the cluster's ks CTAs, in a
-// fixed order, scale, and store U rows: row i of the group is token tok[i]
-// (i < n). Rank c of the cluster owns rows [c*16/ks, (c+1)*16/ks): every CTA
-// pushes its partial of those rows into the owner's `recv` (plain stores into
-// the peer's shared memory), then the owner sums what it received in rank
-// order. Earlier readers of U must be done before the stores: the caller has
-// waited for them.
-template <int NT>
-__device__ __forceinline__ void shrink_reduce_store(const float (&acc)[NT][4], float (*part)[16][NT * 8 + 1],
-                                                    float* recv, const int* tok, int n, int rc8, float sc,
-                                                    float* U, int R_max, int ks, __nv_bfloat16* U_hl = nullptr,
-                                                    int R16 = 0, int pos0 = 0) {
-    constexpr int RC = NT * 8;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, q = lane & 3;
-    // Fragment: c0,c1 at (row g, col 2q..), c2,c3 at (row g+8, col 2q..).
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int col = nt * 8 + 2 * q;
-        part[warp][g][col] = acc[nt][0];
-        part[warp][g][col + 1] = acc[nt][1];
-        part[warp][g + 8][col] = acc[nt][2];
-        part[warp][g + 8][col + 1] = acc[nt][3];
-    }
-    __syncthreads();
-    if (ks > 1) {
-        cg::cluster_group cluster = cg::this_cluster();
-        const int rows_per = 16 / ks;
-        const int me = (int)cluster.block_rank();
-        cluster.sync();                               // owners are done with recv of an earlier group
-        const uint32_t rbase = smem_u32(recv);
-        for (int el = threadIdx.x; el < 16 * rc8; el += kShrinkThreads) {
-            const int row = el / rc8, col = el % rc8;
-            const float v = ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) + part[3][row][col];
-            const int owner = row / rows_per, lr = row % rows_per;
-            st_cluster_f32(mapa_shared(rbase, (uint32_t)owner) + (uint32_t)(((me * rows_per + lr) * RC + col) * 4), v);
+__global__ void __launch_bounds__(kShThreads, 1)
+shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    // header: barriers, the unit's tokens and scratch ints; then the ring
+    uint64_t* full = reinterpret_cast<uint64_t*>(base);      // [kShMaxStages]
+    uint64_t* empty = full + kShMaxStages;                   // [kShMaxStages]
+    uint64_t* ready = empty + kShMaxStages;                  // [kShMaxStages] stage landed, proxy-fenced
+    uint64_t* done = ready + kShMaxStages;
+    int* tok = reinterpret_cast<int*>(done + 1);             // [128] token of each unit row
+    int* misc = tok + kShM;                                  // [0] TMEM address; by-slot scan: [1..32] slot bits,
+                                                             // [33] slot, [34..37] counts
+    uint8_t* ring = base + kShHeader;
+    float* recv = reinterpret_cast<float*>(ring);            // after the K loop: [ks][128 / ks][R16] partial rows
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ks = a.ks;
+    const int kz = ks > 1 ? (int)blockIdx.y : 0;    // rank in the cluster (clusters run along y)
+    const int KK = a.kk;                            // K slices per stage
+    const int kc = ((a.K + ks * 64 * KK - 1) / (ks * 64 * KK)) * 64 * KK;   // whole stages per CTA
+    const int k_lo = kz * kc, k_hi = min(a.K, k_lo + kc);
+    const int n_sl = k_hi > k_lo ? (k_hi - k_lo + 63) / 64 : 0;             // this CTA's slices
+    const int n_it = (n_sl + KK - 1) / KK;                                  // and stages
+
+    if (warp == 0 && lane == 0) {
+        for (int g = 0; g < a.R16 / 16; ++g) tma_prefetch_desc(&maps.a[g]);
+        for (int i = 0; i < kShMaxStages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1 + 128);   // the A copies' arrival + every gathering thread's copies
+            // the MMA commit (or a plain arrive), and with x_sorted every gathering thread's copy-out
+            mbar_init(smem_u32(&empty[i]), 1 + (a.x_sorted ? 128 : 0));
+            mbar_init(smem_u32(&ready[i]), 1);
         }
-        cluster.sync();                               // every push has landed
-        const int wc = U_hl ? R16 : rc8;
-        for (int el = threadIdx.x; el < rows_per * wc; el += kShrinkThreads) {
-            const int lr = el / wc, col = el % wc;
-            float v = 0.f;
-            if (col < rc8) {
-                v = recv[lr * RC + col];
-                for (int z = 1; z < ks; ++z) v += recv[(z * rows_per + lr) * RC + col];
+        mbar_init(smem_u32(done), 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&misc[0]), (uint32_t)a.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)misc[0];
+
+    // The plan, the ids and x come from the kernels ahead, which may also still
+    // read U or x_sorted: wait for them, then let the next kernel start.
+    pdl_wait_trigger();
+
+    // This CTA's unit: slot s, plan positions [b, b + n), its rows' tokens.
+    int s = 0, b = 0, n = 0;
+    if (a.by_slot) {
+        // Unit u is the u-th smallest adapter slot (rank > 0) that the batch's
+        // ids name; its rows are the tokens on it, ascending.
+        uint32_t* present = reinterpret_cast<uint32_t*>(misc + 1);    // [32] bits: slots 0..1023
+        if (threadIdx.x < 32) present[threadIdx.x] = 0u;
+        __syncthreads();
+        const int t = threadIdx.x;
+        const int id = t < a.T ? a.ids[t] : 0;
+        if (t < a.T && id >= 1 && id < a.S && a.rank[id] > 0) atomicOr(&present[id >> 5], 1u << (id & 31));
+        __syncthreads();
+        if (warp == 0) {
+            const uint32_t wbits = present[lane];
+            int inc = __popc(wbits);
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, d);
+                if (lane >= d) inc += v;
             }
-            const int row = me * rows_per + lr;
-            if (row < n) store_u(U, U_hl, tok, row, col, col < rc8 ? sc * v : 0.f, R_max, R16, pos0);
+            const int u = (int)blockIdx.x, before = inc - __popc(wbits);
+            if (u >= before && u < inc) {
+                uint32_t w = wbits;
+                for (int q = 0; q < u - before; ++q) w &= w - 1u;       // drop the lower set bits
+                misc[33] = 32 * lane + __ffs(w) - 1;
+            }
+            if (lane == 31 && u >= inc) misc[33] = 0;                  // fewer adapter slots than units
+        }
+        __syncthreads();
+        s = misc[33];
+        const bool f = s > 0 && t < kShM && t < a.T && id == s;
+        const unsigned bal = __ballot_sync(0xffffffffu, f);
+        if (warp < 4 && lane == 0) misc[34 + warp] = __popc(bal);
+        __syncthreads();
+        int before = 0;
+        for (int w = 0; w < 4; ++w) {
+            before += w < warp ? misc[34 + w] : 0;
+            n += misc[34 + w];
+        }
+        if (f) tok[before + __popc(bal & ((1u << lane) - 1u))] = t;
+    } else if ((int)blockIdx.x < *a.n_tiles) {
+        const int4 tile = a.tiles[blockIdx.x];
+        s = tile.x;
+        b = tile.y;
+        n = tile.z - tile.y;
+        if (threadIdx.x < n) tok[threadIdx.x] = a.token_order[b + threadIdx.x];
+    }
+    const int r = s > 0 ? min(a.rank[s], a.R_max) : 0;
+    const bool do_mma = r > 0 && n > 0;
+    const bool copy = a.x_sorted != nullptr && n > 0;
+    __syncthreads();                                 // tok[] is complete
+
+    // Nothing to do (the same for every CTA of the cluster): leave.
+    if (!do_mma && !copy) {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
+        }
+        return;
+    }
+    // The ring for this unit: x slices of its own rows (rounded up to 8), so a
+    // unit of few rows keeps many K slices in flight. The MMA reads 128 rows
+    // of an x slice; past the unit's rows it reads the next bytes of the ring
+    // (or the slack after it), which only reach product rows never read back.
+    const int r16 = (r + 15) & ~15;                  // MMA N; A rows past r are zero in the pool
+    const uint32_t xslice = (uint32_t)((n + 7) & ~7) * kShSlice;   // one slice of the unit's x rows
+    const uint32_t aslice = (uint32_t)r16 * kShSlice;              // one slice of A_s
+    const uint32_t xbytes = (uint32_t)KK * xslice;                 // x part of a stage, then the A part
+    const uint32_t stage_bytes = xbytes + (uint32_t)KK * aslice;
+    const int NST = min(kShMaxStages, (int)(kShRing / stage_bytes));
+    bool ok = true;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // A_s slices by TMA.
+            int it = 0;
+            for (; it < n_it; ++it) {
+                const int st = it % NST;
+                if (it >= NST && !mbar_wait(smem_u32(&empty[st]), (uint32_t)((it / NST) & 1) ^ 1u, kErrEmptyWait)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = smem_u32(&full[st]);
+                if (do_mma) {
+                    // the whole box is counted, slices past d_in included (zero filled)
+                    mbar_arrive_expect_tx(fb, (uint32_t)KK * aslice);
+                    const uint32_t dA = smem_u32(ring + (size_t)st * stage_bytes + xbytes);
+                    const CUtensorMap* tm = &maps.a[r16 / 16 - 1];
+                    if (KK == 1) tma_load_3d(dA, tm, fb, k_lo + it * 64, 0, s);
+                    else tma_load_4d(dA, tm, fb, 0, 0, s, k_lo / 64 + it * KK);
+                } else {
+                    mbar_arrive(fb);
+                }
+            }
+            // Let the copies this thread started land before the CTA can exit.
+            if (do_mma)
+                for (int i = max(0, it - NST); i < it; ++i)
+                    mbar_wait(smem_u32(&full[i % NST]), (uint32_t)((i / NST) & 1), kErrFullWait);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // MMA issuer: D[row, j] (+)= x_slice[row, :] . A_slice[j, :]
+            const uint32_t idesc = idesc_bf16_f32(kShM, (uint32_t)(r16 > 0 ? r16 : 16));
+            for (int it = 0; it < n_it; ++it) {
+                const int st = it % NST;
+                if (!mbar_wait(smem_u32(&ready[st]), (uint32_t)((it / NST) & 1), kErrFullWait)) {
+                    ok = false;
+                    break;
+                }
+                if (do_mma) {
+                    tc_fence_after();
+                    const uint32_t sX0 = smem_u32(ring + (size_t)st * stage_bytes);
+                    const int nq = min(KK, n_sl - it * KK);          // slices of this CTA's range
+                    for (int q = 0; q < nq; ++q) {
+                        const uint32_t sX = sX0 + (uint32_t)q * xslice, sA = sX0 + xbytes + (uint32_t)q * aslice;
+#pragma unroll
+                        for (int kq = 0; kq < 4; ++kq)
+                            tc_mma_bf16(tmem, sdesc_sw128(sX + kq * 32), sdesc_sw128(sA + kq * 32), idesc,
+                                        (it > 0 || q > 0 || kq > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[st]));
+                } else {
+                    mbar_arrive(smem_u32(&empty[st]));
+                }
+            }
+            if (do_mma) {
+                if (ok && n_it > 0) tc_commit(smem_u32(done));
+                else mbar_arrive(smem_u32(done));    // no product (the epilogue then sends zeros)
+            }
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // A stage's x rows arrive by cp.async (generic proxy) and the MMA reads
+        // them through the async proxy: once the stage has landed, this thread
+        // fences and hands the stage to the MMA.
+        // A proxy fence costs about 0.4 us whatever it orders, so one fence
+        // covers every stage that has landed by the time the oldest one has.
+        if (lane == 0) {
+            for (int it = 0; it < n_it;) {
+                if (!mbar_wait(smem_u32(&full[it % NST]), (uint32_t)((it / NST) & 1), kErrFullWait)) break;
+                int c = 1;
+                while (it + c < n_it && mbar_try_wait(smem_u32(&full[(it + c) % NST]), (uint32_t)(((it + c) / NST) & 1)))
+                    ++c;
+                fence_proxy_async_smem();
+                for (int j = it; j < it + c; ++j) mbar_arrive(smem_u32(&ready[j % NST]));
+                it += c;
+            }
+        }
+        __syncwarp();
+    } else {
+        // Gathering threads: thread g owns 16-byte chunk (g & 7) of rows
+        // (g >> 3) + 16 m of every slice; the swizzled chunk position depends
+        // on the row's low three bits, the same for all of them.
+        const int g = threadIdx.x - 64;
+        const int ch = g & 7, row0 = g >> 3;
+        const uint32_t swz = (uint32_t)((ch ^ (row0 & 7)) << 4);
+        const __nv_bfloat16* src[8];
+        __nv_bfloat16* dstx[8];
+        int nm = 0;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            const int row = row0 + 16 * m;
+            const bool v = row < n;
+            src[m] = a.x + (size_t)(v ? tok[row] : 0) * a.K + ch * 8;
+            dstx[m] = copy ? a.x_sorted + (size_t)(b + (v ? row : 0)) * a.K + ch * 8 : nullptr;
+            nm += v ? 1 : 0;
+        }
+        // With x_sorted: once stage j has landed (its full barrier), copy this
+        // thread's chunks of it out, then release them to the ring. The copy
+        // trails the gathering by D = NST - 1 stages.
+        const int D = NST - 1;
+        auto copy_out = [&](int j) -> bool {
+            const int st = j % NST;
+            if (!mbar_wait(smem_u32(&full[st]), (uint32_t)((j / NST) & 1), kErrFullWait)) return false;
+            const uint32_t sX0 = smem_u32(ring + (size_t)st * stage_bytes);
+            for (int q = 0; q < KK; ++q) {
+                const int kq0 = k_lo + (j * KK + q) * 64;                 // the slice's first column
+                if (kq0 + ch * 8 >= k_hi) break;
+                const uint32_t sX = sX0 + (uint32_t)q * xslice;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    if (m < nm) {
+                        const uint4 v = ld_shared_v4(sX + (uint32_t)(row0 + 16 * m) * kShSlice + swz);
+                        *reinterpret_cast<uint4*>(dstx[m] + kq0) = v;
+                    }
+            }
+            mbar_arrive(smem_u32(&empty[st]));
+            return true;
+        };
+        int it = 0;
+        for (; it < n_it && ok; ++it) {
+            const int st = it % NST;
+            if (it >= NST && !mbar_wait(smem_u32(&empty[st]), (uint32_t)((it / NST) & 1) ^ 1u, kErrEmptyWait)) {
+                ok = false;
+                break;
+            }
+            const uint32_t sX0 = smem_u32(ring + (size_t)st * stage_bytes);
+            for (int q = 0; q < KK; ++q) {
+                const int k = k_lo + (it * KK + q) * 64 + ch * 8;
+                const uint32_t nb = k < k_hi ? 16u : 0u;    // past this CTA's range (or d_in): zero fill
+                const uint32_t sX = sX0 + (uint32_t)q * xslice;
+#pragma unroll
+                for (int m = 0; m < 8; ++m)
+                    if (m < nm) cp_async16(sX + (uint32_t)(row0 + 16 * m) * kShSlice + swz, src[m] + (nb ? k - ch * 8 : 0), nb);
+            }
+            cp_async_arrive(smem_u32(&full[st]));
+            if (copy && it >= D) ok = copy_out(it - D);
+        }
+        if (copy && ok)
+            for (int j = max(0, it - D); j < it && ok; ++j) ok = copy_out(j);
+        asm volatile("cp.async.wait_all;" ::: "memory");   // nothing of this thread is in flight at exit
+        __syncwarp();
+    }
+
+    // Epilogue, warps 2..5: warp w reads TMEM lanes 32 (w % 4) .. +31, i.e.
+    // unit rows i = 32 (w % 4) + lane, and sends or stores them.
+    const float sc = do_mma ? a.scale[s] : 0.f;
+    const int rc8 = (r + 7) & ~7;                    // U columns written
+    const int wc = a.U_hl ? a.R16 : rc8;
+    const bool epi = warp >= 2 && warp < 6;
+    const int i = 32 * (warp & 3) + lane;
+    bool have = false;
+    if (epi && do_mma) {
+        bool got = true;
+        if (lane == 0) got = mbar_wait_sleep(smem_u32(done), 0u, kErrAccWait);
+        have = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+        tc_fence_after();
+    }
+    const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    if (ks == 1) {
+        if (epi && do_mma) {
+            for (int c = 0; c < wc; c += 16) {
+                float v[16];
+                if (have && c < r16 && n_it > 0) {
+                    tc_ld16(trow + (uint32_t)c, v);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] = 0.f;
+                }
+                if (i < n)
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (c + q < wc) shrink_store(a, tok, b, i, c + q, c + q < rc8 ? sc * v[q] : 0.f);
+            }
         }
     } else {
-        const int wc = U_hl ? R16 : rc8;
-        for (int el = threadIdx.x; el < 16 * wc; el += kShrinkThreads) {
-            const int row = el / wc, col = el % wc;
-            const float v = col < rc8 ? ((part[0][row][col] + part[1][row][col]) + part[2][row][col]) +
-                                            part[3][row][col]
-                                      : 0.f;
-            if (row < n) store_u(U, U_hl, tok, row, col, sc * v, R_max, R16, pos0);
+        // Row i goes to cluster rank i % ks, which keeps it as its row i / ks.
+        const int rows_per = kShM / ks;
+        cluster_sync_all();                          // every CTA is done with its stages (recv)
+        if (epi && do_mma && 32 * (warp & 3) < n) {
+            // the TMEM loads are warp-wide; lanes past the unit's rows send nothing
+            const bool mine = i < n;
+            const uint32_t rb = mapa_shared(smem_u32(recv), (uint32_t)(i % ks));
+            const uint32_t off = (uint32_t)((kz * rows_per + i / ks) * a.R16) * 4u;
+            for (int c = 0; c < r16; c += 16) {
+                float v[16];
+                if (have && n_it > 0) {
+                    tc_ld16(trow + (uint32_t)c, v);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] = 0.f;
+                }
+                if (mine)
+#pragma unroll
+                    for (int q = 0; q < 16; q += 4)
+                        st_cluster_v4(rb + off + (uint32_t)(c + q) * 4u, v[q], v[q + 1], v[q + 2], v[q + 3]);
+            }
+        }
+        cluster_sync_all();                          // every partial row has landed
+        if (do_mma) {
+            // Rows kz, kz + ks, ... of the unit: the senders' partials in rank order.
+            const int n_mine = n > kz ? (n - kz + ks - 1) / ks : 0;
+            for (int el = threadIdx.x; el < n_mine * wc; el += kShThreads) {
+                const int li = el / wc, col = el % wc;
+                float v = 0.f;
+                if (col < rc8) {
+                    v = recv[(size_t)li * a.R16 + col];
+                    for (int z = 1; z < ks; ++z) v += recv[((size_t)z * rows_per + li) * a.R16 + col];
+                    v *= sc;
+                }
+                shrink_store(a, tok, b, kz + li * ks, col, v);
+            }
         }
     }
-    __syncthreads();                                  // part / recv are reused by the next group
-}
 
-// One CTA (cluster of ks CTAs along K) per plan work tile: up to 16 rows of
-// one slot's segment. Used with the wide GEMM, so it also writes x_sorted;
-// tiles of slot 0 and of rank-0 slots only copy.
-template <int NT>
-__global__ void __launch_bounds__(kShrinkThreads)
-shrink_tiles_kernel(ShrinkArgs a) {
-    constexpr int RC = NT * 8;
-    __shared__ float part[4][16][RC + 1];
-    __shared__ float recv[16 * RC];
-    __shared__ int tok[16];
-
-    // This kernel needs the plan, and the previous call's readers of U /
-    // x_sorted must be done, before it goes on; then the next kernel may start
-    // its prologue.
-    pdl_wait_trigger();
-
-    const int n_tiles = *a.n_tiles;
-    const int tile_idx = blockIdx.x;
-    if (tile_idx >= n_tiles) return;                 // the whole cluster shares tile_idx
-    const int4 tile = a.tiles[tile_idx];
-    const int s = tile.x, b = tile.y, e = tile.z;
-    const int r = (s > 0) ? min(a.rank[s], a.R_max) : 0;
-    const bool do_mma = r > 0;
-    const bool do_copy = a.x_sorted != nullptr;
-    if (!do_mma && !do_copy) return;
-
-    const int lane = threadIdx.x & 31;
-    const int g = lane >> 2;
-    const int K = a.K;
-    const int kz = (a.ks > 1) ? (int)blockIdx.y : 0;
-    const int kc = ((K + a.ks * 32 - 1) / (a.ks * 32)) * 32;
-    const int k_lo = kz * kc, k_hi = min(K, k_lo + kc);
-    if (threadIdx.x < 16) tok[threadIdx.x] = (b + (int)threadIdx.x < e) ? a.token_order[b + threadIdx.x] : 0;
-    const int i0 = b + g, i1 = b + g + 8;            // plan positions of this lane's rows
-    const bool v0 = i0 < e, v1 = i1 < e;
-    const int t0 = v0 ? a.token_order[i0] : 0;
-    const int t1 = v1 ? a.token_order[i1] : 0;
-    float acc[NT][4];
-    shrink_accumulate<NT>(acc, a.x + (size_t)t0 * K, a.x + (size_t)t1 * K, v0, v1,
-                          do_copy ? a.x_sorted + (size_t)i0 * K : nullptr,
-                          do_copy ? a.x_sorted + (size_t)i1 * K : nullptr,
-                          a.A + (size_t)(do_mma ? s : 0) * a.R_max * K, K, (r + 7) >> 3, k_lo, k_hi, do_mma);
-    if (!do_mma) return;                              // copy-only tiles are done
-    __syncthreads();                                  // tok[] is visible
-    shrink_reduce_store<NT>(acc, part, recv, tok, e - b, ((r + 7) >> 3) * 8, a.scale[s], a.U, a.R_max, a.ks,
-                            a.U_hl, a.R16, b);
-}
-
-// Decode-sized batches (T <= 256): one cluster of ks CTAs (split along K) per
-// adapter slot s >= 1. The CTA finds the rows on its slot from the step's ids
-// itself (ascending, so the same grouping the plan would give); it needs no
-// plan arrays.
-template <int NT>
-__global__ void __launch_bounds__(kShrinkThreads)
-shrink_by_slot_kernel(ShrinkArgs a) {
-    constexpr int RC = NT * 8;
-    __shared__ float part[4][16][RC + 1];
-    __shared__ float recv[16 * RC];
-    __shared__ int rows[kSkinnyMaxT];
-    __shared__ int wtot[4];
-
-    // The ids and x may come from the kernel ahead, which may also still read
-    // U: wait for it first.
-    pdl_wait_trigger();
-    const int s = blockIdx.x + 1;
-    const int r = min(a.rank[s], a.R_max);           // written only by the synchronous install
-    // rows on slot s, ascending: two ids per thread, then a block prefix sum
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t_a = 2 * tid, t_b = 2 * tid + 1;
-    const int id_a = t_a < a.T ? a.ids[t_a] : -1;   // loaded alongside the rank, not after it
-    const int id_b = t_b < a.T ? a.ids[t_b] : -1;
-    const int f_a = (r > 0 && id_a == s) ? 1 : 0;
-    const int f_b = (r > 0 && id_b == s) ? 1 : 0;
-    int inc = f_a + f_b;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += v;
-    }
-    if (lane == 31) wtot[warp] = inc;
+    tc_fence_before();
     __syncthreads();
-    int before = 0, n_rows = 0;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        before += (w < warp) ? wtot[w] : 0;
-        n_rows += wtot[w];
-    }
-    const int pos = before + inc - f_a - f_b;
-    if (f_a) rows[pos] = t_a;
-    if (f_b) rows[pos + f_a] = t_b;
-    if (n_rows == 0) return;           // no rows (or rank 0): same for the whole cluster
-    __syncthreads();
-
-    const int g = lane >> 2;
-    const int K = a.K;
-    const int kz = (a.ks > 1) ? (int)blockIdx.y : 0;
-    const int kc = ((K + a.ks * 32 - 1) / (a.ks * 32)) * 32;
-    const int k_lo = kz * kc, k_hi = min(K, k_lo + kc);
-    const int nt_used = (r + 7) >> 3;
-    const float sc = a.scale[s];
-    const __nv_bfloat16* Ablk = a.A + (size_t)s * a.R_max * K;
-    for (int g0 = 0; g0 < n_rows; g0 += 16) {
-        const bool v0 = g0 + g < n_rows, v1 = g0 + g + 8 < n_rows;
-        const int t0 = v0 ? rows[g0 + g] : 0, t1 = v1 ? rows[g0 + g + 8] : 0;
-        float acc[NT][4];
-        shrink_accumulate<NT>(acc, a.x + (size_t)t0 * K, a.x + (size_t)t1 * K, v0, v1, nullptr, nullptr,
-                              Ablk, K, nt_used, k_lo, k_hi, true);
-        shrink_reduce_store<NT>(acc, part, recv, rows + g0, min(16, n_rows - g0), nt_used * 8, sc, a.U,
-                                a.R_max, a.ks);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
     }
 }
 
-template <int NT>
-static cudaError_t launch_shrink_nt(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream) {
+int shrink_kk(int xrows, int R16, int K) {
+    if (K % 64 != 0) return 1;               // the 4-D views need whole slices
+    for (int kk = 8; kk > 1; kk /= 2)
+        if (kk <= K / 64 && 2u * (uint32_t)kk * (uint32_t)(xrows + R16) * kShSlice <= kShRing) return kk;
+    return 1;
+}
+
+cudaError_t launch_shrink(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_x, bool pdl, cudaStream_t stream) {
+    if (grid_x <= 0) return cudaSuccess;
+    cudaError_t e = ensure_smem_attr((const void*)shrink_tc_kernel, 6, kShSmem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, a.ks, 1);
-    cfg.blockDim = dim3(kShrinkThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.blockDim = dim3(kShThreads, 1, 1);
+    cfg.dynamicSmemBytes = kShSmem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -306,21 +467,17 @@ static cudaError_t launch_shrink_nt(const ShrinkArgs& a, int grid_x, bool by_slo
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return by_slot ? cudaLaunchKernelEx(&cfg, shrink_by_slot_kernel<NT>, a)
-                   : cudaLaunchKernelEx(&cfg, shrink_tiles_kernel<NT>, a);
+    return cudaLaunchKernelEx(&cfg, shrink_tc_kernel, maps, a);
 }
 
-cudaError_t launch_shrink(const ShrinkArgs& a, int grid_x, bool by_slot, bool pdl, cudaStream_t stream) {
-    if (grid_x <= 0) return cudaSuccess;
-    const int nt = (a.R_max + 7) / 8;
-    if (nt <= 1) return launch_shrink_nt<1>(a, grid_x, by_slot, pdl, stream);
-    if (nt <= 2) return launch_shrink_nt<2>(a, grid_x, by_slot, pdl, stream);
-    if (nt <= 4) return launch_shrink_nt<4>(a, grid_x, by_slot, pdl, stream);
-    if (nt <= 8) return launch_shrink_nt<8>(a, grid_x, by_slot, pdl, stream);
-    return launch_shrink_nt<16>(a, grid_x, by_slot, pdl, stream);
+cudaError_t shrink_take_error(int* code) {
+    int v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_lora_error, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_lora_error, &zero, sizeof(int));
+    if (code) *code = v;
+    return e;
 }
 
-// Count bf16 words that encode Inf or NaN (exponent bits all ones).
 // x_rows[i, :] = x[rows[i], :] for i < T, 16 bytes per thread step; an index
 // outside [0, T_all) gives a zero row.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ rows, int T, int T_all,
@@ -343,6 +500,7 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* rows, int 
     return cudaGetLastError();
 }
 
+// Count bf16 words that encode Inf or NaN (exponent bits all ones).
 __global__ void count_nonfinite_kernel(const uint16_t* __restrict__ p, size_t n, int32_t* out) {
     int cnt = 0;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)

@@ -25,7 +25,7 @@ STATUS = {
     -5: "LORA_ENONFINITE", -6: "LORA_ECUDA", -7: "LORA_EIDRANGE", -8: "LORA_ESPACE",
     -9: "LORA_ETIMEOUT", -10: "LORA_ESCRATCH",
 }
-TILE_ROWS = 16
+TILE_ROWS = 128
 
 
 class LoraError(RuntimeError):

@@ -83,7 +83,8 @@ typedef struct {
  *   active        [S]     slots >= 1 with rows, ascending; n_active valid
  *   tiles         [max_tiles][4] (slot, begin, end, 0): every slot's segment
  *                         (slot 0 included) cut every LORA_TILE_ROWS rows,
- *                         positions into token_order; n_tiles valid
+ *                         positions into token_order; n_tiles valid; the
+ *                         shrink's units of work (128 rows: its MMA's M)
  *   n_active, n_tiles, n_invalid [1] each
  *   U             [T, R_max] fp32: the shrink result of the last lora_linear
  *                         call, row t = token t (scratch)
@@ -104,7 +105,7 @@ typedef struct {
  * lora_linear calls that share a plan share its scratch, so they must be
  * ordered on one stream.
  */
-#define LORA_TILE_ROWS 16
+#define LORA_TILE_ROWS 128
 typedef struct {
     int32_t* slot_of_token;
     int32_t* token_order;

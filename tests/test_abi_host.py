@@ -58,7 +58,7 @@ def test_plan_init_carves_workspace(lib):
     assert ptrs == sorted(ptrs) and len(set(ptrs)) == len(ptrs)
     assert p.U + 300 * 16 * 4 <= p.x_sorted
     assert p.x_sorted + 300 * 4096 * 2 <= FAKE + n
-    assert p.max_tiles == (300 + 15) // 16 + 17
+    assert p.max_tiles == (300 + 127) // 128 + 17
     # decode-sized plans carry no x_sorted
     q = L.lora_plan_t()
     m = lib.lora_plan_workspace_bytes(64, 9, 16, 4096)
