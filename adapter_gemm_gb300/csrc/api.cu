@@ -193,10 +193,13 @@ int skinny_kk(int TN, bool fuse, bool tce, int a_rows, int K) {
 // Launch shape of the skinny kernel. The K split depends only on (T, d_in,
 // d_out) - a base-only call, a call with the shrink kernel ahead and one with
 // the shrink fused in split K identically, so their partial sums agree. The
-// kernel holds tensor memory, so it runs one CTA per SM, and a CTA of the next
-// GEMM cannot share an SM with it: for decode-sized token tiles the split is
-// the largest (<= 8) whose CTAs fit in half of the SMs, so that consecutive
-// GEMMs stream their weights side by side; wider tiles may use every SM.
+// kernel holds tensor memory, so it runs one CTA per SM: the split is the
+// largest (<= 8) whose CTAs fit the SMs. Consecutive layers form a dependent
+// chain (the next layer's x is this one's y), so one GEMM should stream its
+// weights from every SM; measured per chained step (us, half / all SMs):
+// T = 64, 4096 -> 4096, shrink fused: 23.3 / 17.0; layer sweep T = 1: 149.5 /
+// 134.6; T = 8: 170.3 / 165.8; T = 64 (shrink kernel ahead on the SMs the GEMM
+// leaves free): 219.6 / 230.9.
 // `mode`: 0 base only, 1 U from the shrink kernel (expand on the CUDA cores),
 // 2 shrink fused in, 3 U from the shrink kernel with the expand on the tensor
 // cores (rank 0 of the cluster), 4 the same with the expand's chunks dealt over
@@ -210,9 +213,7 @@ SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S) {
     const size_t canon_smem = skinny_smem_bytes(c.TN, canon_stages, 8, false, false, false, true, 1);
     const int units = ((N + 127) / 128) * ((T + c.TN - 1) / c.TN);
     const int kb = (K + 63) / 64;
-    // Decode-sized token tiles are latency-bound: half the SMs, so that the
-    // next GEMM streams beside this one. Wider tiles are compute-heavy: all.
-    const int cap = c.TN <= 64 ? num_sms() / 2 : num_sms();
+    const int cap = num_sms();
     c.ks = 1;
     for (int ks = 8; ks >= 2; ks /= 2) {
         if (kb < ks) continue;

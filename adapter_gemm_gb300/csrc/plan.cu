@@ -8,9 +8,11 @@
 // the host side of the launch; here one CTA builds it on the device, so the
 // step needs no host round trip.
 //
-// One CTA of 32 warps. Warp w owns a contiguous range of rows, so rows of
-// lower warps precede rows of higher warps, and inside a warp rows are taken
-// 32 at a time in order: the sort is stable by construction.
+// One CTA of up to 32 warps: enough for one thread per slot and, up to 1024
+// rows, one thread per row (a decode step's plan then runs on a few warps,
+// with short scans over them). Warp w owns a contiguous range of rows, so
+// rows of lower warps precede rows of higher warps, and inside a warp rows are
+// taken 32 at a time in order: the sort is stable by construction.
 //   pass 1: each warp counts its rows per slot (__match_any_sync groups lanes
 //           with equal slot; the group leader adds the group size);
 //   scan:   per slot, an exclusive prefix over warps; over slots, an
@@ -23,6 +25,8 @@
 // The kernel is launched as a dependent of the previous kernel of the stream.
 // That kernel may still read the plan arrays, and may be the one that wrote
 // the ids, so the plan kernel waits for it before it reads or writes anything.
+// It lets its own dependents start at once (they read only weights before
+// they wait for it).
 #include <cstdint>
 #include <cuda_runtime.h>
 #include "ptx.cuh"
@@ -30,10 +34,18 @@
 
 namespace lora {
 
-constexpr int kPlanThreads = 1024;
-constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kPlanMaxThreads = 1024;
+constexpr int kPlanMaxWarps = kPlanMaxThreads / 32;
 
-// Exclusive block-wide prefix sum of one value per thread (1024 threads).
+// Threads of the plan CTA for T rows and S slots: a multiple of 32, at least
+// one per slot and one per row, at most 1024.
+int plan_threads(int T, int S) {
+    int n = T > S ? T : S;
+    n = (n + 31) / 32 * 32;
+    return n < 32 ? 32 : (n > kPlanMaxThreads ? kPlanMaxThreads : n);
+}
+
+// Exclusive block-wide prefix sum of one value per thread.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int inc = v;
@@ -45,7 +57,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& t
     if (lane == 31) warp_tot[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        int t = warp_tot[lane];
+        int t = lane < (int)(blockDim.x >> 5) ? warp_tot[lane] : 0;
         int ti = t;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
@@ -62,27 +74,31 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& t
     return r;
 }
 
-__global__ void __launch_bounds__(kPlanThreads, 1)
+__global__ void __launch_bounds__(kPlanMaxThreads, 1)
 plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     extern __shared__ int smem[];
     const int S = p.S;
-    int* wc = smem;                       // [kPlanWarps][S] per-warp slot counts, then cursors
-    int* tot = smem + kPlanWarps * S;     // [S] per-slot totals
+    const int NT = blockDim.x, NW = NT >> 5;
+    int* wc = smem;                       // [NW][S] per-warp slot counts, then cursors
+    int* tot = smem + NW * S;             // [S] per-slot totals
     __shared__ int warp_tot[33];
     __shared__ int s_invalid;
 
-    // The ids may come from the kernel ahead, which may also still read the
-    // plan arrays: wait for it, then let the next kernel start its prologue
-    // (it waits for this grid before it reads the plan).
-    pdl_wait_trigger();
+    // The next kernel may start its prologue at once: every kernel of this
+    // library reads, before its own wait, only weights, and that wait (for
+    // this grid to complete) also covers this kernel's wait below. The ids may
+    // come from the kernel ahead, which may also still read the plan arrays:
+    // wait for it before reading or writing anything.
+    pdl_trigger();
+    pdl_wait();
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < kPlanWarps * S; i += kPlanThreads) wc[i] = 0;
+    for (int i = tid; i < NW * S; i += NT) wc[i] = 0;
     if (tid == 0) s_invalid = 0;
     __syncthreads();
 
     // Rows [lo, hi) of this warp; chunk is a multiple of 32.
-    const int chunk = ((T + kPlanWarps * 32 - 1) / (kPlanWarps * 32)) * 32;
+    const int chunk = ((T + NW * 32 - 1) / (NW * 32)) * 32;
     const int lo = min(T, warp * chunk), hi = min(T, lo + chunk);
 
     int n_bad = 0;
@@ -102,9 +118,9 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     __syncthreads();
 
     // Per slot: exclusive prefix over warps (in place) and the slot total.
-    for (int s = tid; s < S; s += kPlanThreads) {
+    for (int s = tid; s < S; s += NT) {
         int run = 0;
-        for (int w = 0; w < kPlanWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             const int c = wc[w * S + s];
             wc[w * S + s] = run;
             run += c;
@@ -118,7 +134,7 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     const int my_cnt = tid < S ? tot[tid] : 0;
     const int start = block_exclusive_scan(my_cnt, warp_tot, total);
     if (tid < S)
-        for (int w = 0; w < kPlanWarps; ++w) wc[w * S + tid] += start;
+        for (int w = 0; w < NW; ++w) wc[w * S + tid] += start;
     __syncthreads();
 
     // Pass 2: stable scatter of row ids.
@@ -183,7 +199,7 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
         }
         __syncthreads();
         // mt_ptr[m] = first entry whose block is >= m
-        for (int m = tid; m <= m_blocks; m += kPlanThreads) {
+        for (int m = tid; m <= m_blocks; m += NT) {
             int lo = 0, hi = n_ent;
             while (lo < hi) {
                 const int mid = (lo + hi) >> 1;
@@ -196,15 +212,16 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
 }
 
 // Shared memory of the plan kernel: per-warp slot counts and slot totals.
-size_t plan_smem_bytes(int S) { return sizeof(int) * (size_t)(kPlanWarps + 1) * S; }
+size_t plan_smem_bytes(int NT, int S) { return sizeof(int) * (size_t)(NT / 32 + 1) * S; }
 
 cudaError_t launch_plan(const int32_t* ids, int T, const PlanArgs& p, bool pdl, cudaStream_t stream) {
-    const size_t smem = plan_smem_bytes(p.S);
-    cudaError_t e = ensure_smem_attr((const void*)plan_kernel, 0, smem);
+    const int NT = plan_threads(T, p.S);
+    const size_t smem = plan_smem_bytes(NT, p.S);
+    cudaError_t e = ensure_smem_attr((const void*)plan_kernel, 0, plan_smem_bytes(kPlanMaxThreads, p.S));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(kPlanThreads, 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

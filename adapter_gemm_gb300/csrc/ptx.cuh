@@ -176,14 +176,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------- PDL -------
-// Programmatic dependent launch. Every kernel of this library lets the next
-// kernel of its stream start (launch_dependents) only after its own wait for
-// the kernels ahead of it has returned: when a kernel starts, every kernel
-// before its immediate predecessor has then completed and its writes are
-// visible, so the only work that may still run beside it is that predecessor.
-// A kernel reads, before its own wait, only weights (W and the pool, which no
-// running kernel writes) and buffers that its immediate predecessor - a kernel
-// of the same library call that does not write them - left untouched.
+// Programmatic dependent launch. Every kernel of this library but the plan
+// kernel lets the next kernel of its stream start (launch_dependents) only
+// after its own wait for the kernels ahead of it has returned: when such a
+// kernel's dependent starts, every kernel before that kernel has completed and
+// its writes are visible. The plan kernel lets its dependents start at once;
+// they read nothing but weights before their own wait, which returns only once
+// the plan kernel - and so its own wait - has completed. A kernel reads, before
+// its own wait, only weights (W and the pool, which no running kernel writes)
+// and buffers that its immediate predecessor - a shrink kernel of the same
+// library call, which waited before it let this kernel start and does not
+// write them - left untouched.
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
