@@ -574,33 +574,61 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         sa.T = T;
         sa.K = d_in;
         sa.R_max = pool->R_max;
-        // Small decode batches group rows by slot inside the shrink (one unit
-        // per adapter slot the ids name, at most T of them); larger ones use
-        // the plan's 128-row work tiles.
+        // A unit of the shrink is one adapter slot's rows, or - for decode
+        // batches of pools with R_max <= 16 - the rows of a group of G
+        // consecutive slot ids, whose A rows (R_max each) one TMA box brings in
+        // and one MMA per K step contracts (G R_max <= 256 columns, of which
+        // each row keeps its slot's): a tcgen05 MMA costs about the same for
+        // 16 columns as for 256, and a copy has a fixed cost, so grouping cuts
+        // both by up to G. Prefill batches (many rows per slot) and wider
+        // ranks keep one slot per unit, whose A rows are the slot's own rank.
+        // Small decode batches find their rows in the ids (no plan needed);
+        // larger ones take the plan's segments (groups: its indptr; slots: its
+        // 128-row work tiles).
+        // A group pays for all its slots' A rows, so it is taken only when the
+        // batch has rows enough to name several slots of each group (T at
+        // least 8 per group). Measured per chained layer sweep step (us, one
+        // slot / groups of 16): T = 512: 432.7 / 404.0; T = 64: 231.7 / 227.2;
+        // T = 8: 166.6 / 190.0; T = 1: 135.1 / 160.5.
         const bool by_slot = path == 0 && T <= kBySlotMaxT;
-        const int grid_x = by_slot ? (pool->S - 1 < T ? pool->S - 1 : T) : plan->max_tiles;
+        int G = 256 / sa.R16;
+        if ((G * pool->R_max) % 16 != 0) G &= ~1;
+        const bool grouped = path == 0 && pool->R_max <= 16 && pool->S > 2 &&
+                             T >= 8 * ((pool->S - 1 + G - 1) / G);
+        if (!grouped) G = 0;
+        const int n_groups = grouped ? (pool->S - 1 + G - 1) / G : pool->S - 1;
+        int grid_x;
+        if (by_slot) grid_x = n_groups < T ? n_groups : T;
+        else if (grouped) grid_x = (T + kTileRows - 1) / kTileRows + n_groups;
+        else grid_x = plan->max_tiles;
         sa.S = pool->S;
         sa.by_slot = by_slot ? 1 : 0;
+        sa.G = G;
+        sa.indptr = plan->indptr;
+        sa.slot_of_token = plan->slot_of_token;
         sa.ks = shrink_splits(grid_x, d_in);
+        const int ncol_max = grouped ? G * pool->R_max : sa.R16;
         sa.tmem_cols = 32;
-        while (sa.tmem_cols < sa.R16) sa.tmem_cols *= 2;
+        while (sa.tmem_cols < ncol_max) sa.tmem_cols *= 2;
         const int xrows = ((T < kTileRows ? T : kTileRows) + 7) / 8 * 8;   // rows of a unit, at most
-        sa.kk = shrink_kk(xrows, sa.R16, d_in);
+        sa.kk = shrink_kk(xrows, ncol_max, d_in);
         // A pool [S][R_max][d_in]: map g has boxes of 64 columns x 16 (g + 1)
-        // rank rows of one slot (x kk slices: {64, R_max, S, d_in / 64} view)
+        // rank rows of one slot, or (groups) map 0 boxes of R_max rows of G
+        // slots (x kk slices: {64, R_max, S, d_in / 64} view)
         ShrinkMaps smaps;
-        for (int g = 0; g < sa.R16 / 16; ++g) {
-            const uint32_t rows = (uint32_t)(16 * (g + 1));
+        for (int g = 0; g < (grouped ? 1 : sa.R16 / 16); ++g) {
+            const uint32_t rows = grouped ? (uint32_t)pool->R_max : (uint32_t)(16 * (g + 1));
+            const uint32_t slots = grouped ? (uint32_t)G : 1u;
             bool okm;
             if (sa.kk == 1) {
                 const uint64_t da[3] = {(uint64_t)d_in, (uint64_t)pool->R_max, (uint64_t)pool->S};
                 const uint64_t pa[2] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2};
-                const uint32_t ba[3] = {64, rows, 1};
+                const uint32_t ba[3] = {64, rows, slots};
                 okm = make_tmap_nd(&smaps.a[g], pool->A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
             } else {
                 const uint64_t da[4] = {64, (uint64_t)pool->R_max, (uint64_t)pool->S, (uint64_t)d_in / 64};
                 const uint64_t pa[3] = {(uint64_t)d_in * 2, (uint64_t)pool->R_max * d_in * 2, 128};
-                const uint32_t ba[4] = {64, rows, 1, (uint32_t)sa.kk};
+                const uint32_t ba[4] = {64, rows, slots, (uint32_t)sa.kk};
                 okm = make_tmap_nd(&smaps.a[g], pool->A, 4, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B);
             }
             if (!okm) return LORA_ECUDA;

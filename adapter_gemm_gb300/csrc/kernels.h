@@ -50,10 +50,14 @@ struct ShrinkArgs {
     int by_slot;                 // unit u = the u-th adapter slot the ids name, rows found in the ids (T <= 128)
     int tmem_cols;               // TMEM columns allocated: a power of two >= max(32, R16)
     int kk;                      // 64-column K slices per stage (> 1: 4-D views of the A pool)
+    int G;                       // 0: one slot per unit; else groups of G consecutive slot ids (R_max each)
+    const int32_t* indptr;       // [S + 1] plan segment starts (grouped units on the plan)
+    const int32_t* slot_of_token;  // [T] each token's slot (grouped units on the plan)
 };
 
 // The shrink's A-pool maps: map g has boxes of 16 (g + 1) rank rows of one
-// slot, 64 columns, kk slices (a 4-D view when kk > 1).
+// slot, 64 columns, kk slices (a 4-D view when kk > 1); for units of slot
+// groups, map 0 has boxes of R_max rows of G slots.
 struct ShrinkMaps {
     CUtensorMap a[kMaxRank / 16];
 };

@@ -44,7 +44,7 @@ constexpr uint32_t kShHeader = 2048;         // barriers, tokens, scratch ints (
 constexpr uint32_t kShRing = 192 * 1024;     // ring of stages; also the partial rows after the K loop
 constexpr uint32_t kShSlack = kShM * kShSlice;  // what an MMA may read past the ring's end
 constexpr size_t kShSmem = 1024 + kShHeader + kShRing + kShSlack;
-static_assert((3 * kShMaxStages + 1) * 8 + (kShM + 40) * 4 <= kShHeader, "shrink header");
+static_assert((3 * kShMaxStages + 1) * 8 + (2 * kShM + 40) * 4 <= kShHeader, "shrink header");
 static_assert((size_t)kShM * kMaxRank * 4 <= kShRing, "partial rows of every sender fit the ring");
 static_assert(kShRing >= 2 * (kShM + kMaxRank) * kShSlice, "two one-slice stages of the largest unit");
 
@@ -101,8 +101,9 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     uint64_t* ready = empty + kShMaxStages;                  // [kShMaxStages] stage landed, proxy-fenced
     uint64_t* done = ready + kShMaxStages;
     int* tok = reinterpret_cast<int*>(done + 1);             // [128] token of each unit row
-    int* misc = tok + kShM;                                  // [0] TMEM address; by-slot scan: [1..32] slot bits,
-                                                             // [33] slot, [34..37] counts
+    int* rslot = tok + kShM;                                 // [128] its slot
+    int* misc = rslot + kShM;                                // [0] TMEM address; unit search: [1..32] group bits,
+                                                             // [33..37] choice and counts
     uint8_t* ring = base + kShHeader;
     float* recv = reinterpret_cast<float*>(ring);            // after the K loop: [ks][128 / ks][R16] partial rows
 
@@ -139,17 +140,22 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     // read U or x_sorted: wait for them, then let the next kernel start.
     pdl_wait_trigger();
 
-    // This CTA's unit: slot s, plan positions [b, b + n), its rows' tokens.
-    int s = 0, b = 0, n = 0;
+    // This CTA's unit: adapter slots [s0, s1) - one slot, or a group of G
+    // consecutive slot ids - plan positions [b, b + n), and per row its token
+    // and its slot.
+    int s0 = 0, s1 = 0, b = 0, n = 0;
+    const int G = a.G > 0 ? a.G : 1;
     if (a.by_slot) {
-        // Unit u is the u-th smallest adapter slot (rank > 0) that the batch's
-        // ids name; its rows are the tokens on it, ascending.
-        uint32_t* present = reinterpret_cast<uint32_t*>(misc + 1);    // [32] bits: slots 0..1023
+        // Unit u: the u-th smallest group that holds a slot of rank > 0 named
+        // by the batch's ids; its rows are the tokens on such slots, ascending.
+        uint32_t* present = reinterpret_cast<uint32_t*>(misc + 1);    // [32] bits: groups 0..1023
         if (threadIdx.x < 32) present[threadIdx.x] = 0u;
         __syncthreads();
         const int t = threadIdx.x;
         const int id = t < a.T ? a.ids[t] : 0;
-        if (t < a.T && id >= 1 && id < a.S && a.rank[id] > 0) atomicOr(&present[id >> 5], 1u << (id & 31));
+        const bool adapted = t < a.T && id >= 1 && id < a.S && a.rank[id] > 0;
+        const int grp = adapted ? (id - 1) / G : 0;
+        if (adapted) atomicOr(&present[grp >> 5], 1u << (grp & 31));
         __syncthreads();
         if (warp == 0) {
             const uint32_t wbits = present[lane];
@@ -165,11 +171,15 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
                 for (int q = 0; q < u - before; ++q) w &= w - 1u;       // drop the lower set bits
                 misc[33] = 32 * lane + __ffs(w) - 1;
             }
-            if (lane == 31 && u >= inc) misc[33] = 0;                  // fewer adapter slots than units
+            if (lane == 31 && u >= inc) misc[33] = -1;                 // fewer groups than units
         }
         __syncthreads();
-        s = misc[33];
-        const bool f = s > 0 && t < kShM && t < a.T && id == s;
+        const int gsel = misc[33];
+        if (gsel >= 0) {
+            s0 = 1 + gsel * G;
+            s1 = min(a.S, s0 + G);
+        }
+        const bool f = gsel >= 0 && adapted && grp == gsel && t < kShM;
         const unsigned bal = __ballot_sync(0xffffffffu, f);
         if (warp < 4 && lane == 0) misc[34 + warp] = __popc(bal);
         __syncthreads();
@@ -178,18 +188,74 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
             before += w < warp ? misc[34 + w] : 0;
             n += misc[34 + w];
         }
-        if (f) tok[before + __popc(bal & ((1u << lane) - 1u))] = t;
+        if (f) {
+            const int pos = before + __popc(bal & ((1u << lane) - 1u));
+            tok[pos] = t;
+            rslot[pos] = id;
+        }
+    } else if (a.G > 0) {
+        // Plan order: the rows of slots [lo, hi) are the plan positions
+        // [indptr[lo], indptr[hi]); unit u is a 128-row chunk of one group's.
+        const int n_groups = (a.S - 1 + G - 1) / G;
+        if (warp == 0) {
+            if (lane == 0) misc[33] = -1;
+            __syncwarp();
+            int base = 0;
+            for (int g0 = 0; g0 < n_groups; g0 += 32) {
+                const int g = g0 + lane;
+                int beg = 0, cnt = 0;
+                if (g < n_groups) {
+                    const int lo = 1 + g * G, hi = min(a.S, lo + G);
+                    beg = a.indptr[lo];
+                    cnt = a.indptr[hi] - beg;
+                }
+                const int ch = (cnt + kShM - 1) / kShM;
+                int inc = ch;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, inc, d);
+                    if (lane >= d) inc += v;
+                }
+                const int before = base + inc - ch, u = (int)blockIdx.x;
+                if (u >= before && u < before + ch) {
+                    misc[33] = g;
+                    misc[34] = beg + kShM * (u - before);
+                    misc[35] = min(kShM, cnt - kShM * (u - before));
+                }
+                base += __shfl_sync(0xffffffffu, inc, 31);
+            }
+        }
+        __syncthreads();
+        if (misc[33] >= 0) {
+            s0 = 1 + misc[33] * G;
+            s1 = min(a.S, s0 + G);
+            b = misc[34];
+            n = misc[35];
+        }
+        if ((int)threadIdx.x < n) {
+            const int t = a.token_order[b + threadIdx.x];
+            tok[threadIdx.x] = t;
+            rslot[threadIdx.x] = a.slot_of_token[t];
+        }
     } else if ((int)blockIdx.x < *a.n_tiles) {
         const int4 tile = a.tiles[blockIdx.x];
-        s = tile.x;
+        s0 = tile.x;
+        s1 = tile.x + 1;
         b = tile.y;
         n = tile.z - tile.y;
-        if (threadIdx.x < n) tok[threadIdx.x] = a.token_order[b + threadIdx.x];
+        if ((int)threadIdx.x < n) {
+            tok[threadIdx.x] = a.token_order[b + threadIdx.x];
+            rslot[threadIdx.x] = s0;
+        }
     }
-    const int r = s > 0 ? min(a.rank[s], a.R_max) : 0;
+    (void)s1;
+    // The MMA's columns: one slot's rank rounded up to 16, or the G slots of a
+    // group at R_max ranks each (row i reads its slot's at (slot - s0) R_max).
+    const int r = (a.G > 0) ? (s0 > 0 ? a.R_max : 0) : (s0 > 0 ? min(a.rank[s0], a.R_max) : 0);
+    const int ncol = a.G > 0 ? a.G * a.R_max : (r + 15) & ~15;
     const bool do_mma = r > 0 && n > 0;
     const bool copy = a.x_sorted != nullptr && n > 0;
-    __syncthreads();                                 // tok[] is complete
+    __syncthreads();                                 // tok[], rslot[] are complete
 
     // Nothing to do (the same for every CTA of the cluster): leave.
     if (!do_mma && !copy) {
@@ -205,9 +271,8 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     // unit of few rows keeps many K slices in flight. The MMA reads 128 rows
     // of an x slice; past the unit's rows it reads the next bytes of the ring
     // (or the slack after it), which only reach product rows never read back.
-    const int r16 = (r + 15) & ~15;                  // MMA N; A rows past r are zero in the pool
     const uint32_t xslice = (uint32_t)((n + 7) & ~7) * kShSlice;   // one slice of the unit's x rows
-    const uint32_t aslice = (uint32_t)r16 * kShSlice;              // one slice of A_s
+    const uint32_t aslice = (uint32_t)ncol * kShSlice;             // one slice of the A rows
     const uint32_t xbytes = (uint32_t)KK * xslice;                 // x part of a stage, then the A part
     const uint32_t stage_bytes = xbytes + (uint32_t)KK * aslice;
     const int NST = min(kShMaxStages, (int)(kShRing / stage_bytes));
@@ -228,9 +293,9 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
                     // the whole box is counted, slices past d_in included (zero filled)
                     mbar_arrive_expect_tx(fb, (uint32_t)KK * aslice);
                     const uint32_t dA = smem_u32(ring + (size_t)st * stage_bytes + xbytes);
-                    const CUtensorMap* tm = &maps.a[r16 / 16 - 1];
-                    if (KK == 1) tma_load_3d(dA, tm, fb, k_lo + it * 64, 0, s);
-                    else tma_load_4d(dA, tm, fb, 0, 0, s, k_lo / 64 + it * KK);
+                    const CUtensorMap* tm = &maps.a[a.G > 0 ? 0 : ncol / 16 - 1];
+                    if (KK == 1) tma_load_3d(dA, tm, fb, k_lo + it * 64, 0, s0);
+                    else tma_load_4d(dA, tm, fb, 0, 0, s0, k_lo / 64 + it * KK);
                 } else {
                     mbar_arrive(fb);
                 }
@@ -244,7 +309,7 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     } else if (warp == 1) {
         if (lane == 0) {
             // MMA issuer: D[row, j] (+)= x_slice[row, :] . A_slice[j, :]
-            const uint32_t idesc = idesc_bf16_f32(kShM, (uint32_t)(r16 > 0 ? r16 : 16));
+            const uint32_t idesc = idesc_bf16_f32(kShM, (uint32_t)(ncol > 0 ? ncol : 16));
             for (int it = 0; it < n_it; ++it) {
                 const int st = it % NST;
                 if (!mbar_wait(smem_u32(&ready[st]), (uint32_t)((it / NST) & 1), kErrFullWait)) {
@@ -357,12 +422,21 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     }
 
     // Epilogue, warps 2..5: warp w reads TMEM lanes 32 (w % 4) .. +31, i.e.
-    // unit rows i = 32 (w % 4) + lane, and sends or stores them.
-    const float sc = do_mma ? a.scale[s] : 0.f;
-    const int rc8 = (r + 7) & ~7;                    // U columns written
-    const int wc = a.U_hl ? a.R16 : rc8;
+    // unit rows i = 32 (w % 4) + lane, and sends or stores them. Row i's U is
+    // its slot's rank columns, rounded up to 8, at (slot - s0) R_max in a
+    // group, from 0 for one slot; with U_hl the columns past them up to R16
+    // are written as zeros.
     const bool epi = warp >= 2 && warp < 6;
     const int i = 32 * (warp & 3) + lane;
+    int i_off = 0, i_rc8 = 0;
+    float i_sc = 0.f;
+    if (epi && do_mma && i < n) {
+        const int si = rslot[i];
+        const int ri = si > 0 ? min(a.rank[si], a.R_max) : 0;
+        i_rc8 = (ri + 7) & ~7;
+        i_sc = ri > 0 ? a.scale[si] : 0.f;
+        i_off = a.G > 0 ? (si - s0) * a.R_max : 0;
+    }
     bool have = false;
     if (epi && do_mma) {
         bool got = true;
@@ -372,31 +446,9 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     }
     const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     if (ks == 1) {
-        if (epi && do_mma) {
-            for (int c = 0; c < wc; c += 16) {
-                float v[16];
-                if (have && c < r16 && n_it > 0) {
-                    tc_ld16(trow + (uint32_t)c, v);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) v[q] = 0.f;
-                }
-                if (i < n)
-#pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        if (c + q < wc) shrink_store(a, tok, b, i, c + q, c + q < rc8 ? sc * v[q] : 0.f);
-            }
-        }
-    } else {
-        // Row i goes to cluster rank i % ks, which keeps it as its row i / ks.
-        const int rows_per = kShM / ks;
-        cluster_sync_all();                          // every CTA is done with its stages (recv)
         if (epi && do_mma && 32 * (warp & 3) < n) {
-            // the TMEM loads are warp-wide; lanes past the unit's rows send nothing
-            const bool mine = i < n;
-            const uint32_t rb = mapa_shared(smem_u32(recv), (uint32_t)(i % ks));
-            const uint32_t off = (uint32_t)((kz * rows_per + i / ks) * a.R16) * 4u;
-            for (int c = 0; c < r16; c += 16) {
+            // the TMEM loads are warp-wide; lanes past the unit's rows store nothing
+            for (int c = 0; c < ncol; c += 16) {
                 float v[16];
                 if (have && n_it > 0) {
                     tc_ld16(trow + (uint32_t)c, v);
@@ -404,25 +456,58 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
 #pragma unroll
                     for (int q = 0; q < 16; ++q) v[q] = 0.f;
                 }
-                if (mine)
+                if (i < n)
 #pragma unroll
-                    for (int q = 0; q < 16; q += 4)
-                        st_cluster_v4(rb + off + (uint32_t)(c + q) * 4u, v[q], v[q + 1], v[q + 2], v[q + 3]);
+                    for (int q = 0; q < 16; ++q) {
+                        const int j = c + q - i_off;
+                        if (j >= 0 && j < i_rc8) shrink_store(a, tok, b, i, j, i_sc * v[q]);
+                    }
+            }
+            if (a.U_hl && i < n)
+                for (int j = i_rc8; j < a.R16; ++j) shrink_store(a, tok, b, i, j, 0.f);
+        }
+    } else {
+        // Row i goes to cluster rank i % ks, which keeps it as its row i / ks.
+        const int rows_per = kShM / ks;
+        cluster_sync_all();                          // every CTA is done with its stages (recv)
+        if (epi && do_mma && 32 * (warp & 3) < n) {
+            // the TMEM loads are warp-wide; lanes past the unit's rows send nothing
+            const uint32_t rb = mapa_shared(smem_u32(recv), (uint32_t)(i % ks)) +
+                                (uint32_t)((kz * rows_per + i / ks) * a.R16) * 4u;
+            for (int c = 0; c < ncol; c += 16) {
+                float v[16];
+                if (have && n_it > 0) {
+                    tc_ld16(trow + (uint32_t)c, v);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) v[q] = 0.f;
+                }
+                if (i < n)
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const int j = c + q - i_off;
+                        if (j >= 0 && j < i_rc8) st_cluster_f32(rb + (uint32_t)j * 4u, v[q]);
+                    }
             }
         }
         cluster_sync_all();                          // every partial row has landed
         if (do_mma) {
             // Rows kz, kz + ks, ... of the unit: the senders' partials in rank order.
             const int n_mine = n > kz ? (n - kz + ks - 1) / ks : 0;
-            for (int el = threadIdx.x; el < n_mine * wc; el += kShThreads) {
-                const int li = el / wc, col = el % wc;
+            for (int el = threadIdx.x; el < n_mine * a.R16; el += kShThreads) {
+                const int li = el / a.R16, col = el % a.R16;
+                const int row = kz + li * ks;
+                const int si = rslot[row];
+                const int ri = si > 0 ? min(a.rank[si], a.R_max) : 0;
+                const int rc8 = (ri + 7) & ~7;
+                if (col >= (a.U_hl ? a.R16 : rc8)) continue;
                 float v = 0.f;
                 if (col < rc8) {
                     v = recv[(size_t)li * a.R16 + col];
                     for (int z = 1; z < ks; ++z) v += recv[((size_t)z * rows_per + li) * a.R16 + col];
-                    v *= sc;
+                    v *= a.scale[si];
                 }
-                shrink_store(a, tok, b, kz + li * ks, col, v);
+                shrink_store(a, tok, b, row, col, v);
             }
         }
     }

@@ -185,6 +185,33 @@ def test_ragged_shapes(T, K, N, S, R):
     assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
 
 
+# Decode batches whose pool has R_max <= 16 and enough rows per group of G
+# consecutive slot ids (G R_max <= 256) take grouped shrink units: one MMA per
+# K step over every slot of the group, each row keeping its own slot's
+# columns. The cases: groups found in the ids (T <= 64) and on the plan
+# (chunks of 128 rows), R_max 8 and 16, d_in not a multiple of 64 (one slice
+# per stage), ranks below R_max, uninstalled (rank-0) slots inside a group, a
+# last group cut short by S, invalid ids, slot-0 rows.
+GROUPED = [(64, 1024, 512, 40, 16), (48, 1000, 264, 20, 8), (100, 512, 256, 30, 16),
+           (300, 768, 384, 51, 16), (256, 4096, 1024, 51, 16)]
+
+
+@pytest.mark.parametrize("T,K,N,S,R", GROUPED)
+def test_grouped_shrink_units(T, K, N, S, R):
+    rng = np.random.default_rng(T + S)
+    ranks = [0] + [0 if s % 7 == 3 else int(rng.integers(1, R + 1)) for s in range(1, S)]
+    w = WL.random_case(seed=900 + T, T=T, K=K, N=N, S=S, R_max=R, ranks=ranks)
+    w.ids[::17] = -1                                   # invalid ids: counted, base rows
+    w.ids[5::23] = S
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    assert_parity(y, dw.oracle(0), f"grouped shrink T={T} S={S} R={R}")
+    base = torch.as_tensor((w.ids <= 0) | (w.ids >= S) | (np.asarray(ranks)[np.clip(w.ids, 0, S - 1)] == 0),
+                           device=DEV)
+    yb = dw.run(0, base_only=True)
+    assert torch.equal(y[base].view(torch.int16), yb[base].view(torch.int16))
+
+
 # ---------------------------------------------------------- wiring & edges ----
 
 def test_perturbing_a_slot_changes_exactly_its_rows():
