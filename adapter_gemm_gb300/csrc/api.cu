@@ -587,19 +587,22 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // 128-row work tiles).
         // A group pays for all its slots' A rows, so it is taken only when the
         // batch has rows enough to name several slots of each group (T at
-        // least 8 per group). Measured per chained layer sweep step (us, one
-        // slot / groups of 16): T = 512: 432.7 / 404.0; T = 64: 231.7 / 227.2;
-        // T = 8: 166.6 / 190.0; T = 1: 135.1 / 160.5.
+        // least 8 per group), and few enough per slot that one slot's rows do
+        // not fill the MMA's 128 (fewer than 32 per slot; prefill batches keep
+        // one slot per unit). Measured per chained layer sweep step (us, one
+        // slot / groups of 16): T = 512: 432.7 / 404.0 (decode targets only);
+        // T = 64: 231.7 / 227.2; T = 8: 166.6 / 190.0; T = 1: 135.1 / 160.5.
         const bool by_slot = path == 0 && T <= kBySlotMaxT;
         int G = 256 / sa.R16;
         if ((G * pool->R_max) % 16 != 0) G &= ~1;
-        const bool grouped = path == 0 && pool->R_max <= 16 && pool->S > 2 &&
-                             T >= 8 * ((pool->S - 1 + G - 1) / G);
+        const bool grouped = pool->R_max <= 16 && pool->S > 2 && T >= 8 * ((pool->S - 1 + G - 1) / G) &&
+                             T < 32 * (pool->S - 1);
         if (!grouped) G = 0;
         const int n_groups = grouped ? (pool->S - 1 + G - 1) / G : pool->S - 1;
         int grid_x;
         if (by_slot) grid_x = n_groups < T ? n_groups : T;
-        else if (grouped) grid_x = (T + kTileRows - 1) / kTileRows + n_groups;
+        else if (grouped) grid_x = (T + kTileRows - 1) / kTileRows + n_groups +
+                                   (path == 1 ? (T + kTileRows - 1) / kTileRows : 0);   // slot 0's chunks
         else grid_x = plan->max_tiles;
         sa.S = pool->S;
         sa.by_slot = by_slot ? 1 : 0;

@@ -196,11 +196,21 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     } else if (a.G > 0) {
         // Plan order: the rows of slots [lo, hi) are the plan positions
         // [indptr[lo], indptr[hi]); unit u is a 128-row chunk of one group's.
+        // With x_sorted the chunks of slot 0's rows come first (copy only).
         const int n_groups = (a.S - 1 + G - 1) / G;
         if (warp == 0) {
             if (lane == 0) misc[33] = -1;
             __syncwarp();
             int base = 0;
+            if (a.x_sorted) {
+                const int cnt0 = a.indptr[1], u = (int)blockIdx.x;
+                base = (cnt0 + kShM - 1) / kShM;
+                if (lane == 0 && u < base) {
+                    misc[33] = -2;                            // slot 0
+                    misc[34] = kShM * u;
+                    misc[35] = min(kShM, cnt0 - kShM * u);
+                }
+            }
             for (int g0 = 0; g0 < n_groups; g0 += 32) {
                 const int g = g0 + lane;
                 int beg = 0, cnt = 0;
@@ -226,9 +236,9 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
             }
         }
         __syncthreads();
-        if (misc[33] >= 0) {
-            s0 = 1 + misc[33] * G;
-            s1 = min(a.S, s0 + G);
+        if (misc[33] >= 0 || misc[33] == -2) {
+            s0 = misc[33] >= 0 ? 1 + misc[33] * G : 0;
+            s1 = misc[33] >= 0 ? min(a.S, s0 + G) : 1;
             b = misc[34];
             n = misc[35];
         }

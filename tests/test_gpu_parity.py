@@ -185,15 +185,19 @@ def test_ragged_shapes(T, K, N, S, R):
     assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
 
 
-# Decode batches whose pool has R_max <= 16 and enough rows per group of G
-# consecutive slot ids (G R_max <= 256) take grouped shrink units: one MMA per
-# K step over every slot of the group, each row keeping its own slot's
-# columns. The cases: groups found in the ids (T <= 64) and on the plan
-# (chunks of 128 rows), R_max 8 and 16, d_in not a multiple of 64 (one slice
-# per stage), ranks below R_max, uninstalled (rank-0) slots inside a group, a
-# last group cut short by S, invalid ids, slot-0 rows.
+# Batches whose pool has R_max <= 16, at least 8 rows per group of G
+# consecutive slot ids (G R_max <= 256) and fewer than 32 rows per slot take
+# grouped shrink units: one MMA per K step over every slot of the group, each
+# row keeping its own slot's columns. The cases: groups found in the ids
+# (T <= 64) and on the plan (chunks of 128 rows), for the decode kernel and
+# for the prefill kernel (its plan-ordered copy of x, slot 0's rows as
+# copy-only units, U as bf16 high and low parts), R_max 8 and 16, d_in not a
+# multiple of 64 (one slice per stage), ranks below R_max, uninstalled
+# (rank-0) slots inside a group, a last group cut short by S, invalid ids,
+# slot-0 rows.
 GROUPED = [(64, 1024, 512, 40, 16), (48, 1000, 264, 20, 8), (100, 512, 256, 30, 16),
-           (300, 768, 384, 51, 16), (256, 4096, 1024, 51, 16)]
+           (300, 768, 384, 51, 16), (256, 4096, 1024, 51, 16), (700, 512, 512, 51, 16),
+           (900, 256, 264, 40, 8)]
 
 
 @pytest.mark.parametrize("T,K,N,S,R", GROUPED)
