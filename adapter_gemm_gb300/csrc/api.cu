@@ -482,6 +482,23 @@ int lora_linear_path(int T, int d_in, int d_out) {
     return (kb >= 2 && units * 2 <= num_sms()) ? 0 : 1;
 }
 
+// With a pool the choice also weighs the adapters' ranks: from 257 to 640
+// rows the skinny kernel's expand grows with the pool's (slot, 16-rank)
+// chunks, while the wide kernel's expand steps stay within its tiles.
+// Measured per chained step (us, skinny / wide; K = N = 4096, 256 < T <= 640):
+// rank 16 x 64 adapters: 42.6 / 56.6 at 281 rows, 65.9 / 59.6 at 563; rank 64
+// x 16: 52.0 / 55.5 at 299, 78.8 / 62.9 at 616; rank 64 x 32: 64.4 / 62.4 at
+// 281; rank 64 x 64: 93.6 / 87.1 at 281, 162.8 / 78.3 at 563; rank 128 x 16:
+// 69.4 / 70.7 at 299, 71.2 / 67.8 at 457; rank 128 x 64: 149.7 / 131.2 at
+// 281. So the wide kernel takes pools of at least 128 chunks, and of at
+// least 64 above 560 rows.
+int lora_linear_path_for(int T, int d_in, int d_out, int S, int R_max) {
+    const int base = lora_linear_path(T, d_in, d_out);
+    if (base != 0 || T <= kSkinnyOnlyMaxT || S < 2 || R_max < 1) return base;
+    const int chunks = (S - 1) * ((R_max + 15) / 16);
+    return (chunks >= 128 || (T > 560 && chunks >= 64)) ? 1 : 0;
+}
+
 static_assert(kMaxSlices == LORA_MAX_SLICES, "slice limit of the C ABI and the kernels");
 
 namespace {
@@ -512,7 +529,8 @@ bool pool_overlaps(const Range& prev, const lora_pool* pool, int d_in, int d_out
 lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out, const lora_pool* pool,
                         const lora_plan_t* plan, void* y, int ldy, const SliceSet* slices, void* stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int path = lora_linear_path(T, d_in, d_out);
+    const int path = pool ? lora_linear_path_for(T, d_in, d_out, pool->S, pool->R_max)
+                          : lora_linear_path(T, d_in, d_out);
     if (plan && path == 1 && !plan->x_sorted) return LORA_ESHAPE;
     if (plan && path == 0 && !plan->ids) return LORA_EINVAL;     // lora_plan was never run
     const int n_sl = slices ? slices->n : 1;
@@ -587,16 +605,18 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // 128-row work tiles).
         // A group pays for all its slots' A rows, so it is taken only when the
         // batch has rows enough to name several slots of each group (T at
-        // least 8 per group), and few enough per slot that one slot's rows do
-        // not fill the MMA's 128 (fewer than 32 per slot; prefill batches keep
-        // one slot per unit). Measured per chained layer sweep step (us, one
-        // slot / groups of 16): T = 512: 432.7 / 404.0 (decode targets only);
-        // T = 64: 231.7 / 227.2; T = 8: 166.6 / 190.0; T = 1: 135.1 / 160.5.
+        // least 8 per group); on the prefill kernel also only while one slot's
+        // rows do not fill the MMA's 128 (fewer than 32 per slot). Measured
+        // per chained layer sweep step (us, one slot / groups of 16): T = 512:
+        // 432.7 / 404.0 (decode targets only); T = 64: 231.7 / 227.2; T = 8:
+        // 166.6 / 190.0; T = 1: 135.1 / 160.5. On one 4096 -> 4096 layer with 4
+        // adapters of 64 rows (T = 281): 32.7 / 30.1 (rank 16), 32.5 / 29.9
+        // (rank 8).
         const bool by_slot = path == 0 && T <= kBySlotMaxT;
         int G = 256 / sa.R16;
         if ((G * pool->R_max) % 16 != 0) G &= ~1;
         const bool grouped = pool->R_max <= 16 && pool->S > 2 && T >= 8 * ((pool->S - 1 + G - 1) / G) &&
-                             T < 32 * (pool->S - 1);
+                             (path == 0 || T < 32 * (pool->S - 1));
         if (!grouped) G = 0;
         const int n_groups = grouped ? (pool->S - 1 + G - 1) / G : pool->S - 1;
         int grid_x;
@@ -886,7 +906,7 @@ lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* 
         const lora_status r = lora_plan(ids_dev, T, plan, stream);
         if (r != LORA_OK) return r;
     }
-    const lora_status r = lora_linear(x_dev, W, T, d_in, d_out, plan ? pool : nullptr, plan, y_dev, stream);
+    const lora_status r = lora_linear(x_dev, W, T, d_in, d_out, pool, plan, y_dev, stream);
     if (r != LORA_OK) return r;
     if (cudaMemcpyAsync(y_host, y_dev, (size_t)T * d_out * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return LORA_ECUDA;
@@ -922,7 +942,7 @@ lora_status lora_linear_sliced(const void* x, const void* W, int T, int d_in, in
     // shrink fused in) and no weight tile straddles two slices; else one
     // call per slice, each writing its columns of y.
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    bool one = lora_linear_path(T, d_in, N) == 0 && T <= 64 && plan->S >= 2 &&
+    bool one = lora_linear_path_for(T, d_in, N, plan->S, plan->R_max) == 0 && T <= 64 && plan->S >= 2 &&
                (plan->S - 1) * ((plan->R_max + 15) / 16 * 16) <= 128;
     for (int q = 0; q + 1 < n_slices; ++q) one = one && d_outs[q] % 128 == 0;
     if (one) {

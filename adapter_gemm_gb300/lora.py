@@ -65,6 +65,7 @@ _SIGS = {
     "lora_linear": (_c_int, [_c_void_p, _c_void_p, _c_int, _c_int, _c_int, ctypes.POINTER(lora_pool),
                              ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p]),
     "lora_linear_path": (_c_int, [_c_int, _c_int, _c_int]),
+    "lora_linear_path_for": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "lora_linear_rows": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
                                   ctypes.POINTER(lora_pool), ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p,
                                   _c_void_p]),
@@ -141,8 +142,11 @@ def version() -> int:
     return _lib().lora_version()
 
 
-def linear_path(T: int, d_in: int, d_out: int) -> int:
-    """0 = skinny (swap-AB split-K cluster kernel), 1 = wide (persistent 128x256)."""
+def linear_path(T: int, d_in: int, d_out: int, pool: "Pool | None" = None) -> int:
+    """Kernel family a call takes: 0 skinny (decode), 1 wide (prefill); with a
+    pool, the rank-aware choice for its S and R_max."""
+    if pool is not None:
+        return _lib().lora_linear_path_for(T, d_in, d_out, pool.S, pool.R_max)
     return _lib().lora_linear_path(T, d_in, d_out)
 
 
@@ -241,7 +245,8 @@ class Plan:
 
 def linear(x: torch.Tensor, W: torch.Tensor, pool: Pool | None = None, plan: Plan | None = None,
            y: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y = x W^T + per-row adapter correction (plan=None: base projection only)."""
+    """y = x W^T + per-row adapter correction (plan=None: base projection only,
+    on the kernel a call with this pool would take)."""
     if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1]:
         raise ValueError("x [T, d_in] and W [d_out, d_in] expected")
     T, d_in = x.shape
@@ -251,7 +256,7 @@ def linear(x: torch.Tensor, W: torch.Tensor, pool: Pool | None = None, plan: Pla
     if plan is not None and pool is None:
         raise ValueError("a plan needs a pool")
     _check(_lib().lora_linear(_ptr(x, torch.bfloat16, "x"), _ptr(W, torch.bfloat16, "W"), T, d_in, d_out,
-                              ctypes.byref(pool.c) if plan is not None else None,
+                              ctypes.byref(pool.c) if pool is not None else None,
                               ctypes.byref(plan.c) if plan is not None else None,
                               _ptr(y, torch.bfloat16, "y"), _stream(stream)), "lora_linear")
     return y
@@ -273,7 +278,7 @@ def linear_rows(x_all: torch.Tensor, rows: torch.Tensor, W: torch.Tensor, pool: 
         raise ValueError("a plan needs a pool")
     _check(_lib().lora_linear_rows(_ptr(x_all, torch.bfloat16, "x_all"), T_all, _ptr(rows, torch.int32, "rows"), T,
                                    d_in, d_out, _ptr(W, torch.bfloat16, "W"),
-                                   ctypes.byref(pool.c) if plan is not None else None,
+                                   ctypes.byref(pool.c) if pool is not None else None,
                                    ctypes.byref(plan.c) if plan is not None else None,
                                    _ptr(x_rows, torch.bfloat16, "x_rows"), _ptr(y, torch.bfloat16, "y"),
                                    _stream(stream)), "lora_linear_rows")
@@ -303,7 +308,7 @@ def linear_host(x_host: torch.Tensor, W: torch.Tensor, y_host: torch.Tensor, x_d
     _check(_lib().lora_linear_host(_c_void_p(x_host.data_ptr()),
                                    _c_void_p(ids_host.data_ptr()) if plan is not None else None,
                                    _c_void_p(y_host.data_ptr()), T, d_in, d_out, _ptr(W, torch.bfloat16, "W"),
-                                   ctypes.byref(pool.c) if plan is not None else None,
+                                   ctypes.byref(pool.c) if pool is not None else None,
                                    ctypes.byref(plan.c) if plan is not None else None,
                                    _ptr(x_dev, torch.bfloat16, "x_dev"),
                                    _ptr(ids_dev, torch.int32, "ids_dev") if plan is not None else None,

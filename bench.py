@@ -477,7 +477,8 @@ class Runner:
             achieved, peak, unit = work.bytes / t_k / 1e9, hbm, "GB/s"
         else:
             achieved, peak, unit = work.flops / t_k / 1e12, tf_burst, "TFLOP/s"
-        kname = ("gemm_skinny_kernel" if L.linear_path(T, td.d_in, n_dom) == 0 else "gemm_wide_kernel")
+        kname = ("gemm_skinny_kernel" if L.linear_path(T, td.d_in, n_dom, self.copies[0][j][1][0]) == 0
+                 else "gemm_wide_kernel")
         if all_kernels:
             kname = f"all {self.u_launch[j]} kernels of the per-slice calls"
         roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,

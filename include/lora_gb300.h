@@ -163,8 +163,12 @@ lora_status lora_plan_check(const lora_plan_t* plan, void* stream, int32_t* n_in
 /* The layer:
  *   x [T, d_in] bf16 device, W [d_out, d_in] bf16 device (nn.Linear layout),
  *   y [T, d_out] bf16 device, written once, round-to-nearest-even from fp32.
- * plan == NULL (pool ignored) runs the base projection only, with the same
- * kernels and tiling that a call with a plan uses for this (T, d_in, d_out).
+ * plan == NULL runs the base projection only, with the same kernels and
+ * tiling that a call with a plan and this pool uses for this (T, d_in, d_out):
+ * the kernel choice weighs the pool's S and R_max (lora_linear_path_for), so
+ * pass the pool (only its S and R_max are read) for a base run whose rows
+ * equal the slot-0 rows of a planned call bitwise; pool == NULL picks as
+ * lora_linear_path.
  * With a plan, pool->S == plan->S, pool->R_max == plan->R_max,
  * pool->d_in == d_in <= plan->d_in_cap, pool->d_out == d_out, T == plan->T.
  * Rows whose slot is 0, or whose slot has rank 0, get exactly the base result.
@@ -201,18 +205,28 @@ lora_status lora_linear_rows(const void* x_all, int T_all, const int32_t* rows, 
  * y_host holds the result once `stream` reaches the end of this call. Calls on
  * two streams, each with its own staging buffers and plan, overlap one call's
  * copies with the other's kernels. plan == NULL runs the base projection
- * (pool, ids_host and ids_dev ignored). Arguments otherwise as for lora_plan
+ * (ids_host and ids_dev ignored; a pool only picks the kernel, as for
+ * lora_linear). Arguments otherwise as for lora_plan
  * and lora_linear; LORA_EINVAL for missing buffers, before anything is queued. */
 lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* y_host, int T, int d_in,
                              int d_out, const void* W, const lora_pool* pool, lora_plan_t* plan,
                              void* x_dev, int32_t* ids_dev, void* y_dev, void* stream);
 
-/* The kernel family lora_linear picks for these sizes on the current device:
- * 0 = skinny (swap-AB, split-K across a thread-block cluster), 1 = wide
- * (persistent 128x256 tiles). Up to 256 rows always 0, above 640 always 1; in
- * between 0 while the skinny kernel's weight tiles can split K in two on
- * every SM. */
+/* The kernel family lora_linear picks for these sizes on the current device
+ * without a pool: 0 = skinny (swap-AB, split-K across a thread-block
+ * cluster), 1 = wide (persistent 128x256 tiles). Up to 256 rows always 0,
+ * above 640 always 1; in between 0 while the skinny kernel's weight tiles can
+ * split K in two on every SM. */
 int lora_linear_path(int T, int d_in, int d_out);
+
+/* The kernel family for a call with a pool of S slots and rank cap R_max
+ * (the rank-aware choice of the LoRA-serving page's section "SGLang: chunked
+ * SGMV, and a rank-aware kernel", made here between the two kernels): as
+ * lora_linear_path, except that from 257 to 640 rows a pool of at least 128
+ * (slot, 16-rank) chunks ((S - 1) * ceil(R_max / 16)), or of at least 64
+ * above 560 rows, takes the wide kernel, whose expand does not grow with the
+ * pool. S < 2 or R_max < 1: as lora_linear_path. */
+int lora_linear_path_for(int T, int d_in, int d_out, int S, int R_max);
 
 /* Most output slices one lora_linear_sliced call takes. */
 #define LORA_MAX_SLICES 4

@@ -43,7 +43,9 @@ class DeviceWorkload:
 
     def run(self, i: int = 0, base_only: bool = False) -> torch.Tensor:
         dt = self.targets[i]
-        y = L.linear(self.x_for(i), dt.W, None if base_only else dt.pool, None if base_only else self.plan)
+        # a base-only run takes the pool too: it picks the kernel (the choice
+        # weighs the pool's ranks), so slot-0 rows compare bitwise
+        y = L.linear(self.x_for(i), dt.W, dt.pool, None if base_only else self.plan)
         torch.cuda.synchronize()
         return y
 

@@ -190,3 +190,11 @@ def test_path_choice(lib):
     assert lib.lora_linear_path(300, 64, 1024) == 1          # one 64-column K slice: no split
     assert lib.lora_linear_path(700, 4096, 1024) == 1
     assert lib.lora_linear_path(4096, 4096, 14336) == 1
+    # the rank-aware choice: (S - 1) * ceil(R_max / 16) chunks from 257 to 640 rows
+    assert lib.lora_linear_path_for(300, 512, 512, 33, 64) == 1      # 128 chunks
+    assert lib.lora_linear_path_for(300, 512, 512, 32, 64) == 0      # 124 chunks
+    assert lib.lora_linear_path_for(600, 512, 512, 17, 64) == 1      # 64 chunks above 560 rows
+    assert lib.lora_linear_path_for(560, 512, 512, 17, 64) == 0
+    assert lib.lora_linear_path_for(256, 4096, 4096, 1024, 128) == 0  # decode-sized: no x_sorted
+    assert lib.lora_linear_path_for(512, 4096, 4096, 51, 16) == 0    # the layer sweep's pools (50 chunks)
+    assert lib.lora_linear_path_for(300, 512, 512, 1, 64) == lib.lora_linear_path(300, 512, 512)

@@ -558,6 +558,27 @@ def test_chunk_dealt_expand_batches(T, K, N, S, R):
     assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
 
 
+# The rank-aware kernel choice: from 257 to 640 rows a pool of at least 128
+# (slot, 16-rank) chunks, or of at least 64 above 560 rows, takes the wide
+# kernel; a base-only run given the pool takes the same one.
+@pytest.mark.parametrize("T,K,N,S,R,path", [
+    (300, 512, 512, 33, 64, 1),      # 128 chunks
+    (600, 512, 520, 17, 64, 1),      # 64 chunks above 560 rows
+    (400, 512, 512, 17, 64, 0),      # 64 chunks at 400 rows: the swap-AB kernel
+    (500, 256, 384, 9, 128, 0),      # 64 chunks of rank 128 at 500 rows
+])
+def test_rank_aware_kernel_choice(T, K, N, S, R, path):
+    assert L.linear_path(T, K, N) == 0
+    w = WL.random_case(seed=T + 31 * S, T=T, K=K, N=N, S=S, R_max=R, base_frac=0.1)
+    dw = DeviceWorkload(w, DEV)
+    assert L.linear_path(T, K, N, dw.targets[0].pool) == path
+    y = dw.run(0)
+    assert_parity(y, dw.oracle(0), f"rank-aware T={T} S={S} R={R} path {path}")
+    slot0 = torch.as_tensor(w.ids == 0, device=DEV)
+    yb = dw.run(0, base_only=True)
+    assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
+
+
 @pytest.mark.parametrize("T,K,N,path", [
     (640, 512, 1024, 0),         # three token tiles on the swap-AB kernel
     (641, 512, 1024, 1),         # past the swap-AB kernel's range
