@@ -734,6 +734,7 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
             if (!make_tmap_nd(&maps.b, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B)) return LORA_ECUDA;
         }
         a.y = static_cast<__nv_bfloat16*>(y);
+        a.W = static_cast<const __nv_bfloat16*>(W);
         a.ldy = ldy;
         a.ex = ex;
         a.T = T;

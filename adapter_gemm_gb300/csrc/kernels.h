@@ -91,6 +91,7 @@ struct SkinnyMaps {
 
 struct SkinnyArgs {
     __nv_bfloat16* y;  // [T, ldy]
+    const __nv_bfloat16* W;  // [N, K] (also read through maps.w): the L2 prefetch before the wait
     ExpandArgs ex;
     SliceExpand sl[kMaxSlices];
     int n_slices;

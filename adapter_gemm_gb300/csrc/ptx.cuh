@@ -176,17 +176,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---------------------------------------------------------------- PDL -------
-// Programmatic dependent launch. Every kernel of this library but the plan
-// kernel lets the next kernel of its stream start (launch_dependents) only
-// after its own wait for the kernels ahead of it has returned: when such a
-// kernel's dependent starts, every kernel before that kernel has completed and
-// its writes are visible. The plan kernel lets its dependents start at once;
-// they read nothing but weights before their own wait, which returns only once
-// the plan kernel - and so its own wait - has completed. A kernel reads, before
-// its own wait, only weights (W and the pool, which no running kernel writes)
-// and buffers that its immediate predecessor - a shrink kernel of the same
-// library call, which waited before it let this kernel start and does not
-// write them - left untouched.
+// Programmatic dependent launch. The plan kernel lets the next kernel of its
+// stream start (launch_dependents) at once; the other kernels only after their
+// own wait for the kernels ahead has returned. A kernel reads, before its own
+// wait, only weights (W and the pool, which no running kernel writes) and -
+// a GEMM right after its call's shrink kernel, which waited for every kernel
+// ahead before it let the GEMM start and writes neither - x and the ids. Its
+// wait returns once the kernel ahead has completed, and that kernel completes
+// only after its own wait, so every kernel before it has completed too and its
+// writes are visible.
 __device__ __forceinline__ void pdl_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }

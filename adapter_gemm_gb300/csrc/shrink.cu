@@ -137,7 +137,11 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     const uint32_t tmem = (uint32_t)misc[0];
 
     // The plan, the ids and x come from the kernels ahead, which may also still
-    // read U or x_sorted: wait for them, then let the next kernel start.
+    // read U or x_sorted: wait for them, then let this call's GEMM start. It
+    // starts its K loop at once (x and the ids are complete by then, and this
+    // kernel writes neither), beside this kernel, and waits for U only in its
+    // epilogue. (Letting it start before this wait costs that overlap: the
+    // layer sweep at T = 1 measured 190.7 against 136.7 us per step.)
     pdl_wait_trigger();
 
     // This CTA's unit: adapter slots [s0, s1) - one slot, or a group of G
