@@ -65,6 +65,9 @@ def parse(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=60.0,
                     help="total CPU time of the reference arm (warm-up + timed steps)")
     ap.add_argument("--kernel-steps", type=int, default=40)
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="run this many eager steps of --config after 3 warm-up steps, untimed, and exit: "
+                         "the launch sequence of one step, for an external profiler's launch list")
     return ap.parse_args(argv)
 
 
@@ -647,6 +650,21 @@ def main(argv=None):
     from adapter_gemm_gb300 import build as B
     B.build()
     from adapter_gemm_gb300 import lora as L, workloads as WL
+
+    if args.profile_steps > 0:
+        # The steps the timed run replays as graphs, launched eagerly (the
+        # same kernels, one launch each), with no timing around them.
+        w = WL.by_name(args.config)
+        r = Runner(w, dev, use_graph=False)
+        n0 = L.launch_count()
+        r.run_steps(3 + args.profile_steps)
+        torch.cuda.synchronize()
+        assert L.last_device_error() == 0, "a kernel gave up a bounded wait"
+        if rank == 0:
+            print(json.dumps({"profile_steps": args.profile_steps, "warmup": 3, "workload": w.name,
+                              "launches": L.launch_count() - n0,
+                              "launches_per_step": r.launches_per_step}), flush=True)
+        return 0
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
