@@ -40,11 +40,11 @@ constexpr int kShThreads = 224;              // warp 0 A copies, warp 1 MMA + TM
 constexpr int kShM = 128;                    // token rows of the MMA
 constexpr uint32_t kShSlice = 128;           // bytes of one row's 64-column K slice
 constexpr int kShMaxStages = 32;
-constexpr uint32_t kShHeader = 2048;         // barriers, tokens, scratch ints (1024-byte multiple)
+constexpr uint32_t kShHeader = 3072;         // barriers, tokens and their slots' ranks and scales, scratch ints
 constexpr uint32_t kShRing = 192 * 1024;     // ring of stages; also the partial rows after the K loop
 constexpr uint32_t kShSlack = kShM * kShSlice;  // what an MMA may read past the ring's end
 constexpr size_t kShSmem = 1024 + kShHeader + kShRing + kShSlack;
-static_assert((3 * kShMaxStages + 1) * 8 + (2 * kShM + 40) * 4 <= kShHeader, "shrink header");
+static_assert((3 * kShMaxStages + 1) * 8 + (4 * kShM + 40) * 4 <= kShHeader, "shrink header");
 static_assert((size_t)kShM * kMaxRank * 4 <= kShRing, "partial rows of every sender fit the ring");
 static_assert(kShRing >= 2 * (kShM + kMaxRank) * kShSlice, "two one-slice stages of the largest unit");
 
@@ -102,7 +102,9 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     uint64_t* done = ready + kShMaxStages;
     int* tok = reinterpret_cast<int*>(done + 1);             // [128] token of each unit row
     int* rslot = tok + kShM;                                 // [128] its slot
-    int* misc = rslot + kShM;                                // [0] TMEM address; unit search: [1..32] group bits,
+    int* rrc8 = rslot + kShM;                                // [128] its slot's rank rounded up to 8 (0: no U)
+    float* rsc = reinterpret_cast<float*>(rrc8 + kShM);     // [128] its slot's alpha / r
+    int* misc = reinterpret_cast<int*>(rsc + kShM);          // [0] TMEM address; unit search: [1..32] group bits,
                                                              // [33..37] choice and counts
     uint8_t* ring = base + kShHeader;
     float* recv = reinterpret_cast<float*>(ring);            // after the K loop: [ks][128 / ks][R16] partial rows
@@ -353,6 +355,15 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
         }
         __syncwarp();
     } else if (warp == 6) {
+        // First, each row's rank and scale for the split-K epilogue (global
+        // loads, off its critical path: they land during the K loop).
+        for (int r = lane; r < n; r += 32) {
+            const int si = rslot[r];
+            const int ri = si > 0 ? min(a.rank[si], a.R_max) : 0;
+            rrc8[r] = (ri + 7) & ~7;
+            rsc[r] = ri > 0 ? a.scale[si] : 0.f;
+        }
+        __syncwarp();
         // A stage's x rows arrive by cp.async (generic proxy) and the MMA reads
         // them through the async proxy: once the stage has landed, this thread
         // fences and hands the stage to the MMA.
@@ -511,15 +522,13 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
             for (int el = threadIdx.x; el < n_mine * a.R16; el += kShThreads) {
                 const int li = el / a.R16, col = el % a.R16;
                 const int row = kz + li * ks;
-                const int si = rslot[row];
-                const int ri = si > 0 ? min(a.rank[si], a.R_max) : 0;
-                const int rc8 = (ri + 7) & ~7;
+                const int rc8 = rrc8[row];               // written by warp 6 before the cluster barriers
                 if (col >= (a.U_hl ? a.R16 : rc8)) continue;
                 float v = 0.f;
                 if (col < rc8) {
                     v = recv[(size_t)li * a.R16 + col];
                     for (int z = 1; z < ks; ++z) v += recv[((size_t)z * rows_per + li) * a.R16 + col];
-                    v *= a.scale[si];
+                    v *= rsc[row];
                 }
                 shrink_store(a, tok, b, row, col, v);
             }
