@@ -194,10 +194,11 @@ def test_ragged_shapes(T, K, N, S, R):
 # copy-only units, U as bf16 high and low parts), R_max 8 and 16, d_in not a
 # multiple of 64 (one slice per stage), ranks below R_max, uninstalled
 # (rank-0) slots inside a group, a last group cut short by S, invalid ids,
-# slot-0 rows.
+# slot-0 rows; 7 groups of 16 slots beside a wide decode output (112 weight
+# tiles).
 GROUPED = [(64, 1024, 512, 40, 16), (48, 1000, 264, 20, 8), (100, 512, 256, 30, 16),
            (300, 768, 384, 51, 16), (256, 4096, 1024, 51, 16), (700, 512, 512, 51, 16),
-           (900, 256, 264, 40, 8)]
+           (900, 256, 264, 40, 8), (64, 4096, 14336, 100, 16)]
 
 
 @pytest.mark.parametrize("T,K,N,S,R", GROUPED)
