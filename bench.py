@@ -80,15 +80,24 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def src_digest() -> str:
-    """Digest of the CUDA sources with comments and blank lines dropped, so a
-    comment-only edit keeps the recorded ncu traffic valid."""
+# The files a kernel's DRAM traffic depends on: its own source, the shared
+# headers and the host code that picks its launch shape.
+KERNEL_SOURCES = {
+    "gemm_skinny_kernel": "gemm_skinny.cu",
+    "gemm_wide_kernel": "gemm_wide.cu",
+    "shrink_tc_kernel": "shrink.cu",
+    "plan_kernel": "plan.cu",
+}
+
+
+def src_digest(kernel: str) -> str:
+    """Digest of the CUDA sources a kernel's traffic depends on, with comments
+    and blank lines dropped, so a comment-only edit (or a change to another
+    kernel) keeps the recorded ncu traffic valid."""
     import re
     h = hashlib.sha256()
     d = os.path.join(ROOT, "adapter_gemm_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
-        if not f.endswith((".cu", ".cuh", ".h")):
-            continue
+    for f in sorted([KERNEL_SOURCES[kernel], "kernels.h", "ptx.cuh", "api.cu"]):
         text = open(os.path.join(d, f), encoding="utf-8").read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         text = re.sub(r"//[^\n]*", "", text)
@@ -100,12 +109,12 @@ def src_digest() -> str:
 
 def ncu_traffic(config: str):
     """dram read+write bytes per launch of the dominant kernel from a committed
-    ncu summary, if it was taken on the current kernel sources."""
+    ncu summary, if it was taken on that kernel's current sources."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(config)
-    if not d or d.get("src_sha") != src_digest():
+    if not d or d.get("src_sha") != src_digest(d["kernel"]):
         return None
     return float(d["dram_bytes_per_launch"])
 
