@@ -1006,7 +1006,7 @@ static int skinny_mode(const SkinnyArgs& a) {
 template <int MODE>
 static cudaError_t launch_skinny_mode(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl, cudaStream_t stream) {
     const size_t smem = a.smem;
-    cudaError_t e = ensure_smem_attr((const void*)gemm_skinny_kernel<MODE>, MODE == 0 ? 1 : 6 + MODE, smem);
+    cudaError_t e = ensure_smem_attr((const void*)gemm_skinny_kernel<MODE>, 1 + MODE, smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.N + kWRows - 1) / kWRows, a.ks, (a.T + a.TN - 1) / a.TN);

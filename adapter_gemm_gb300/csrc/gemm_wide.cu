@@ -349,7 +349,7 @@ gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
 template <int BN, int KK>
 static cudaError_t launch_wide_bn(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
     const size_t smem = WideCfg<BN, KK>::kSmem;
-    cudaError_t e = ensure_smem_attr((const void*)gemm_wide_kernel<BN, KK>, (BN == 256 ? 2 : 3) + (KK == 1 ? 0 : 2),
+    cudaError_t e = ensure_smem_attr((const void*)gemm_wide_kernel<BN, KK>, 6 + (BN == 256 ? 0 : 1) + (KK == 1 ? 0 : 2),
                                      smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};

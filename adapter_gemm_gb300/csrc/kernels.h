@@ -155,7 +155,7 @@ cudaError_t shrink_take_error(int* code);
 // One slot per kernel (instantiation) whose dynamic shared memory limit is
 // raised: 0 plan, 1 swap-AB decode, 2..5 wide (tile width x K slices), 6..8
 // shrink (cp.async depth).
-constexpr int kSmemSlots = 11;
+constexpr int kSmemSlots = 18;
 cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
 
 // Shared-memory bytes the skinny kernel needs for a token tile of TN columns

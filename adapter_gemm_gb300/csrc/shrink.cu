@@ -91,8 +91,10 @@ __device__ __forceinline__ void shrink_store(const ShrinkArgs& a, const int* tok
     }
 }
 
+template <bool BYSLOT, bool GROUPED, bool COPY>
 __global__ void __launch_bounds__(kShThreads, 1)
 shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
+    static_assert(!(BYSLOT && COPY), "rows found in the ids are never copied out");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     // header: barriers, the unit's tokens and scratch ints; then the ring
@@ -123,7 +125,7 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
         for (int i = 0; i < kShMaxStages; ++i) {
             mbar_init(smem_u32(&full[i]), 1 + 128);   // the A copies' arrival + every gathering thread's copies
             // the MMA commit (or a plain arrive), and with x_sorted every gathering thread's copy-out
-            mbar_init(smem_u32(&empty[i]), 1 + (a.x_sorted ? 128 : 0));
+            mbar_init(smem_u32(&empty[i]), 1 + (COPY ? 128 : 0));
             mbar_init(smem_u32(&ready[i]), 1);
         }
         mbar_init(smem_u32(done), 1);
@@ -150,8 +152,8 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     // consecutive slot ids - plan positions [b, b + n), and per row its token
     // and its slot.
     int s0 = 0, s1 = 0, b = 0, n = 0;
-    const int G = a.G > 0 ? a.G : 1;
-    if (a.by_slot) {
+    const int G = GROUPED ? a.G : 1;
+    if (BYSLOT) {
         // Unit u: the u-th smallest group that holds a slot of rank > 0 named
         // by the batch's ids; its rows are the tokens on such slots, ascending.
         uint32_t* present = reinterpret_cast<uint32_t*>(misc + 1);    // [32] bits: groups 0..1023
@@ -199,7 +201,7 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
             tok[pos] = t;
             rslot[pos] = id;
         }
-    } else if (a.G > 0) {
+    } else if (GROUPED) {
         // Plan order: the rows of slots [lo, hi) are the plan positions
         // [indptr[lo], indptr[hi]); unit u is a 128-row chunk of one group's.
         // With x_sorted the chunks of slot 0's rows come first (copy only).
@@ -208,7 +210,7 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
             if (lane == 0) misc[33] = -1;
             __syncwarp();
             int base = 0;
-            if (a.x_sorted) {
+            if (COPY) {
                 const int cnt0 = a.indptr[1], u = (int)blockIdx.x;
                 base = (cnt0 + kShM - 1) / kShM;
                 if (lane == 0 && u < base) {
@@ -267,10 +269,10 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
     (void)s1;
     // The MMA's columns: one slot's rank rounded up to 16, or the G slots of a
     // group at R_max ranks each (row i reads its slot's at (slot - s0) R_max).
-    const int r = (a.G > 0) ? (s0 > 0 ? a.R_max : 0) : (s0 > 0 ? min(a.rank[s0], a.R_max) : 0);
-    const int ncol = a.G > 0 ? a.G * a.R_max : (r + 15) & ~15;
+    const int r = GROUPED ? (s0 > 0 ? a.R_max : 0) : (s0 > 0 ? min(a.rank[s0], a.R_max) : 0);
+    const int ncol = GROUPED ? a.G * a.R_max : (r + 15) & ~15;
     const bool do_mma = r > 0 && n > 0;
-    const bool copy = a.x_sorted != nullptr && n > 0;
+    const bool copy = COPY && n > 0;
     __syncthreads();                                 // tok[], rslot[] are complete
 
     // Nothing to do (the same for every CTA of the cluster): leave.
@@ -309,7 +311,7 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
                     // the whole box is counted, slices past d_in included (zero filled)
                     mbar_arrive_expect_tx(fb, (uint32_t)KK * aslice);
                     const uint32_t dA = smem_u32(ring + (size_t)st * stage_bytes + xbytes);
-                    const CUtensorMap* tm = &maps.a[a.G > 0 ? 0 : ncol / 16 - 1];
+                    const CUtensorMap* tm = &maps.a[GROUPED ? 0 : ncol / 16 - 1];
                     if (KK == 1) tma_load_3d(dA, tm, fb, k_lo + it * 64, 0, s0);
                     else tma_load_4d(dA, tm, fb, 0, 0, s0, k_lo / 64 + it * KK);
                 } else {
@@ -460,7 +462,7 @@ shrink_tc_kernel(const __grid_constant__ ShrinkMaps maps, ShrinkArgs a) {
         const int ri = si > 0 ? min(a.rank[si], a.R_max) : 0;
         i_rc8 = (ri + 7) & ~7;
         i_sc = ri > 0 ? a.scale[si] : 0.f;
-        i_off = a.G > 0 ? (si - s0) * a.R_max : 0;
+        i_off = GROUPED ? (si - s0) * a.R_max : 0;
     }
     bool have = false;
     if (epi && do_mma) {
@@ -550,9 +552,16 @@ int shrink_kk(int xrows, int R16, int K) {
     return 1;
 }
 
-cudaError_t launch_shrink(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_x, bool pdl, cudaStream_t stream) {
-    if (grid_x <= 0) return cudaSuccess;
-    cudaError_t e = ensure_smem_attr((const void*)shrink_tc_kernel, 6, kShSmem);
+// One instantiation per unit source (ids, plan groups or plan tiles) and
+// copy-out, each with only its own code: measured per chained step against
+// one kernel that branches at run time, layer sweep T = 8: 158.3 -> 155.2
+// us; T = 64: 217.2 -> 211.6; T = 512: 401.1 -> 396.4.
+template <bool BYSLOT, bool GROUPED, bool COPY>
+static cudaError_t launch_shrink_as(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_x, bool pdl,
+                                    cudaStream_t stream) {
+    auto kern = shrink_tc_kernel<BYSLOT, GROUPED, COPY>;
+    cudaError_t e = ensure_smem_attr((const void*)kern, 10 + (BYSLOT ? 4 : 0) + (GROUPED ? 2 : 0) + (COPY ? 1 : 0),
+                                     kShSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, a.ks, 1);
@@ -575,7 +584,22 @@ cudaError_t launch_shrink(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, shrink_tc_kernel, maps, a);
+    return cudaLaunchKernelEx(&cfg, kern, maps, a);
+}
+
+cudaError_t launch_shrink(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_x, bool pdl, cudaStream_t stream) {
+    if (grid_x <= 0) return cudaSuccess;
+    const bool grouped = a.G > 0, copy = a.x_sorted != nullptr;
+    if (a.by_slot) {
+        if (copy) return cudaErrorInvalidValue;
+        return grouped ? launch_shrink_as<true, true, false>(maps, a, grid_x, pdl, stream)
+                       : launch_shrink_as<true, false, false>(maps, a, grid_x, pdl, stream);
+    }
+    if (grouped)
+        return copy ? launch_shrink_as<false, true, true>(maps, a, grid_x, pdl, stream)
+                    : launch_shrink_as<false, true, false>(maps, a, grid_x, pdl, stream);
+    return copy ? launch_shrink_as<false, false, true>(maps, a, grid_x, pdl, stream)
+                : launch_shrink_as<false, false, false>(maps, a, grid_x, pdl, stream);
 }
 
 cudaError_t shrink_take_error(int* code) {
