@@ -630,6 +630,12 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         sa.indptr = plan->indptr;
         sa.slot_of_token = plan->slot_of_token;
         sa.ks = shrink_splits(grid_x, d_in);
+        // A few rows of several slots (by-slot units of one or two rows each):
+        // each unit's K loop is short, and its CTAs only take SMs from this
+        // call's GEMM, which starts beside it. Measured per chained layer
+        // sweep step at T = 8 (8 units), split 8 / 4 / 2 / 1: 155.2 / 150.1 /
+        // 148.3 / 182.3 us (T = 1 and T = 64 unchanged by the rule).
+        if (by_slot && grid_x >= 2 && T <= 16 && sa.ks > 2) sa.ks = 2;
         const int ncol_max = grouped ? G * pool->R_max : sa.R16;
         sa.tmem_cols = 32;
         while (sa.tmem_cols < ncol_max) sa.tmem_cols *= 2;
