@@ -191,20 +191,21 @@ int skinny_kk(int TN, bool fuse, bool tce, int a_rows, int K) {
 }
 
 // Launch shape of the skinny kernel. The K split depends only on (T, d_in,
-// d_out) - a base-only call, a call with the shrink kernel ahead and one with
-// the shrink fused in split K identically, so their partial sums agree. The
-// kernel holds tensor memory, so it runs one CTA per SM: the split is the
-// largest (<= 8) whose CTAs fit the SMs. Consecutive layers form a dependent
-// chain (the next layer's x is this one's y), so one GEMM should stream its
-// weights from every SM; measured per chained step (us, half / all SMs):
-// T = 64, 4096 -> 4096, shrink fused: 23.3 / 17.0; layer sweep T = 1: 149.5 /
-// 134.6; T = 8: 170.3 / 165.8; T = 64 (shrink kernel ahead on the SMs the GEMM
-// leaves free): 219.6 / 230.9.
+// d_out) and `cap`, the SMs its CTAs may take (call_shape gives a base-only
+// call with the pool the planned call's cap) - a base-only call, a call with
+// the shrink kernel ahead and one with the shrink fused in split K
+// identically, so their partial sums agree. The kernel holds tensor memory,
+// so it runs one CTA per SM: the split is the largest (<= 8) whose CTAs fit
+// the cap. Consecutive layers form a dependent chain (the next layer's x is
+// this one's y), so one GEMM should stream its weights from every SM it may;
+// measured per chained step (us, half / all SMs): T = 64, 4096 -> 4096,
+// shrink fused: 23.3 / 17.0; layer sweep T = 1: 149.5 / 134.6; T = 8: 170.3 /
+// 165.8.
 // `mode`: 0 base only, 1 U from the shrink kernel (expand on the CUDA cores),
 // 2 shrink fused in, 3 U from the shrink kernel with the expand on the tensor
 // cores (rank 0 of the cluster), 4 the same with the expand's chunks dealt over
 // the cluster.
-SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S) {
+SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S, int cap) {
     SkinnyConfig c;
     const int Tt = T < kSkinnyMaxT ? T : kSkinnyMaxT;
     c.TN = ((Tt + 15) / 16) * 16;
@@ -213,7 +214,6 @@ SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S) {
     const size_t canon_smem = skinny_smem_bytes(c.TN, canon_stages, 8, false, false, false, true, 1);
     const int units = ((N + 127) / 128) * ((T + c.TN - 1) / c.TN);
     const int kb = (K + 63) / 64;
-    const int cap = num_sms();
     c.ks = 1;
     for (int ks = 8; ks >= 2; ks /= 2) {
         if (kb < ks) continue;
@@ -523,6 +523,98 @@ bool pool_overlaps(const Range& prev, const lora_pool* pool, int d_in, int d_out
            overlaps(prev, pool->rank, (size_t)pool->S * 4) || overlaps(prev, pool->scale, (size_t)pool->S * 4);
 }
 
+// How a planned call of these sizes runs its low-rank terms: the expand
+// mode of the decode GEMM and the shrink kernel's units and split. A
+// base-only call with the pool computes the same, so that its GEMM splits K
+// exactly as the planned call's (slot-0 rows then match it bit for bit).
+struct CallShape {
+    bool tc_expand = false, fuse = false, tcl = false;
+    bool by_slot = false, grouped = false;
+    int G = 0, grid_x = 0, shrink_ks = 1;
+    int gemm_cap = 0;       // SMs the decode GEMM's CTAs may take
+};
+
+CallShape call_shape(int T, int d_in, int d_out, const lora_pool* pool, bool sliced, int path, int max_tiles) {
+    CallShape c;
+    c.gemm_cap = num_sms();
+    const int r16 = (pool->R_max + 15) / 16 * 16;
+    // Decode batches of one token tile, with a pool whose adapter slots
+    // (1..S-1, R_max ranks each, rounded up to 16) fit one 128-row tile,
+    // compute U and the expand inside the GEMM (tensor cores: that A tile
+    // against each K slice of x, then Bcat against U): no shrink kernel. The
+    // tokens' slots are read during the K loop by otherwise idle warps.
+    // The expand runs on the tensor cores (Bcat against U) when every adapter
+    // slot's ranks (rounded up to 16) fit 128 pairs; else on the CUDA cores.
+    c.tc_expand = path == 0 && T <= 64 && pool->S >= 2 && (pool->S - 1) * r16 <= 128;
+    // With the shrink fused in, every weight tile re-reads the A tile ((S-1) *
+    // R_max rows of the whole K range) from L2; with the shrink kernel ahead,
+    // A is read once but the call has one more launch. Measured on q_decode
+    // (32 tiles, 33.5 MB of A re-reads) fusing is faster (12.1 against 15.3
+    // us per step); on an LM head of 1002 tiles (1 GB) the shrink kernel is
+    // (198 against 279 us). Sliced calls fuse, for their one launch.
+    const double a_rereads =
+        (double)((d_out + 127) / 128) * ((T + 63) / 64) * (pool->S - 1) * pool->R_max * d_in * 2.0;
+    c.fuse = c.tc_expand && (sliced || a_rereads <= kFuseMaxAReread);
+    // Otherwise, with U from the shrink kernel and more slots than the
+    // rank-0 expand holds, the expand's (slot, 16-rank) chunks are dealt over
+    // the cluster and run on the tensor cores, except for batches of at most
+    // kCoreExpandMaxT rows, whose few (row, token) products the CUDA cores
+    // finish sooner. Measured alone (us per GEMM, tensor / CUDA cores):
+    // T = 256, 14336 -> 4096, ranks 8..64 on 31 slots: 52.4 / 64.1; T = 64,
+    // 4096 -> 4096, 50 rank-16 slots: 26.8 / 30.8; T = 8: 22.7 / 22.6;
+    // T = 1: 22.6 / 20.5.
+    c.tcl = path == 0 && !c.tc_expand && T > kCoreExpandMaxT;
+    if (c.fuse) return c;
+
+    // A unit of the shrink is one adapter slot's rows, or - for decode
+    // batches of pools with R_max <= 16 - the rows of a group of G
+    // consecutive slot ids, whose A rows (R_max each) one TMA box brings in
+    // and one MMA per K step contracts (G R_max <= 256 columns, of which
+    // each row keeps its slot's): a tcgen05 MMA costs about the same for
+    // 16 columns as for 256, and a copy has a fixed cost, so grouping cuts
+    // both by up to G. Prefill batches (many rows per slot) and wider
+    // ranks keep one slot per unit, whose A rows are the slot's own rank.
+    // Small decode batches find their rows in the ids (no plan needed);
+    // larger ones take the plan's segments (groups: its indptr; slots: its
+    // 128-row work tiles).
+    // A group pays for all its slots' A rows, so it is taken only when the
+    // batch has rows enough to name several slots of each group (T at
+    // least 8 per group); on the prefill kernel also only while one slot's
+    // rows do not fill the MMA's 128 (fewer than 32 per slot). Measured
+    // per chained layer sweep step (us, one slot / groups of 16): T = 512:
+    // 432.7 / 404.0 (decode targets only); T = 64: 231.7 / 227.2; T = 8:
+    // 166.6 / 190.0; T = 1: 135.1 / 160.5. On one 4096 -> 4096 layer with 4
+    // adapters of 64 rows (T = 281): 32.7 / 30.1 (rank 16), 32.5 / 29.9
+    // (rank 8).
+    c.by_slot = path == 0 && T <= kBySlotMaxT;
+    int G = 256 / r16;
+    if ((G * pool->R_max) % 16 != 0) G &= ~1;
+    c.grouped = pool->R_max <= 16 && pool->S > 2 && T >= 8 * ((pool->S - 1 + G - 1) / G) &&
+                (path == 0 || T < 32 * (pool->S - 1));
+    c.G = c.grouped ? G : 0;
+    const int n_groups = c.grouped ? (pool->S - 1 + G - 1) / G : pool->S - 1;
+    if (c.by_slot) c.grid_x = n_groups < T ? n_groups : T;
+    else if (c.grouped) c.grid_x = (T + kTileRows - 1) / kTileRows + n_groups +
+                                   (path == 1 ? (T + kTileRows - 1) / kTileRows : 0);   // slot 0's chunks
+    else c.grid_x = max_tiles;
+    c.shrink_ks = shrink_splits(c.grid_x, d_in);
+    // A few rows of several slots (by-slot units of one or two rows each):
+    // each unit's K loop is short, and its CTAs only take SMs from this
+    // call's GEMM, which starts beside it. Measured per chained layer
+    // sweep step at T = 8 (8 units), split 8 / 4 / 2 / 1: 155.2 / 150.1 /
+    // 148.3 / 182.3 us (T = 1 and T = 64 unchanged by the rule).
+    if (c.by_slot && c.grid_x >= 2 && T <= 16 && c.shrink_ks > 2) c.shrink_ks = 2;
+    // The decode GEMM starts its K loop beside the by-slot shrink kernel and
+    // holds one SM per CTA: its K split keeps to the SMs the shrink leaves,
+    // so that no GEMM CTA waits for a shrink CTA to finish. Measured per
+    // chained layer sweep step at T = 64 (32 shrink CTAs; q, o and down
+    // projections then split K over 2 instead of 4): 213.2 -> 200.0 us. The
+    // many CTAs of the plan-tile shrink (T > 64) would leave the GEMM too few
+    // (T = 512: 396.8 -> 455.5 us), so those GEMMs keep every SM.
+    if (c.by_slot) c.gemm_cap = num_sms() - c.grid_x * c.shrink_ks;
+    return c;
+}
+
 // The layer on y rows of pitch ldy (>= d_out). With `slices`, W, y and d_out
 // cover every slice and `pool` is the first slice's; only the decode GEMM
 // with the shrink fused in takes several slices.
@@ -547,34 +639,13 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         for (int q = 0; q < n_sl; ++q)
             pdl = pdl && !pool_overlaps(prev, slices ? slices->pools[q] : pool, d_in, slices ? slices->d_out[q] : d_out);
 
-    // Decode batches of one token tile, with a pool whose adapter slots
-    // (1..S-1, R_max ranks each, rounded up to 16) fit one 128-row tile,
-    // compute U and the expand inside the GEMM (tensor cores: that A tile
-    // against each K slice of x, then Bcat against U): no shrink kernel. The
-    // tokens' slots are read during the K loop by otherwise idle warps.
+    CallShape cs;
+    cs.gemm_cap = num_sms();
+    if (pool) cs = call_shape(T, d_in, d_out, pool, slices != nullptr, path, plan ? plan->max_tiles : 0);
     const int r16 = plan ? (pool->R_max + 15) / 16 * 16 : 0;
-    // The expand runs on the tensor cores (Bcat against U) when every adapter
-    // slot's ranks (rounded up to 16) fit 128 pairs; else on the CUDA cores.
-    const bool tc_expand = plan && path == 0 && T <= 64 && pool->S >= 2 && (pool->S - 1) * r16 <= 128;
-    // With the shrink fused in, every weight tile re-reads the A tile ((S-1) *
-    // R_max rows of the whole K range) from L2; with the shrink kernel ahead,
-    // A is read once but the call has one more launch. Measured on q_decode
-    // (32 tiles, 33.5 MB of A re-reads) fusing is faster (12.1 against 15.3
-    // us per step); on an LM head of 1002 tiles (1 GB) the shrink kernel is
-    // (198 against 279 us). Sliced calls fuse, for their one launch.
-    const double a_rereads = plan ? (double)((d_out + 127) / 128) * ((T + 63) / 64) * (pool->S - 1) * pool->R_max *
-                                        d_in * 2.0
-                                  : 0.0;
-    const bool fuse = tc_expand && (slices || a_rereads <= kFuseMaxAReread);
-    // Otherwise, with U from the shrink kernel and more slots than the
-    // rank-0 expand holds, the expand's (slot, 16-rank) chunks are dealt over
-    // the cluster and run on the tensor cores, except for batches of at most
-    // kCoreExpandMaxT rows, whose few (row, token) products the CUDA cores
-    // finish sooner. Measured alone (us per GEMM, tensor / CUDA cores):
-    // T = 256, 14336 -> 4096, ranks 8..64 on 31 slots: 52.4 / 64.1; T = 64,
-    // 4096 -> 4096, 50 rank-16 slots: 26.8 / 30.8; T = 8: 22.7 / 22.6;
-    // T = 1: 22.6 / 20.5.
-    const bool tcl = plan && path == 0 && !tc_expand && T > kCoreExpandMaxT;
+    const bool tc_expand = plan && cs.tc_expand;
+    const bool fuse = plan && cs.fuse;
+    const bool tcl = plan && cs.tcl;
     if (slices && !fuse) return LORA_EINVAL;                   // callers check this first
     if (plan && !fuse) {
         ShrinkArgs sa;
@@ -592,50 +663,14 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         sa.T = T;
         sa.K = d_in;
         sa.R_max = pool->R_max;
-        // A unit of the shrink is one adapter slot's rows, or - for decode
-        // batches of pools with R_max <= 16 - the rows of a group of G
-        // consecutive slot ids, whose A rows (R_max each) one TMA box brings in
-        // and one MMA per K step contracts (G R_max <= 256 columns, of which
-        // each row keeps its slot's): a tcgen05 MMA costs about the same for
-        // 16 columns as for 256, and a copy has a fixed cost, so grouping cuts
-        // both by up to G. Prefill batches (many rows per slot) and wider
-        // ranks keep one slot per unit, whose A rows are the slot's own rank.
-        // Small decode batches find their rows in the ids (no plan needed);
-        // larger ones take the plan's segments (groups: its indptr; slots: its
-        // 128-row work tiles).
-        // A group pays for all its slots' A rows, so it is taken only when the
-        // batch has rows enough to name several slots of each group (T at
-        // least 8 per group); on the prefill kernel also only while one slot's
-        // rows do not fill the MMA's 128 (fewer than 32 per slot). Measured
-        // per chained layer sweep step (us, one slot / groups of 16): T = 512:
-        // 432.7 / 404.0 (decode targets only); T = 64: 231.7 / 227.2; T = 8:
-        // 166.6 / 190.0; T = 1: 135.1 / 160.5. On one 4096 -> 4096 layer with 4
-        // adapters of 64 rows (T = 281): 32.7 / 30.1 (rank 16), 32.5 / 29.9
-        // (rank 8).
-        const bool by_slot = path == 0 && T <= kBySlotMaxT;
-        int G = 256 / sa.R16;
-        if ((G * pool->R_max) % 16 != 0) G &= ~1;
-        const bool grouped = pool->R_max <= 16 && pool->S > 2 && T >= 8 * ((pool->S - 1 + G - 1) / G) &&
-                             (path == 0 || T < 32 * (pool->S - 1));
-        if (!grouped) G = 0;
-        const int n_groups = grouped ? (pool->S - 1 + G - 1) / G : pool->S - 1;
-        int grid_x;
-        if (by_slot) grid_x = n_groups < T ? n_groups : T;
-        else if (grouped) grid_x = (T + kTileRows - 1) / kTileRows + n_groups +
-                                   (path == 1 ? (T + kTileRows - 1) / kTileRows : 0);   // slot 0's chunks
-        else grid_x = plan->max_tiles;
+        const bool by_slot = cs.by_slot, grouped = cs.grouped;
+        const int G = cs.G, grid_x = cs.grid_x;
         sa.S = pool->S;
         sa.by_slot = by_slot ? 1 : 0;
         sa.G = G;
         sa.indptr = plan->indptr;
         sa.slot_of_token = plan->slot_of_token;
-        sa.ks = shrink_splits(grid_x, d_in);
-        // A few rows of several slots (by-slot units of one or two rows each):
-        // each unit's K loop is short, and its CTAs only take SMs from this
-        // call's GEMM, which starts beside it. Measured per chained layer
-        // sweep step at T = 8 (8 units), split 8 / 4 / 2 / 1: 155.2 / 150.1 /
-        // 148.3 / 182.3 us (T = 1 and T = 64 unchanged by the rule).
-        if (by_slot && grid_x >= 2 && T <= 16 && sa.ks > 2) sa.ks = 2;
+        sa.ks = cs.shrink_ks;
         const int ncol_max = grouped ? G * pool->R_max : sa.R16;
         sa.tmem_cols = 32;
         while (sa.tmem_cols < ncol_max) sa.tmem_cols *= 2;
@@ -681,7 +716,8 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_start, st) != cudaSuccess) return LORA_ECUDA;
     if (path == 0) {
         const int mode = !plan ? 0 : (fuse ? 2 : (tc_expand ? 3 : (tcl ? 4 : 1)));
-        const SkinnyConfig c = skinny_config(T, d_in, d_out, mode, plan ? pool->R_max : 8, plan ? pool->S : 1);
+        const SkinnyConfig c =
+            skinny_config(T, d_in, d_out, mode, plan ? pool->R_max : 8, plan ? pool->S : 1, cs.gemm_cap);
         SkinnyMaps maps;
         CUtensorMap& tmW = maps.w;
         CUtensorMap& tmX = maps.x;
