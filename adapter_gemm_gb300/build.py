@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "lib", "liblora_gb300.so")
 
-SOURCES = ["api.cu", "plan.cu", "shrink.cu", "gemm_skinny.cu", "gemm_wide.cu", "no_alloc.cu"]
+SOURCES = ["api.cu", "plan.cu", "shrink.cu", "gemm_skinny.cu", "gemm_wide.cu", "gemm_wide_pair.cu", "no_alloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I", INCLUDE, "-I", CSRC]

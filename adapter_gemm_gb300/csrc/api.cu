@@ -808,15 +808,28 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // 41.2 us); wide wins at T = 512 with 14336 outputs (65.5 against 69.6
         // us), T = 1500 with 4096 (57.3 against 59.4) and T = 4096 with 1288
         // (55.3 against 57.3). Depends on the shape only.
-        const int m_tiles = (T + 127) / 128;
+        const int m_blocks = (T + 127) / 128;
         const int sms = num_sms();
-        const int t256 = m_tiles * ((d_out + 255) / 256), t128 = m_tiles * ((d_out + 127) / 128);
+        const int t256 = m_blocks * ((d_out + 255) / 256), t128 = m_blocks * ((d_out + 127) / 128);
         const int cost256 = 3 * ((t256 + sms - 1) / sms), cost128 = 2 * ((t128 + sms - 1) / sms);
         const int bn = (t256 < 2 * sms && cost128 < cost256) ? 128 : 256;
         // narrow tiles take two K slices per stage (3-D views; x and the
         // plan-ordered copy of x are [T][d_in], W is [d_out][d_in]), so that a
         // stage's copies are as large as a wide tile's
-        const int kk = (bn == 128 && d_in % 64 == 0 && d_in >= 128) ? 2 : 1;
+        // Long GEMMs (d_in or d_out of 8192 or more) run their wide tiles on
+        // CTA pairs: 256 x 256 tiles, one M = 256 MMA over the two SMs of a
+        // cluster, each CTA streaming 128 rows of x and 128 of W per K slice
+        // (384 rows for the same tensor work unpaired), two K slices per stage
+        // in one copy per operand: fewer TMA copies per MMA, which keeps the
+        // tensor cores fed. Measured alone, T = 4096 (us, unpaired / pairs
+        // with one slice per stage / two): 4096 -> 14336: 299.5 / 287.5 /
+        // 275.4; 14336 -> 4096: 335.5 / 320.5 / 309.1; 4096 -> 4096: 107.6 /
+        // 111.2 / 109.8 (so those stay unpaired).
+        const int max_pairs = (bn == 256 && (d_in >= 8192 || d_out >= 8192)) ? wide_max_pairs() : 0;
+        const bool pair = max_pairs > 0;
+        const int kk = ((bn == 128 || pair) && d_in % 64 == 0 && d_in >= 128) ? 2 : 1;
+        const int m_tiles = pair ? (T + 255) / 256 : m_blocks;
+        const int units = pair ? max_pairs : sms;        // tiles that run at once
         // With a short last wave of wide tiles (at most half the CTAs busy),
         // that wave's tiles are split into 128-column halves, which need W's
         // and B's maps with 128-row boxes too. Measured alone with adapters
@@ -825,24 +838,26 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // -> 4096: 53.2 / 57.3; 2048 x 4096 -> 8192: 102.4 / 106.5.
         const int t_w = m_tiles * ((d_out + bn - 1) / bn);
         int n_wide = t_w, tiles_total = t_w;
-        if (bn == 256 && d_out % 256 == 0 && t_w > sms) {
-            const int r = t_w % sms;
-            if (r > 0 && 2 * r <= sms) {
+        if (bn == 256 && d_out % 256 == 0 && t_w > units) {
+            const int r = t_w % units;
+            if (r > 0 && 2 * r <= units) {
                 n_wide = t_w - r;
                 tiles_total = n_wide + 2 * r;
             }
         }
         const bool halves = tiles_total > n_wide;
+        // weight rows of a tile that one CTA loads (a pair splits them)
+        const uint32_t brows = pair ? (uint32_t)bn / 2 : (uint32_t)bn;
         WideMaps maps;
         if (kk == 1) {
             if (!make_tmap(&maps.a, A, (uint64_t)d_in, (uint64_t)T, 64, 128) ||
-                !make_tmap(&maps.b, W, (uint64_t)d_in, (uint64_t)d_out, 64, (uint32_t)bn) ||
-                (halves && !make_tmap(&maps.b_half, W, (uint64_t)d_in, (uint64_t)d_out, 64, (uint32_t)bn / 2)))
+                !make_tmap(&maps.b, W, (uint64_t)d_in, (uint64_t)d_out, 64, brows) ||
+                (halves && !make_tmap(&maps.b_half, W, (uint64_t)d_in, (uint64_t)d_out, 64, brows / 2)))
                 return LORA_ECUDA;
         } else {
             const uint64_t da[3] = {64, (uint64_t)T, (uint64_t)d_in / 64}, pa[2] = {(uint64_t)d_in * 2, 128};
             const uint64_t db[3] = {64, (uint64_t)d_out, (uint64_t)d_in / 64}, pb[2] = {(uint64_t)d_in * 2, 128};
-            const uint32_t ba[3] = {64, 128, 2}, bbx[3] = {64, (uint32_t)bn, 2}, bbh[3] = {64, (uint32_t)bn / 2, 2};
+            const uint32_t ba[3] = {64, 128, 2}, bbx[3] = {64, brows, 2}, bbh[3] = {64, brows / 2, 2};
             if (!make_tmap_nd(&maps.a, A, 3, da, pa, ba, CU_TENSOR_MAP_SWIZZLE_128B) ||
                 !make_tmap_nd(&maps.b, W, 3, db, pb, bbx, CU_TENSOR_MAP_SWIZZLE_128B) ||
                 (halves && !make_tmap_nd(&maps.b_half, W, 3, db, pb, bbh, CU_TENSOR_MAP_SWIZZLE_128B)))
@@ -856,7 +871,7 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
             const uint32_t bu[2] = {16, 128};
             const uint64_t db[3] = {(uint64_t)pool->R_max, (uint64_t)d_out, (uint64_t)pool->S};
             const uint64_t pb[2] = {(uint64_t)pool->R_max * 2, (uint64_t)d_out * pool->R_max * 2};
-            const uint32_t bb[3] = {16, (uint32_t)bn, 1}, bbh[3] = {16, (uint32_t)bn / 2, 1};
+            const uint32_t bb[3] = {16, brows, 1}, bbh[3] = {16, brows / 2, 1};
             if (!make_tmap_nd(&maps.u, plan->U_hl, 2, du, pu, bu, CU_TENSOR_MAP_SWIZZLE_32B) ||
                 !make_tmap_nd(&maps.bs, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B) ||
                 (halves && !make_tmap_nd(&maps.bs_half, pool->B, 3, db, pb, bbh, CU_TENSOR_MAP_SWIZZLE_32B)))
@@ -880,13 +895,15 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         a.K = d_in;
         a.N = d_out;
         a.m_tiles = m_tiles;
+        a.m_blocks = m_blocks;
+        a.pair = pair ? 1 : 0;
         a.bn = bn;
         a.kk = kk;
         a.kb_total = (d_in + 63) / 64;
         a.n_wide = n_wide;
         a.tiles_total = tiles_total;
-        int grid = tiles_total;
-        if (grid > sms) grid = sms;
+        int grid = tiles_total < units ? tiles_total : units;
+        if (pair) grid *= 2;
         if (counted(launch_wide(maps, a, pdl, grid, st)) != cudaSuccess) return LORA_ECUDA;
     }
     if (g_prof_start && g_prof_stop && cudaEventRecord(g_prof_stop, st) != cudaSuccess) return LORA_ECUDA;
@@ -1024,11 +1041,11 @@ lora_status lora_profile_gemm_events(void* start, void* stop) {
 
 lora_status lora_last_device_error(int32_t* code_out) {
     if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ECUDA;
-    int a = 0, b = 0, c = 0;
+    int a = 0, b = 0, c = 0, d = 0;
     if (skinny_take_error(&a) != cudaSuccess || wide_take_error(&b) != cudaSuccess ||
-        shrink_take_error(&c) != cudaSuccess)
+        shrink_take_error(&c) != cudaSuccess || wide_pair_take_error(&d) != cudaSuccess)
         return LORA_ECUDA;
-    const int v = a ? a : (b ? b : c);
+    const int v = a ? a : (b ? b : (c ? c : d));
     if (code_out) *code_out = v;
     return v ? LORA_ETIMEOUT : LORA_OK;
 }

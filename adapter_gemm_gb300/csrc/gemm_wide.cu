@@ -370,6 +370,7 @@ static cudaError_t launch_wide_bn(const WideMaps& maps, const WideArgs& a, bool 
 }
 
 cudaError_t launch_wide(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream) {
+    if (a.pair) return launch_wide_pair(maps, a, pdl, grid, stream);
     if (a.kk == 2)
         return a.bn == 128 ? launch_wide_bn<128, 2>(maps, a, pdl, grid, stream)
                            : launch_wide_bn<256, 2>(maps, a, pdl, grid, stream);

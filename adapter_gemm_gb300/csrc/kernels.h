@@ -122,8 +122,10 @@ struct WideArgs {
     const int32_t* rank;            // [S]
     int R_max, R16;
     int T, K, N;
-    int m_tiles, kb_total;          // 128-row blocks of T; 64-column K slices
+    int m_tiles, kb_total;          // row blocks of the tiles (128 rows, 256 with pairs); 64-column K slices
+    int m_blocks;                   // 128-row blocks of T (entries of mt_ptr, less one)
     int bn;                         // output tile width: 256 or 128
+    int pair;                       // tiles of 256 rows shared by the two CTAs of a cluster
     int kk;                         // 64-column K slices per stage: 1 or 2 (3-D tensor maps)
     int n_wide;                     // tiles 0..n_wide-1 are bn wide, in (m, strip) order;
     int tiles_total;                //   the rest split the following (m, strip) pairs in halves
@@ -142,6 +144,10 @@ cudaError_t launch_shrink(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_
 int shrink_kk(int xrows, int R16, int K);
 cudaError_t launch_skinny(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream);
 cudaError_t launch_wide(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
+// The prefill GEMM on CTA pairs (a.pair; grid = 2 x pairs, clusters of 2), and
+// how many pairs can be resident at once.
+cudaError_t launch_wide_pair(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
+int wide_max_pairs();
 cudaError_t launch_count_nonfinite(const __nv_bfloat16* p, size_t n, int32_t* out, cudaStream_t stream);
 cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* rows, int T, int T_all, int d_in,
                                __nv_bfloat16* out, cudaStream_t stream);
@@ -150,12 +156,13 @@ cudaError_t launch_gather_rows(const __nv_bfloat16* x, const int32_t* rows, int 
 cudaError_t skinny_take_error(int* code);
 cudaError_t wide_take_error(int* code);
 cudaError_t shrink_take_error(int* code);
+cudaError_t wide_pair_take_error(int* code);
 
 // Raise a kernel's dynamic shared memory limit once per device.
 // One slot per kernel (instantiation) whose dynamic shared memory limit is
 // raised: 0 plan, 1 swap-AB decode, 2..5 wide (tile width x K slices), 6..8
 // shrink (cp.async depth).
-constexpr int kSmemSlots = 18;
+constexpr int kSmemSlots = 20;
 cudaError_t ensure_smem_attr(const void* func, int slot, size_t bytes);
 
 // Shared-memory bytes the skinny kernel needs for a token tile of TN columns

@@ -277,6 +277,84 @@ __device__ __forceinline__ void tc_mma_bf16_masked(uint32_t d_tmem, uint64_t a_d
            "r"(disable[0]), "r"(disable[1]), "r"(disable[2]), "r"(disable[3]), "r"(1u) : "memory");
 }
 
+// ------------------------------------------------------------ CTA pairs ---
+// A CTA pair (the two CTAs of a cluster of 2) shares one tensor-core MMA of
+// M = 256: CTA rank r holds rows [128 r, 128 r + 128) of A and half of B's N
+// rows in its shared memory (same offsets in both), and rows 128 r.. of D in
+// its tensor memory. Rank 0 issues the MMAs. Every tcgen05 instruction of a
+// kernel that uses pairs takes .cta_group::2.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Both CTAs of the pair call these (one warp each).
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+                 :: "r"(taddr), "r"(ncols) : "memory");
+}
+// Tiled loads into this CTA's shared memory that complete on `bar`, which may
+// be the pair leader's barrier (a shared::cluster address from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
+                                                 int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3}], [%4];"
+        :: "r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, uint32_t bar, int32_t c0,
+                                                 int32_t c1, int32_t c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        :: "r"(dst), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar) : "memory");
+}
+// D (+)= A B^T over the pair, M = 256.
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// D += A B^T over the pair for the rows whose bit in `disable` is clear (8 x
+// 32 bits: row 32 w + i of the pair's 256 <-> bit i of word w).
+__device__ __forceinline__ void tc_mma_bf16_pair_masked(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                        uint32_t idesc, const uint32_t (&disable)[8]) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %12, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, {%4, %5, %6, %7, %8, %9, %10, %11}, p;\n\t}"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(disable[0]), "r"(disable[1]), "r"(disable[2]),
+           "r"(disable[3]), "r"(disable[4]), "r"(disable[5]), "r"(disable[6]), "r"(disable[7]), "r"(1u)
+        : "memory");
+}
+// Arrive once on the barrier at this offset in each CTA of `mask` when every
+// MMA issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        :: "r"(bar), "h"(mask) : "memory");
+}
+// Arrive on a barrier of another CTA of the cluster (a shared::cluster
+// address from mapa), releasing this thread's earlier accesses.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+// A full cluster barrier (every thread of every CTA), ordering the memory
+// accesses before it with those after it.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Arrive once on the barrier when every MMA issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"

@@ -70,12 +70,6 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
-// Full cluster barrier (every thread of every CTA), ordering the shared-memory
-// accesses before it with those after it.
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Store U[row i of the unit, col] = v (already scaled): fp32 by token into U
 // [T][R_max], or (wide GEMM) a bf16 high part and a bf16 low part (v - high)
 // by plan position into U_hl [T][2 * R16].
