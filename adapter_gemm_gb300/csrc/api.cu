@@ -824,8 +824,12 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         // tensor cores fed. Measured alone, T = 4096 (us, unpaired / pairs
         // with one slice per stage / two): 4096 -> 14336: 299.5 / 287.5 /
         // 275.4; 14336 -> 4096: 335.5 / 320.5 / 309.1; 4096 -> 4096: 107.6 /
-        // 111.2 / 109.8 (so those stay unpaired).
-        const int max_pairs = (bn == 256 && (d_in >= 8192 || d_out >= 8192)) ? wide_max_pairs() : 0;
+        // 111.2 / 109.8 (so those stay unpaired). A 256-row tile crosses twice
+        // the adapter segments of a 128-row one, each with its own B_s copies,
+        // so batches with few rows per adapter (T below 2048) stay unpaired:
+        // the layer sweep at T = 512 measured 433.7 us per step paired.
+        const int max_pairs =
+            (bn == 256 && T >= 2048 && (d_in >= 8192 || d_out >= 8192)) ? wide_max_pairs() : 0;
         const bool pair = max_pairs > 0;
         const int kk = ((bn == 128 || pair) && d_in % 64 == 0 && d_in >= 128) ? 2 : 1;
         const int m_tiles = pair ? (T + 255) / 256 : m_blocks;
