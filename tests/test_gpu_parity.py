@@ -129,7 +129,8 @@ def test_slot0_rows_bitwise_equal_base_only(name):
 
 # --------------------------------------------------------- exact integers ----
 
-@pytest.mark.parametrize("T,K,N,R", [(9, 16, 24, 8), (64, 64, 136, 8), (300, 64, 264, 8), (513, 32, 520, 16)])
+@pytest.mark.parametrize("T,K,N,R", [(9, 16, 24, 8), (64, 64, 136, 8), (300, 64, 264, 8), (513, 32, 520, 16),
+                                     (2049, 64, 8704, 16)])    # CTA pairs, a last row block of one row
 def test_integer_inputs_bit_exact(T, K, N, R):
     """Small-integer inputs with power-of-two scales: every partial sum is exact
     in fp32 and every output is an integer of magnitude <= 256, so the GPU must
@@ -180,6 +181,26 @@ def test_ragged_shapes(T, K, N, S, R):
     y = dw.run(0)
     rows = np.arange(T) if T <= 400 else sample_rows(w.ids, 200)
     assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(0, rows=rows), f"ragged {T},{K},{N}")
+    slot0 = torch.as_tensor(w.ids == 0, device=DEV)
+    yb = dw.run(0, base_only=True)
+    assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
+
+
+# Long projections (d_in or d_out of 8192 or more) of batches of 2048 rows or
+# more run the prefill GEMM on CTA pairs (256-row tiles, one M = 256 MMA over
+# the two CTAs of a cluster). The cases: the long side in d_in and in d_out; a
+# last row block whose second half lies wholly past T (2100 = 8 x 256 + 52) or
+# partly (2300); a last wave split into 256 x 128 halves (153 and 306 tiles on
+# 76 pairs); slot-0 rows bit for bit against base-only calls, which take the
+# same kernel.
+@pytest.mark.parametrize("T,K,N,S,R", [(2100, 8192, 4352, 17, 32), (2300, 2048, 8704, 30, 16)])
+def test_pair_prefill_ragged(T, K, N, S, R):
+    assert L.linear_path(T, K, N) == 1
+    w = WL.random_case(seed=T + K + N, T=T, K=K, N=N, S=S, R_max=R, base_frac=0.15)
+    dw = DeviceWorkload(w, DEV)
+    y = dw.run(0)
+    rows = np.unique(np.concatenate([sample_rows(w.ids, 160), np.arange(T - 64, T), np.arange(2040, 2060)]))
+    assert_parity(y[torch.as_tensor(rows, device=DEV)], dw.oracle(0, rows=rows), f"pairs T={T} {K}->{N}")
     slot0 = torch.as_tensor(w.ids == 0, device=DEV)
     yb = dw.run(0, base_only=True)
     assert torch.equal(y[slot0].view(torch.int16), yb[slot0].view(torch.int16))
