@@ -214,7 +214,9 @@ lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* 
 
 /* The kernel family lora_linear picks for these sizes on the current device
  * without a pool: 0 = skinny (swap-AB, split-K across a thread-block
- * cluster), 1 = wide (persistent 128x256 tiles). Up to 256 rows always 0,
+ * cluster), 1 = wide (persistent 128x256 tiles; for 2048 rows or more with
+ * d_in or d_out of 8192 or more, 256x256 tiles shared by the two CTAs of a
+ * cluster). Up to 256 rows always 0,
  * above 640 always 1; in between 0 while the skinny kernel's weight tiles can
  * split K in two on every SM. */
 int lora_linear_path(int T, int d_in, int d_out);
