@@ -875,7 +875,10 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
             const uint32_t bu[2] = {16, 128};
             const uint64_t db[3] = {(uint64_t)pool->R_max, (uint64_t)d_out, (uint64_t)pool->S};
             const uint64_t pb[2] = {(uint64_t)pool->R_max * 2, (uint64_t)d_out * pool->R_max * 2};
-            const uint32_t bb[3] = {16, brows, 1}, bbh[3] = {16, brows / 2, 1};
+            // an expand stage's B_s copy: 16 ranks of the tile's weight rows
+            // for wide_xslots consecutive slots
+            const uint32_t xs = (uint32_t)wide_xslots((uint32_t)kk * (16384u + brows * 128u), brows * 32u);
+            const uint32_t bb[3] = {16, brows, xs}, bbh[3] = {16, brows / 2, xs};
             if (!make_tmap_nd(&maps.u, plan->U_hl, 2, du, pu, bu, CU_TENSOR_MAP_SWIZZLE_32B) ||
                 !make_tmap_nd(&maps.bs, pool->B, 3, db, pb, bb, CU_TENSOR_MAP_SWIZZLE_32B) ||
                 (halves && !make_tmap_nd(&maps.bs_half, pool->B, 3, db, pb, bbh, CU_TENSOR_MAP_SWIZZLE_32B)))

@@ -26,7 +26,8 @@
 // and the expand operands (U 128 x 16 hi and lo, B_s 256 x 16, 32-byte
 // swizzle), with TMA into a 4-stage ring; warp 1 lane 0 issues tcgen05.mma
 // (M=128, N=256, K=16) into one of two 256-column TMEM accumulators; warp 2
-// owns the 512-column TMEM allocation; warps 4..7 drain the other accumulator
+// owns the 512-column TMEM allocation; warp 3 lane 0 builds the tiles' expand
+// lists ahead of them; warps 4..7 drain the other accumulator
 // (warp w reads TMEM lanes 32(w-4)..), round and store, while the next tile's
 // MMAs run.
 #include <cstdint>
@@ -53,10 +54,10 @@ struct WideCfg {
     static constexpr uint32_t kSliceBytes = kWdABytes + kBBytes;
     static constexpr uint32_t kStageBytes = KK * kSliceBytes;
     static constexpr int kStages = (int)((192u * 1024u) / kStageBytes) > 6 ? 6 : (int)((192u * 1024u) / kStageBytes);
-    static constexpr uint32_t kXbBytes = BN * 16 * 2;              // expand step: B_s tile
-    // B_s tiles per expand stage, next to the U tiles (hi, lo)
-    static constexpr int kXPer = (int)((kStageBytes - 2 * kXuBytes) / kXbBytes) > 16
-                                     ? 16 : (int)((kStageBytes - 2 * kXuBytes) / kXbBytes);
+    static constexpr uint32_t kXbBytes = BN * 16 * 2;              // expand step: B_s tile of a slot
+    // consecutive slots' B_s tiles per expand stage (one copy), next to the U
+    // tiles (hi, lo)
+    static constexpr int kXPer = wide_xslots(kStageBytes, kXbBytes);
     static constexpr uint32_t kTmemCols = 2 * BN;                  // two accumulators
     // ring | barriers (256 B) | two expand lists of kMaxSegs int4 + counts
     static constexpr size_t kSmem = 1024 + (size_t)kStageBytes * kStages + 256 + 2 * (size_t)kMaxSegs * 16 + 16;
@@ -88,7 +89,6 @@ gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
     constexpr int kWdBN = BN;
     constexpr int kWdStages = C::kStages;
     constexpr uint32_t kWdStageBytes = C::kStageBytes;
-    constexpr uint32_t kXbBytes = C::kXbBytes;
     constexpr int kXPer = C::kXPer;
     const int n_kst = (a.kb_total + KK - 1) / KK;      // K stages per tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -124,7 +124,7 @@ gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
             mbar_init(smem_u32(&tfull[i]), 1);
             mbar_init(smem_u32(&tempty[i]), 128);
             mbar_init(smem_u32(&lfull[i]), 1);
-            mbar_init(smem_u32(&lempty[i]), 1);
+            mbar_init(smem_u32(&lempty[i]), 2);      // the producer and the MMA thread
         }
         fence_mbar_init();
     }
@@ -169,47 +169,37 @@ gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
                     ++issued;
                 }
                 if (!expand || !ok) continue;
-                // The tile's expand list: adapter segments crossing rows
-                // [m0, m0 + 128) with a nonzero rank, and 16-rank steps each.
+                // The tile's expand list (built by warp 3).
                 const int as = lt & 1;
                 const uint32_t use = (uint32_t)(lt >> 1);
-                if (!mbar_wait(smem_u32(&lempty[as]), (use & 1u) ^ 1u, kErrEmptyWait)) { ok = false; break; }
-                const int e0 = a.mt_ptr[mt], e1 = a.mt_ptr[mt + 1];
-                int ns = 0;
-                for (int e = e0; e < e1 && ns < kMaxSegs; ++e) {
-                    const int4 sg = a.mt_seg[e];
-                    const int r = min(a.rank[sg.x], a.R_max);
-                    if (r > 0) xlist[as * kMaxSegs + ns++] = make_int4(sg.x, sg.y, sg.z, (r + 15) >> 4);
-                }
-                xcount[as] = ns;
-                mbar_arrive(smem_u32(&lfull[as]));
+                if (!mbar_wait(smem_u32(&lfull[as]), use & 1u, kErrFullWait)) { ok = false; break; }
+                const int ns = xcount[as];
                 // Expand stages: per 16-rank step, the tile's U rows (hi and
-                // lo, shared by every segment) and the B_s tiles of up to
-                // kXPer segments that reach that step.
+                // lo, shared by every segment) and, in one copy, the B_s
+                // tiles of kXPer consecutive slots from the first segment's
+                // (expand_window): a copy has a fixed cost, and a tile's
+                // segments are mostly consecutive slots.
                 int maxw = 0;
                 for (int q = 0; q < ns; ++q) maxw = max(maxw, xlist[as * kMaxSegs + q].w);
+                const int4* lst = xlist + as * kMaxSegs;
                 for (int ks = 0; ks < maxw && ok; ++ks) {
-                    for (int q0 = 0; q0 < ns && ok;) {
-                        int sel[kXPer], n_sel = 0, q = q0;
-                        for (; q < ns && n_sel < kXPer; ++q)
-                            if (xlist[as * kMaxSegs + q].w > ks) sel[n_sel++] = q;
-                        q0 = q;
-                        if (n_sel == 0) continue;
+                    int q0 = 0, q_end = 0, first = 0;
+                    while (ok && expand_window(lst, ns, ks, kXPer, q0, q_end, first)) {
                         const int st = it % kWdStages;
                         const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                         if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
                         const uint32_t sU = smem_u32(base + (size_t)st * kWdStageBytes);
                         const uint32_t fb = smem_u32(&full[st]);
-                        mbar_arrive_expect_tx(fb, 2 * kXuBytes + (uint32_t)n_sel * (uint32_t)wd * 32u);
+                        mbar_arrive_expect_tx(fb, 2 * kXuBytes + (uint32_t)kXPer * (uint32_t)wd * 32u);
                         tma_load_2d(sU, &tmU, fb, ks * 16, m0);                       // U hi
                         tma_load_2d(sU + kXuBytes, &tmU, fb, a.R16 + ks * 16, m0);    // U lo
-                        for (int j = 0; j < n_sel; ++j)                                // B_s
-                            tma_load_3d(sU + 2 * kXuBytes + (uint32_t)j * kXbBytes, tmBs, fb, ks * 16, n0,
-                                        xlist[as * kMaxSegs + sel[j]].x);
+                        tma_load_3d(sU + 2 * kXuBytes, tmBs, fb, ks * 16, n0, first);  // B_s of kXPer slots
                         ++issued;
                         ++it;
+                        q0 = q_end;
                     }
                 }
+                mbar_arrive(smem_u32(&lempty[as]));
             }
             // Let every copy this thread started land before the CTA can exit.
             for (int i = max(0, issued - kWdStages); i < issued; ++i)
@@ -257,22 +247,20 @@ gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
                     const int ns = xcount[as];
                     int maxw = 0;
                     for (int q = 0; q < ns; ++q) maxw = max(maxw, xlist[as * kMaxSegs + q].w);
-                    // the same stages as the producer: per rank step, groups
-                    // of up to kXPer segments that reach it
+                    // the same stages as the producer (expand_window)
+                    const int4* lst = xlist + as * kMaxSegs;
+                    const uint32_t xbt = (uint32_t)wd * 32u;                   // one slot's B_s tile
                     for (int ks = 0; ks < maxw && ok; ++ks) {
-                        for (int q0 = 0; q0 < ns && ok;) {
-                            int sel[kXPer], n_sel = 0, q = q0;
-                            for (; q < ns && n_sel < kXPer; ++q)
-                                if (xlist[as * kMaxSegs + q].w > ks) sel[n_sel++] = q;
-                            q0 = q;
-                            if (n_sel == 0) continue;
+                        int q0 = 0, q_end = 0, first = 0;
+                        while (ok && expand_window(lst, ns, ks, kXPer, q0, q_end, first)) {
                             const int st = it % kWdStages;
                             const uint32_t ph = (uint32_t)(it / kWdStages) & 1u;
                             if (!mbar_wait(smem_u32(&full[st]), ph, kErrFullWait)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t sU = smem_u32(base + (size_t)st * kWdStageBytes);
-                            for (int j = 0; j < n_sel; ++j) {
-                                const int4 sg = xlist[as * kMaxSegs + sel[j]];
+                            for (int q = q0; q < q_end; ++q) {
+                                const int4 sg = lst[q];
+                                if (sg.w <= ks) continue;           // this segment's rank ends below step ks
                                 // lanes (rows) outside [sg.y, sg.z) keep their value
                                 uint32_t dis[4];
 #pragma unroll
@@ -283,17 +271,47 @@ gemm_wide_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
                                                                         : (((1u << (hi - lo)) - 1u) << (lo - 32 * w)));
                                     dis[w] = ~on;
                                 }
-                                const uint64_t bdesc = sdesc_sw32(sU + 2 * kXuBytes + (uint32_t)j * kXbBytes);
+                                const uint64_t bdesc =
+                                    sdesc_sw32(sU + 2 * kXuBytes + (uint32_t)(sg.x - first) * xbt);
                                 tc_mma_bf16_masked(d, sdesc_sw32(sU), bdesc, idesc, dis);
                                 tc_mma_bf16_masked(d, sdesc_sw32(sU + kXuBytes), bdesc, idesc, dis);
                             }
                             tc_commit(smem_u32(&empty[st]));
                             ++it;
+                            q0 = q_end;
                         }
                     }
                     mbar_arrive(smem_u32(&lempty[as]));
                 }
                 tc_commit(smem_u32(&tfull[as]));
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        if (lane == 0 && expand) {
+            // The tiles' expand lists, ahead of the producer and the MMA
+            // thread that read them (two buffers): the adapter segments
+            // crossing the tile's rows [m0, m0 + 128) with a nonzero rank, and
+            // 16-rank steps each. Their global loads, one dependent on the
+            // other, would otherwise stall the producer once per tile.
+            int lt = 0;
+            for (int tile = blockIdx.x; tile < n_tiles_total; tile += gridDim.x, ++lt) {
+                int mt, n0_unused, wd_unused;
+                wide_tile<BN>(a, tile, mt, n0_unused, wd_unused);
+                (void)n0_unused;
+                (void)wd_unused;
+                const int as = lt & 1;
+                const uint32_t use = (uint32_t)(lt >> 1);
+                if (!mbar_wait(smem_u32(&lempty[as]), (use & 1u) ^ 1u, kErrEmptyWait)) break;
+                const int e0 = a.mt_ptr[mt], e1 = a.mt_ptr[mt + 1];
+                int ns = 0;
+                for (int e = e0; e < e1 && ns < kMaxSegs; ++e) {
+                    const int4 sg = a.mt_seg[e];
+                    const int r = min(a.rank[sg.x], a.R_max);
+                    if (r > 0) xlist[as * kMaxSegs + ns++] = make_int4(sg.x, sg.y, sg.z, (r + 15) >> 4);
+                }
+                xcount[as] = ns;
+                mbar_arrive(smem_u32(&lfull[as]));
             }
         }
         __syncwarp();

@@ -40,9 +40,9 @@ struct PairCfg {
     static constexpr uint32_t kBBytes = (kPrBN / 2) * kPrBK * 2;   // this CTA's weight slice, 16 KB
     static constexpr uint32_t kStageBytes = KK * (kPrABytes + kBBytes);
     static constexpr int kStages = (int)((192u * 1024u) / kStageBytes) > 6 ? 6 : (int)((192u * 1024u) / kStageBytes);
-    static constexpr uint32_t kXbBytes = (kPrBN / 2) * 16 * 2;     // expand step: this CTA's B_s tile
-    static constexpr int kXPer = (int)((kStageBytes - 2 * kPrXuBytes) / kXbBytes) > 16
-                                     ? 16 : (int)((kStageBytes - 2 * kPrXuBytes) / kXbBytes);
+    static constexpr uint32_t kXbBytes = (kPrBN / 2) * 16 * 2;     // expand step: this CTA's B_s tile of a slot
+    // consecutive slots' B_s tiles per expand stage (one copy)
+    static constexpr int kXPer = wide_xslots(kStageBytes, kXbBytes);
     static constexpr uint32_t kTmemCols = 2 * kPrBN;               // two accumulators
     // ring | barriers (256 B) | two expand lists of kPrSegs int4 + counts
     static constexpr size_t kSmem = 1024 + (size_t)kStageBytes * kStages + 256 + 2 * (size_t)kPrSegs * 16 + 16;
@@ -71,7 +71,6 @@ gemm_wide_pair_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
     using C = PairCfg<KK>;
     constexpr int kStages = C::kStages;
     constexpr uint32_t kStageBytes = C::kStageBytes;
-    constexpr uint32_t kXbBytes = C::kXbBytes;
     constexpr int kXPer = C::kXPer;
     const CUtensorMap& tmA = maps.a;
     const CUtensorMap& tmU = maps.u;
@@ -112,7 +111,7 @@ gemm_wide_pair_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
             mbar_init(smem_u32(&tfull[i]), 1);
             mbar_init(smem_u32(&tempty[i]), 2 * 128);
             mbar_init(smem_u32(&lfull[i]), 1);
-            mbar_init(smem_u32(&lempty[i]), 1);
+            mbar_init(smem_u32(&lempty[i]), leader ? 2 : 1);   // the producer (and the leader's MMA thread)
         }
         fence_mbar_init();
     }
@@ -161,56 +160,38 @@ gemm_wide_pair_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
                     ++issued;
                 }
                 if (!expand || !ok) continue;
-                // The tile's expand list: adapter segments crossing its two
-                // 128-row blocks with a nonzero rank (rows relative to the
-                // tile), and 16-rank steps each. Both CTAs build it (each
-                // loads its halves of the same stages); the leader's MMA thread
-                // reads the leader's.
+                // The tile's expand list (built by warp 3 of each CTA, which
+                // loads its halves of the same stages; the leader's MMA thread
+                // reads the leader's).
                 const int as = lt & 1;
                 const uint32_t use = (uint32_t)(lt >> 1);
-                if (leader && !mbar_wait(smem_u32(&lempty[as]), (use & 1u) ^ 1u, kErrEmptyWait)) { ok = false; break; }
-                int ns = 0;
-                for (int hb = 0; hb < 2; ++hb) {
-                    const int m = 2 * mt + hb;
-                    if (m >= a.m_blocks) break;
-                    const int e0 = a.mt_ptr[m], e1 = a.mt_ptr[m + 1];
-                    for (int e = e0; e < e1 && ns < kPrSegs; ++e) {
-                        const int4 sg = a.mt_seg[e];
-                        const int r = min(a.rank[sg.x], a.R_max);
-                        if (r > 0)
-                            xlist[as * kPrSegs + ns++] =
-                                make_int4(sg.x, sg.y + kPrBM * hb, sg.z + kPrBM * hb, (r + 15) >> 4);
-                    }
-                }
-                xcount[as] = ns;
-                if (leader) mbar_arrive(smem_u32(&lfull[as]));
+                if (!mbar_wait(smem_u32(&lfull[as]), use & 1u, kErrFullWait)) { ok = false; break; }
+                const int ns = xcount[as];
                 // Expand stages: per 16-rank step, the tile's U rows (hi and
-                // lo, shared by every segment) and the B_s tiles of up to
-                // kXPer segments that reach that step.
+                // lo, shared by every segment) and, in one copy, this CTA's
+                // B_s tiles of kXPer consecutive slots from the first
+                // segment's (expand_window).
                 int maxw = 0;
                 for (int q = 0; q < ns; ++q) maxw = max(maxw, xlist[as * kPrSegs + q].w);
+                const int4* lst = xlist + as * kPrSegs;
                 for (int ks = 0; ks < maxw && ok; ++ks) {
-                    for (int q0 = 0; q0 < ns && ok;) {
-                        int sel[kXPer], n_sel = 0, q = q0;
-                        for (; q < ns && n_sel < kXPer; ++q)
-                            if (xlist[as * kPrSegs + q].w > ks) sel[n_sel++] = q;
-                        q0 = q;
-                        if (n_sel == 0) continue;
+                    int q0 = 0, q_end = 0, first = 0;
+                    while (ok && expand_window(lst, ns, ks, kXPer, q0, q_end, first)) {
                         const int st = it % kStages;
                         const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                         if (!mbar_wait(smem_u32(&empty[st]), ph ^ 1u, kErrEmptyWait)) { ok = false; break; }
                         const uint32_t sU = smem_u32(base + (size_t)st * kStageBytes);
                         const uint32_t fl = smem_u32(&full[st]), fb = mapa_shared(fl, 0);
-                        if (leader) mbar_arrive_expect_tx(fl, 2 * (2 * kPrXuBytes + (uint32_t)n_sel * (uint32_t)brows * 32u));
+                        if (leader) mbar_arrive_expect_tx(fl, 2 * (2 * kPrXuBytes + (uint32_t)kXPer * (uint32_t)brows * 32u));
                         tma_load_2d_pair(sU, &tmU, fb, ks * 16, m_cta);                       // U hi
                         tma_load_2d_pair(sU + kPrXuBytes, &tmU, fb, a.R16 + ks * 16, m_cta);  // U lo
-                        for (int j = 0; j < n_sel; ++j)                                        // B_s
-                            tma_load_3d_pair(sU + 2 * kPrXuBytes + (uint32_t)j * kXbBytes, tmBs, fb, ks * 16, n_cta,
-                                             xlist[as * kPrSegs + sel[j]].x);
+                        tma_load_3d_pair(sU + 2 * kPrXuBytes, tmBs, fb, ks * 16, n_cta, first);  // B_s of kXPer slots
                         ++issued;
                         ++it;
+                        q0 = q_end;
                     }
                 }
+                mbar_arrive(smem_u32(&lempty[as]));
             }
             // Let every copy land before the CTAs can exit: the leader's
             // barriers count both CTAs' copies, and the peer leaves only after
@@ -261,22 +242,20 @@ gemm_wide_pair_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
                     const int ns = xcount[as];
                     int maxw = 0;
                     for (int q = 0; q < ns; ++q) maxw = max(maxw, xlist[as * kPrSegs + q].w);
-                    // the same stages as the producers: per rank step, groups
-                    // of up to kXPer segments that reach it
+                    // the same stages as the producers (expand_window)
+                    const int4* lst = xlist + as * kPrSegs;
+                    const uint32_t xbt = (uint32_t)(wd / 2) * 32u;             // one slot's B_s tile in each CTA
                     for (int ks = 0; ks < maxw && ok; ++ks) {
-                        for (int q0 = 0; q0 < ns && ok;) {
-                            int sel[kXPer], n_sel = 0, q = q0;
-                            for (; q < ns && n_sel < kXPer; ++q)
-                                if (xlist[as * kPrSegs + q].w > ks) sel[n_sel++] = q;
-                            q0 = q;
-                            if (n_sel == 0) continue;
+                        int q0 = 0, q_end = 0, first = 0;
+                        while (ok && expand_window(lst, ns, ks, kXPer, q0, q_end, first)) {
                             const int st = it % kStages;
                             const uint32_t ph = (uint32_t)(it / kStages) & 1u;
                             if (!mbar_wait(smem_u32(&full[st]), ph, kErrFullWait)) { ok = false; break; }
                             tc_fence_after();
                             const uint32_t sU = smem_u32(base + (size_t)st * kStageBytes);
-                            for (int j = 0; j < n_sel; ++j) {
-                                const int4 sg = xlist[as * kPrSegs + sel[j]];
+                            for (int q = q0; q < q_end; ++q) {
+                                const int4 sg = lst[q];
+                                if (sg.w <= ks) continue;           // this segment's rank ends below step ks
                                 // rows of the pair's 256 outside [sg.y, sg.z) keep their value
                                 uint32_t dis[8];
 #pragma unroll
@@ -287,17 +266,53 @@ gemm_wide_pair_kernel(const __grid_constant__ WideMaps maps, WideArgs a) {
                                                                         : (((1u << (hi - lo)) - 1u) << (lo - 32 * w)));
                                     dis[w] = ~on;
                                 }
-                                const uint64_t bdesc = sdesc_sw32(sU + 2 * kPrXuBytes + (uint32_t)j * kXbBytes);
+                                const uint64_t bdesc =
+                                    sdesc_sw32(sU + 2 * kPrXuBytes + (uint32_t)(sg.x - first) * xbt);
                                 tc_mma_bf16_pair_masked(d, sdesc_sw32(sU), bdesc, idesc, dis);
                                 tc_mma_bf16_pair_masked(d, sdesc_sw32(sU + kPrXuBytes), bdesc, idesc, dis);
                             }
                             tc_commit_pair(smem_u32(&empty[st]), (uint16_t)3);
                             ++it;
+                            q0 = q_end;
                         }
                     }
                     mbar_arrive(smem_u32(&lempty[as]));
                 }
                 tc_commit_pair(smem_u32(&tfull[as]), (uint16_t)3);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        if (lane == 0 && expand) {
+            // The tiles' expand lists, ahead of their readers (two buffers):
+            // the adapter segments crossing the tile's two 128-row blocks
+            // with a nonzero rank (rows relative to the tile, slot order),
+            // and 16-rank steps each. Their dependent global loads would
+            // otherwise stall the producer once per tile.
+            int lt = 0;
+            for (int tile = unit; tile < n_tiles_total; tile += n_units, ++lt) {
+                int mt, n0_unused, wd_unused;
+                pair_tile(a, tile, mt, n0_unused, wd_unused);
+                (void)n0_unused;
+                (void)wd_unused;
+                const int as = lt & 1;
+                const uint32_t use = (uint32_t)(lt >> 1);
+                if (!mbar_wait(smem_u32(&lempty[as]), (use & 1u) ^ 1u, kErrEmptyWait)) break;
+                int ns = 0;
+                for (int hb = 0; hb < 2; ++hb) {
+                    const int m = 2 * mt + hb;
+                    if (m >= a.m_blocks) break;
+                    const int e0 = a.mt_ptr[m], e1 = a.mt_ptr[m + 1];
+                    for (int e = e0; e < e1 && ns < kPrSegs; ++e) {
+                        const int4 sg = a.mt_seg[e];
+                        const int r = min(a.rank[sg.x], a.R_max);
+                        if (r > 0)
+                            xlist[as * kPrSegs + ns++] =
+                                make_int4(sg.x, sg.y + kPrBM * hb, sg.z + kPrBM * hb, (r + 15) >> 4);
+                    }
+                }
+                xcount[as] = ns;
+                mbar_arrive(smem_u32(&lfull[as]));
             }
         }
         __syncwarp();

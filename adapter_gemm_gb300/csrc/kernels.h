@@ -143,6 +143,35 @@ cudaError_t launch_shrink(const ShrinkMaps& maps, const ShrinkArgs& a, int grid_
 // K slices per shrink stage for units of up to xrows rows (two stages fit the ring).
 int shrink_kk(int xrows, int R16, int K);
 cudaError_t launch_skinny(const SkinnyMaps& maps, const SkinnyArgs& a, bool pdl, int num_sms, cudaStream_t stream);
+// Expand steps of the prefill GEMMs. A stage holds the tile's U rows (hi and
+// lo, 4 KB each) and the B_s tiles (16 ranks of a slot's weight rows) of
+// wide_xslots consecutive slots, which one TMA copy brings in: as many as fit,
+// at most 8 (a tile crosses a few slots; the rest of a copy is read for
+// nothing).
+constexpr int wide_xslots(uint32_t stage_bytes, uint32_t slot_tile_bytes) {
+    return (int)((stage_bytes - 2u * 4096u) / slot_tile_bytes) > 8 ? 8
+                                                                   : (int)((stage_bytes - 2u * 4096u) / slot_tile_bytes);
+}
+
+#ifdef __CUDACC__
+// A tile's adapter segments (slot, first row, end row, 16-rank steps), in
+// slot order, grouped into expand stages: per 16-rank step ks, a stage takes
+// the segments from q0 on whose slot lies in [first, first + nslots), `first`
+// the slot of the first segment from q0 on that reaches step ks (the ones
+// that do not reach it are skipped). Sets q0 to that segment, q_end past the
+// stage's segments and `first`; false when no segment from q0 on reaches ks.
+__device__ __forceinline__ bool expand_window(const int4* list, int ns, int ks, int nslots, int& q0, int& q_end,
+                                              int& first) {
+    while (q0 < ns && list[q0].w <= ks) ++q0;
+    if (q0 >= ns) return false;
+    first = list[q0].x;
+    int q = q0 + 1;
+    while (q < ns && list[q].x < first + nslots) ++q;
+    q_end = q;
+    return true;
+}
+#endif
+
 cudaError_t launch_wide(const WideMaps& maps, const WideArgs& a, bool pdl, int grid, cudaStream_t stream);
 // The prefill GEMM on CTA pairs (a.pair; grid = 2 x pairs, clusters of 2), and
 // how many pairs can be resident at once.
