@@ -523,6 +523,43 @@ bool pool_overlaps(const Range& prev, const lora_pool* pool, int d_in, int d_out
            overlaps(prev, pool->rank, (size_t)pool->S * 4) || overlaps(prev, pool->scale, (size_t)pool->S * 4);
 }
 
+// The prefill GEMM's tiles for T rows and d_out outputs: 128 x 256, or 128 x
+// 128 for mid-sized grids (fewer than two waves of wide tiles) when the narrow
+// tiles finish sooner. A tile's time is set by its operand stream, (128 +
+// width) rows per K slice, so a wide tile costs 1.5 narrow ones: waves x 2
+// against waves x 3 in half-narrow-tile units, ties to the wide tile.
+// Measured alone: T = 512 with 4096 outputs runs faster narrow (33.7 against
+// 41.2 us); wide wins at T = 512 with 14336 outputs (65.5 against 69.6 us), T
+// = 1500 with 4096 (57.3 against 59.4) and T = 4096 with 1288 (55.3 against
+// 57.3). Depends on the shape only.
+// Batches of 2048 rows or more run their wide tiles on CTA pairs: 256 x 256
+// tiles, one M = 256 MMA over the two SMs of a cluster, each CTA streaming
+// 128 rows of x and 128 of W per K slice (384 rows for the same tensor work
+// unpaired), two K slices per stage in one copy per operand: fewer TMA copies
+// per MMA, which keeps the tensor cores fed. Measured alone, T = 4096 (us,
+// unpaired / pairs with one slice per stage / two): 4096 -> 14336: 299.5 /
+// 287.5 / 275.4; 14336 -> 4096: 335.5 / 320.5 / 309.1; 4096 -> 4096: 107.6 /
+// 111.2 / 109.8, and with the expand lists built ahead (warp 3) skewed_prefill
+// steps at 128.1 against 130.7 unpaired. A 256-row tile crosses twice the
+// adapter segments of a 128-row one, each with its own B_s copies, so batches
+// with few rows per adapter (T below 2048) stay unpaired: the layer sweep at T
+// = 512 measured 433.7 us per step paired.
+struct WideChoice {
+    int bn;           // output tile width
+    int max_pairs;    // > 0: CTA pairs, this many resident at once
+};
+
+WideChoice wide_choice(int T, int d_out) {
+    const int m_blocks = (T + 127) / 128;
+    const int sms = num_sms();
+    const int t256 = m_blocks * ((d_out + 255) / 256), t128 = m_blocks * ((d_out + 127) / 128);
+    const int cost256 = 3 * ((t256 + sms - 1) / sms), cost128 = 2 * ((t128 + sms - 1) / sms);
+    WideChoice c;
+    c.bn = (t256 < 2 * sms && cost128 < cost256) ? 128 : 256;
+    c.max_pairs = (c.bn == 256 && T >= 2048) ? wide_max_pairs() : 0;
+    return c;
+}
+
 // How a planned call of these sizes runs its low-rank terms: the expand
 // mode of the decode GEMM and the shrink kernel's units and split. A
 // base-only call with the pool computes the same, so that its GEMM splits K
@@ -799,38 +836,14 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
         if (counted(launch_skinny(maps, a, pdl, num_sms(), st)) != cudaSuccess) return LORA_ECUDA;
     } else {
         const void* A = plan ? plan->x_sorted : x;
-        // 128 x 256 output tiles, or 128 x 128 for mid-sized grids (fewer
-        // than two waves of wide tiles) when the narrow tiles finish sooner.
-        // A tile's time is set by its operand stream, (128 + width) rows per K
-        // slice, so a wide tile costs 1.5 narrow ones: waves x 2 against
-        // waves x 3 in half-narrow-tile units, ties to the wide tile. Measured
-        // alone: T = 512 with 4096 outputs runs faster narrow (33.7 against
-        // 41.2 us); wide wins at T = 512 with 14336 outputs (65.5 against 69.6
-        // us), T = 1500 with 4096 (57.3 against 59.4) and T = 4096 with 1288
-        // (55.3 against 57.3). Depends on the shape only.
         const int m_blocks = (T + 127) / 128;
         const int sms = num_sms();
-        const int t256 = m_blocks * ((d_out + 255) / 256), t128 = m_blocks * ((d_out + 127) / 128);
-        const int cost256 = 3 * ((t256 + sms - 1) / sms), cost128 = 2 * ((t128 + sms - 1) / sms);
-        const int bn = (t256 < 2 * sms && cost128 < cost256) ? 128 : 256;
-        // narrow tiles take two K slices per stage (3-D views; x and the
-        // plan-ordered copy of x are [T][d_in], W is [d_out][d_in]), so that a
-        // stage's copies are as large as a wide tile's
-        // Long GEMMs (d_in or d_out of 8192 or more) run their wide tiles on
-        // CTA pairs: 256 x 256 tiles, one M = 256 MMA over the two SMs of a
-        // cluster, each CTA streaming 128 rows of x and 128 of W per K slice
-        // (384 rows for the same tensor work unpaired), two K slices per stage
-        // in one copy per operand: fewer TMA copies per MMA, which keeps the
-        // tensor cores fed. Measured alone, T = 4096 (us, unpaired / pairs
-        // with one slice per stage / two): 4096 -> 14336: 299.5 / 287.5 /
-        // 275.4; 14336 -> 4096: 335.5 / 320.5 / 309.1; 4096 -> 4096: 107.6 /
-        // 111.2 / 109.8 (so those stay unpaired). A 256-row tile crosses twice
-        // the adapter segments of a 128-row one, each with its own B_s copies,
-        // so batches with few rows per adapter (T below 2048) stay unpaired:
-        // the layer sweep at T = 512 measured 433.7 us per step paired.
-        const int max_pairs =
-            (bn == 256 && T >= 2048 && (d_in >= 8192 || d_out >= 8192)) ? wide_max_pairs() : 0;
+        const WideChoice wc = wide_choice(T, d_out);
+        const int bn = wc.bn, max_pairs = wc.max_pairs;
         const bool pair = max_pairs > 0;
+        // narrow tiles and pairs take two K slices per stage (3-D views; x and
+        // the plan-ordered copy of x are [T][d_in], W is [d_out][d_in]), so
+        // that a stage's copies are as large as they can be
         const int kk = ((bn == 128 || pair) && d_in % 64 == 0 && d_in >= 128) ? 2 : 1;
         const int m_tiles = pair ? (T + 255) / 256 : m_blocks;
         const int units = pair ? max_pairs : sms;        // tiles that run at once
@@ -919,6 +932,12 @@ lora_status linear_impl(const void* x, const void* W, int T, int d_in, int d_out
 }
 
 }  // namespace
+
+int lora_linear_kernel_for(int T, int d_in, int d_out, int S, int R_max) {
+    if (T < 1 || d_in < 8 || d_out < 8) return -1;
+    if (lora_linear_path_for(T, d_in, d_out, S, R_max) == 0) return 0;
+    return wide_choice(T, d_out).max_pairs > 0 ? 2 : 1;
+}
 
 lora_status lora_linear(const void* x, const void* W, int T, int d_in, int d_out, const lora_pool* pool,
                         const lora_plan_t* plan, void* y, void* stream) {

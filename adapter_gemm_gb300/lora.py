@@ -66,6 +66,7 @@ _SIGS = {
                              ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p]),
     "lora_linear_path": (_c_int, [_c_int, _c_int, _c_int]),
     "lora_linear_path_for": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int]),
+    "lora_linear_kernel_for": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int]),
     "lora_linear_rows": (_c_int, [_c_void_p, _c_int, _c_void_p, _c_int, _c_int, _c_int, _c_void_p,
                                   ctypes.POINTER(lora_pool), ctypes.POINTER(lora_plan_t), _c_void_p, _c_void_p,
                                   _c_void_p]),
@@ -148,6 +149,13 @@ def linear_path(T: int, d_in: int, d_out: int, pool: "Pool | None" = None) -> in
     if pool is not None:
         return _lib().lora_linear_path_for(T, d_in, d_out, pool.S, pool.R_max)
     return _lib().lora_linear_path(T, d_in, d_out)
+
+
+def kernel_for(T: int, d_in: int, d_out: int, pool: "Pool | None" = None) -> int:
+    """Kernel a call runs: 0 skinny (decode), 1 wide (prefill), 2 wide on CTA
+    pairs; with a pool, for its S and R_max."""
+    S, R = (pool.S, pool.R_max) if pool is not None else (0, 0)
+    return _lib().lora_linear_kernel_for(T, d_in, d_out, S, R)
 
 
 def plan_workspace_bytes(T: int, S: int, R_max: int, d_in_cap: int) -> int:

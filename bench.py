@@ -490,15 +490,8 @@ class Runner:
             achieved, peak, unit = work.bytes / t_k / 1e9, hbm, "GB/s"
         else:
             achieved, peak, unit = work.flops / t_k / 1e12, tf_burst, "TFLOP/s"
-        # the library's choice: the decode GEMM, else the prefill GEMM, on CTA
-        # pairs for long projections (d_in or d_out of 8192 or more) of
-        # batches of 2048 rows or more
-        if L.linear_path(T, td.d_in, n_dom, self.copies[0][j][1][0]) == 0:
-            kname = "gemm_skinny_kernel"
-        elif T >= 2048 and (td.d_in >= 8192 or n_dom >= 8192):
-            kname = "gemm_wide_pair_kernel"
-        else:
-            kname = "gemm_wide_kernel"
+        kname = ("gemm_skinny_kernel", "gemm_wide_kernel", "gemm_wide_pair_kernel")[
+            L.kernel_for(T, td.d_in, n_dom, self.copies[0][j][1][0])]
         if all_kernels:
             kname = f"all {self.u_launch[j]} kernels of the per-slice calls"
         roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,

@@ -214,9 +214,8 @@ lora_status lora_linear_host(const void* x_host, const int32_t* ids_host, void* 
 
 /* The kernel family lora_linear picks for these sizes on the current device
  * without a pool: 0 = skinny (swap-AB, split-K across a thread-block
- * cluster), 1 = wide (persistent 128x256 tiles; for 2048 rows or more with
- * d_in or d_out of 8192 or more, 256x256 tiles shared by the two CTAs of a
- * cluster). Up to 256 rows always 0,
+ * cluster), 1 = wide (persistent 128x256 tiles, on CTA pairs for large
+ * batches: lora_linear_kernel_for). Up to 256 rows always 0,
  * above 640 always 1; in between 0 while the skinny kernel's weight tiles can
  * split K in two on every SM. */
 int lora_linear_path(int T, int d_in, int d_out);
@@ -229,6 +228,14 @@ int lora_linear_path(int T, int d_in, int d_out);
  * above 560 rows, takes the wide kernel, whose expand does not grow with the
  * pool. S < 2 or R_max < 1: as lora_linear_path. */
 int lora_linear_path_for(int T, int d_in, int d_out, int S, int R_max);
+
+/* The kernel lora_linear runs for a call of these sizes with a pool of S
+ * slots and rank cap R_max on the current device: 0 = skinny, 1 = wide, 2 =
+ * wide on CTA pairs (256x256 tiles shared by the two CTAs of a cluster, for
+ * batches of 2048 rows or more with 256-wide tiles). S < 2 or R_max < 1: as
+ * without a pool. -1 for sizes lora_linear refuses (T < 1, d_in or d_out below
+ * 8). */
+int lora_linear_kernel_for(int T, int d_in, int d_out, int S, int R_max);
 
 /* Most output slices one lora_linear_sliced call takes. */
 #define LORA_MAX_SLICES 4

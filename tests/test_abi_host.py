@@ -198,3 +198,12 @@ def test_path_choice(lib):
     assert lib.lora_linear_path_for(256, 4096, 4096, 1024, 128) == 0  # decode-sized: no x_sorted
     assert lib.lora_linear_path_for(512, 4096, 4096, 51, 16) == 0    # the layer sweep's pools (50 chunks)
     assert lib.lora_linear_path_for(300, 512, 512, 1, 64) == lib.lora_linear_path(300, 512, 512)
+    # the kernel query: 0 wherever the decode kernel runs, the prefill kernel
+    # (1, or 2 on CTA pairs where a device offers them) elsewhere, -1 for sizes
+    # the layer refuses
+    assert lib.lora_linear_kernel_for(64, 4096, 4096, 9, 16) == 0
+    assert lib.lora_linear_kernel_for(512, 4096, 4096, 51, 16) == 0
+    assert lib.lora_linear_kernel_for(300, 512, 512, 33, 64) in (1, 2)
+    assert lib.lora_linear_kernel_for(4096, 4096, 14336, 51, 16) in (1, 2)
+    assert lib.lora_linear_kernel_for(0, 4096, 4096, 9, 16) == -1
+    assert lib.lora_linear_kernel_for(64, 4, 4096, 9, 16) == -1
