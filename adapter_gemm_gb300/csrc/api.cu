@@ -637,10 +637,11 @@ CallShape call_shape(int T, int d_in, int d_out, const lora_pool* pool, bool sli
     c.shrink_ks = shrink_splits(c.grid_x, d_in);
     // A few rows of several slots (by-slot units of one or two rows each):
     // each unit's K loop is short, and its CTAs only take SMs from this
-    // call's GEMM, which starts beside it. Measured per chained layer
-    // sweep step at T = 8 (8 units), split 8 / 4 / 2 / 1: 155.2 / 150.1 /
-    // 148.3 / 182.3 us (T = 1 and T = 64 unchanged by the rule).
-    if (c.by_slot && c.grid_x >= 2 && T <= 16 && c.shrink_ks > 2) c.shrink_ks = 2;
+    // call's GEMM, which starts beside it (and keeps to the SMs they leave,
+    // below). Measured per chained layer sweep step at T = 8 (8 units),
+    // split 8 / 4 / 2: 155.9 / 147.6 / 149.2 us (T = 1 and T = 64 unchanged
+    // by the rule).
+    if (c.by_slot && c.grid_x >= 2 && T <= 16 && c.shrink_ks > 4) c.shrink_ks = 4;
     // The decode GEMM starts its K loop beside the by-slot shrink kernel and
     // holds one SM per CTA: its K split keeps to the SMs the shrink leaves,
     // so that no GEMM CTA waits for a shrink CTA to finish. Measured per
