@@ -1,5 +1,5 @@
-// The prefill GEMM of gemm_wide.cu on CTA pairs, for long projections (d_in
-// or d_out of 8192 or more): the two CTAs of a cluster share each 256 x 256
+// The prefill GEMM of gemm_wide.cu on CTA pairs, for the 256-wide tiles of
+// batches of 2048 rows or more: the two CTAs of a cluster share each 256 x 256
 // output tile through one tcgen05 MMA of M = 256 (cta_group::2), issued by the
 // leader (rank 0):
 //   - CTA rank r holds rows [128 r, 128 r + 128) of the tile's x rows and
@@ -16,9 +16,10 @@
 //
 // Everything else is the unpaired kernel's: x_sorted rows in plan order, the
 // expand steps per adapter segment as lane-masked MMAs (the mask now covers
-// the pair's 256 rows), the epilogue that scatters each row to its token, the
-// split of a short last wave into half-width tiles (256 x 128: 64 weight rows
-// per CTA), bounded waits that report through the error word.
+// the pair's 256 rows; the segment lists built ahead by warp 3, the B_s rows
+// of consecutive slots in one copy), the epilogue that scatters each row to
+// its token, the split of a short last wave into half-width tiles (256 x 128:
+// 64 weight rows per CTA), bounded waits that report through the error word.
 #include <cstdint>
 #include "ptx.cuh"
 #include "kernels.h"
