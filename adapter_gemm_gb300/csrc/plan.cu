@@ -35,6 +35,7 @@
 namespace lora {
 
 constexpr int kPlanMaxThreads = 1024;
+constexpr int kPlanHeldRounds = 8;      // 32-row rounds of a warp whose ids stay in registers
 constexpr int kPlanMaxWarps = kPlanMaxThreads / 32;
 
 // Threads of the plan CTA for T rows and S slots: a multiple of 32, at least
@@ -100,12 +101,28 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     // Rows [lo, hi) of this warp; chunk is a multiple of 32.
     const int chunk = ((T + NW * 32 - 1) / (NW * 32)) * 32;
     const int lo = min(T, warp * chunk), hi = min(T, lo + chunk);
+    // The warp's first kPlanHeldRounds rounds of ids, loaded at once (one
+    // memory latency instead of one per round) and kept for both passes.
+    int held[kPlanHeldRounds];
+#pragma unroll
+    for (int r = 0; r < kPlanHeldRounds; ++r) {
+        const int t = lo + 32 * r + lane;
+        held[r] = t < hi ? ids[t] : 0;
+    }
+    auto id_of = [&](int base, int t) -> int {
+        const int r = (base - lo) >> 5;
+        int v = 0;
+#pragma unroll
+        for (int q = 0; q < kPlanHeldRounds; ++q)
+            if (q == r) v = held[q];
+        return r < kPlanHeldRounds ? v : ids[t];
+    };
 
     int n_bad = 0;
     for (int base = lo; base < hi; base += 32) {
         const int t = base + lane;
         const bool valid = t < hi;
-        int s = valid ? ids[t] : 0;
+        int s = valid ? id_of(base, t) : 0;
         if (valid && (s < 0 || s >= S)) { ++n_bad; s = 0; }
         const int key = valid ? s : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, key);
@@ -143,7 +160,7 @@ plan_kernel(const int32_t* __restrict__ ids, int T, PlanArgs p) {
     for (int base = lo; base < hi; base += 32) {
         const int t = base + lane;
         const bool valid = t < hi;
-        int s = valid ? ids[t] : 0;
+        int s = valid ? id_of(base, t) : 0;
         if (valid && (s < 0 || s >= S)) s = 0;
         if (valid) slot_out[t] = s;
         const int key = valid ? s : -1;
