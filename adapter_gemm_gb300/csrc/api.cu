@@ -228,6 +228,11 @@ SkinnyConfig skinny_config(int T, int K, int N, int mode, int R_max, int S, int 
     const bool fuse = mode == 2, tce = mode == 2 || mode == 3;   // Bcat and the token tables beside the pipeline
     const int a_rows = fuse ? (S - 1) * R_max : 0;
     c.kk = skinny_kk(c.TN, fuse, tce, a_rows, K);
+    // A single token: W alone streams, and two slices per stage (five stages
+    // in flight instead of two) keep more of it in flight. Measured per
+    // chained layer sweep step at T = 1: 119.9 -> 118.8 us; at T = 8 the same
+    // tiles measured slower (146.5 -> 152.1), so only T = 1 takes it.
+    if (T == 1 && c.kk > 2) c.kk = 2;
     c.stages = skinny_stages(c.TN, fuse, tce, c.kk);
     c.stage_u = (mode == 1 && R_max <= kStageURank &&
                  skinny_epi_bytes(c.TN, R_max, true, false, false) + 2048 <= (size_t)200 * 1024) ? 1 : 0;
